@@ -1,0 +1,420 @@
+"""Benchmark: paged MLA decode step on GB300 (one JSON line on rank 0).
+
+A step is one pass of the hot path over one batch: the cache write of the step's new
+tokens (B * s_q rows) followed by mla_decode (split scheduler, split-KV decode, LSE
+combine). The default workload is the ragged-batch configuration (B=128, s_q=1, H=16,
+page 64, seq_lens ~ U[2048, 6144], bf16 cache); --config picks another.
+
+value      decode TFLOP/s of the whole job (algorithmic flops 2*(576+512) per visible
+           (row, head, key), summed over ranks) with inputs resident in HBM
+e2e        the same metric through the public API with pinned host buffers: every step
+           copies q, the new latent/rope rows, slot mapping, block table and seq_lens in
+           and reads out / lse back inside the timed region
+roofline   the decode call (scheduler + decode + combine, timed with CUDA events on its
+           stream) against the measured HBM copy bandwidth or bf16 tensor peak
+cpu_baseline  the float64 oracle on a bounded sample of the same workload
+
+--impl reference times the oracle itself (the only reference this method has) as the
+reference arm. Multi-GPU: one process per GPU (torchrun), each rank an independent
+replica with its own sequences (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode TFLOP/s and KV GB/s (bf16 & FP8 KV) at 1 GB300; % of roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--kv", default=None, choices=[None, "bf16", "fp8"])
+    ap.add_argument("--s_q", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def make_case(args, rank: int):
+    from mla_paged_decode_02_gb300 import synth
+    kv = None if args.kv is None else (synth.KV_BF16 if args.kv == "bf16" else synth.KV_FP8_E4M3)
+    case = synth.make_config(args.config, kv_dtype=kv, s_q=args.s_q)
+    if rank:
+        kw = dict(synth.CONFIGS[args.config])
+        kw.pop("name")
+        if kv is not None:
+            kw["kv_dtype"] = kv
+        if args.s_q is not None:
+            kw["s_q"] = args.s_q
+        case = synth.make_case(seed=synth.SEED_OF[args.config] + 7919 * rank, name=case.name, **kw)
+    return case
+
+
+def algorithmic(case):
+    """Algorithmic flops and bytes of one decode call: 2*(576+512) flops per visible
+    (row, head, key); every cache row read once; q read once; out and lse written once."""
+    tot = 0
+    for L in case.seq_lens:
+        for i in range(case.s_q):
+            tot += (int(L) - case.s_q + 1 + i) if case.causal else int(L)
+    flops = 2.0 * (576 + 512) * case.H * tot
+    elem = 2 if case.kv_dtype == 0 else 1
+    kv_bytes = float(np.sum(case.seq_lens.astype(np.int64))) * 576 * elem
+    q_bytes = case.B * case.s_q * case.H * 576 * 2.0
+    out_bytes = case.B * case.s_q * case.H * (512 * 2 + 4.0)
+    return flops, kv_bytes, q_bytes, out_bytes
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_paged_decode_02_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """dram bytes per decode launch from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    e = d.get("workloads", {}).get(workload)
+    return None if e is None else float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, enabled: bool):
+        self.proc = None
+        self.index = index
+        if enabled:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                     "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except (OSError, ValueError):
+                self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+    from mla_paged_decode_02_gb300 import api
+    from mla_paged_decode_02_gb300.workload import DeviceWorkload as GpuCase, bits_to_torch_bf16
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    case = make_case(args, rank)
+    g = GpuCase(case, device=device)
+    flops, kv_bytes, q_bytes, out_bytes = algorithmic(case)
+    stream = torch.cuda.current_stream()
+
+    # the step's new tokens: each sequence's last s_q rows (re-written with the same values)
+    step_idx = case.step_tokens()
+    lat_d = bits_to_torch_bf16(case.latent_bits[step_idx], device)
+    rope_d = bits_to_torch_bf16(case.rope_bits[step_idx], device)
+    slots_d = torch.from_numpy(case.slot_mapping[step_idx]).to(device)
+    out = torch.empty((case.B, case.s_q, case.H, 512), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((case.B, case.s_q, case.H), dtype=torch.float32, device=device)
+
+    def step():
+        api.cache_write(lat_d, rope_d, slots_d, g.cache, g.kv_scale)
+        api.decode(g.q, g.cache, g.block_table, g.seq_lens, case.softmax_scale, g.kv_scale,
+                   max_seq_len=case.max_seq_len, causal=case.causal, out=out, lse=lse,
+                   workspace=g.workspace)
+
+    l2_flush = kv_bytes < 3 * 129e6
+    flush_buf = torch.empty(int(512e6), dtype=torch.uint8, device=device) if l2_flush else None
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, bits = api.decode_check(g.workspace)
+    if st != 0:
+        raise RuntimeError(f"device error word after warm-up: status {st} bits {bits:#x}")
+
+    # ---- device-resident timing: K steps, also the decode call alone per step
+    clocks = ClockSampler(local_rank, not args.no_clocks)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for k in range(args.steps):
+        if flush_buf is not None:
+            flush_buf.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        api.cache_write(lat_d, rope_d, slots_d, g.cache, g.kv_scale)
+        dec[k][0].record(stream)
+        api.decode(g.q, g.cache, g.block_table, g.seq_lens, case.softmax_scale, g.kv_scale,
+                   max_seq_len=case.max_seq_len, causal=case.causal, out=out, lse=lse,
+                   workspace=g.workspace)
+        dec[k][1].record(stream)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = sum(a.elapsed_time(b) for a, b in ev)
+    dec_ms = sum(a.elapsed_time(b) for a, b in dec) / args.steps
+    step_ms_max = max_over_ranks(step_ms, world, device)
+    ms_per_step = step_ms_max / args.steps
+    total_flops = sum_over_ranks(flops, world, device)
+    value = total_flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end-to-end through the public API with pinned host buffers
+    h_q = torch.from_numpy(case.q_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_lat = lat_d.cpu().pin_memory()
+    h_rope = rope_d.cpu().pin_memory()
+    h_slots = slots_d.cpu().pin_memory()
+    h_bt = torch.from_numpy(case.block_table).pin_memory()
+    h_sl = torch.from_numpy(case.seq_lens).pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q, d_bt, d_sl = torch.empty_like(g.q), torch.empty_like(g.block_table), torch.empty_like(g.seq_lens)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_lat, h_rope, h_slots, h_bt, h_sl))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        lat_d.copy_(h_lat, non_blocking=True)
+        rope_d.copy_(h_rope, non_blocking=True)
+        slots_d.copy_(h_slots, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        api.cache_write(lat_d, rope_d, slots_d, g.cache, g.kv_scale)
+        api.decode(d_q, g.cache, d_bt, d_sl, case.softmax_scale, g.kv_scale,
+                   max_seq_len=case.max_seq_len, causal=case.causal, out=out, lse=lse,
+                   workspace=g.workspace)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device) / args.steps
+    e2e_value = total_flops / (e2e_ms * 1e-3) / 1e12
+
+    # ---- roofline of the decode call
+    peaks, peak_kind = load_peaks()
+    t = dec_ms * 1e-3
+    hbm_t = (kv_bytes + q_bytes) / (peaks["hbm_gbs"] * 1e9)
+    tc_t = flops / (peaks["bf16_tflops"] * 1e12)
+    if hbm_t >= tc_t:
+        roof = {"bound": "hbm", "achieved": (kv_bytes + q_bytes) / t / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = ncu_traffic(case.name)
+    roof["peak_source"] = f"{peak_kind} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops'})"
+    roof["t_roof_us"] = max(hbm_t, tc_t) * 1e6
+    roof["decode_call_us"] = dec_ms * 1e3
+    roof["kernel_timed"] = "mla_decode call: schedule + decode + combine kernels"
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": case.name, "B": case.B, "s_q": case.s_q, "H": case.H,
+                   "page_size": case.page_size, "kv": "fp8_e4m3" if case.kv_dtype else "bf16",
+                   "tokens": int(case.seq_lens.sum()), "parallelism": f"dp{world} (replicas)",
+                   "l2": "flushed between steps" if l2_flush else "inputs larger than L2"},
+        "kv_gbs": round(kv_bytes / (dec_ms * 1e-3) / 1e9, 1),
+        "decode_tflops": round(flops / (dec_ms * 1e-3) / 1e12, 3),
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 5)},
+        "roofline": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in roof.items()},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+    }
+    return line, case
+
+
+def cpu_baseline(case, budget_s: float = 15.0):
+    """The oracle as it stands on this host's cores, over a bounded sample of sequences."""
+    from oracle import mla_oracle as O
+    cache = O.cache_write(case.empty_cache(), case.latent_bits, case.rope_bits, case.slot_mapping,
+                          case.page_size, case.kv_dtype, case.kv_scale)
+    done_flops, t_used, nb = 0.0, 0.0, 0
+    order = list(range(case.B))
+    t_start = time.perf_counter()
+    for b in order:
+        rows = [(b, i, h) for i in range(case.s_q) for h in range(case.H)]
+        t0 = time.perf_counter()
+        O.mla_decode(case.q_bits, cache, case.block_table, case.seq_lens, case.page_size,
+                     case.softmax_scale, case.kv_dtype, case.kv_scale, case.causal, rows=rows)
+        t_used += time.perf_counter() - t0
+        done_flops += O.flops([case.seq_lens[b]], case.s_q, case.H, case.causal)
+        nb += 1
+        if time.perf_counter() - t_start > budget_s:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": done_flops / t_used / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{nb} of {case.B} sequences of {case.name} (all s_q*H rows each), "
+                      f"float64 numpy, {t_used:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the float64 oracle, timed on the host cores, rank 0 only."""
+    if rank != 0:
+        return None
+    from oracle import mla_oracle as O
+    case = make_case(args, 0)
+    cache = O.cache_write(case.empty_cache(), case.latent_bits, case.rope_bits, case.slot_mapping,
+                          case.page_size, case.kv_dtype, case.kv_scale)
+    per_step = max(1, min(case.B, 2))
+
+    def step(k):
+        bs = [(k * per_step + j) % case.B for j in range(per_step)]
+        rows = [(b, i, h) for b in bs for i in range(case.s_q) for h in range(case.H)]
+        O.mla_decode(case.q_bits, cache, case.block_table, case.seq_lens, case.page_size,
+                     case.softmax_scale, case.kv_dtype, case.kv_scale, case.causal, rows=rows)
+        return sum(O.flops([case.seq_lens[b]], case.s_q, case.H, case.causal) for b in bs)
+
+    for k in range(args.warmup):
+        step(k)
+    fl, t0 = 0.0, time.perf_counter()
+    for k in range(args.steps):
+        fl += step(args.warmup + k)
+    dt = time.perf_counter() - t0
+    value = fl / dt / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": case.name},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} sequences of {case.name} per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+    else:
+        line, case = run_ours(args, rank, local_rank, world)
+        if rank == 0:
+            if not args.no_cpu_baseline and world == 1:
+                line["cpu_baseline"] = cpu_baseline(case)
+            print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,260 @@
+// mla_api.cu — the C ABI (include/mla.h): argument checks, workspace layout, TMA
+// descriptors and the launch sequence  schedule -> decode -> combine  on one stream.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <cudaTypedefs.h>
+#include "mla_internal.h"
+#include "../../include/mla.h"
+
+#define MLA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace mla {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::atomic<int> g_num_sms[kMaxDevices];
+std::atomic<uint32_t> g_prepared[kMaxDevices];   // bit per decode variant
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int variant_bit(int rc, bool fp8) {
+  return (rc == 16 ? 0 : rc == 32 ? 2 : 4) + (fp8 ? 1 : 0);
+}
+
+cudaError_t current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return e;
+  if (*dev < 0 || *dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  return cudaSuccess;
+}
+
+int sm_count(int dev) {
+  int n = g_num_sms[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return -1;
+  g_num_sms[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+bool get_encoder() {
+  if (g_encode) return true;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+mla_status check_params(const mla_decode_params* p) {
+  if (p == nullptr) return MLA_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->s_q < 1 || p->num_heads < 1 || p->page_size < 1 || p->num_pages < 1 ||
+      p->max_blocks_per_seq < 1 || p->max_seq_len < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (p->kv_dtype != MLA_KV_BF16 && p->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (p->causal != 0 && p->causal != 1) return MLA_ERR_INVALID_ARG;
+  if (p->max_seq_len < p->s_q) return MLA_ERR_INVALID_ARG;
+  if (p->page_size % 64 != 0 || p->page_size > 1024) return MLA_ERR_UNSUPPORTED;
+  if (p->s_q > 64 || (int64_t)p->s_q * p->num_heads > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (p->batch > kMaxBatch || p->max_seq_len > kMaxSeqLen) return MLA_ERR_UNSUPPORTED;
+  if ((int64_t)p->num_pages * p->page_size >= (int64_t)1 << 31) return MLA_ERR_UNSUPPORTED;
+  if ((int64_t)p->max_blocks_per_seq * p->page_size < p->s_q) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+bool encode_kv_map(CUtensorMap* m, const void* cache, int64_t rows, bool fp8) {
+  cuuint64_t dims[2] = {(cuuint64_t)kDQK, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kDQK * (fp8 ? 1 : 2)};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(cache), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_q_map(CUtensorMap* m, const void* q, int B, int R, int rc) {
+  cuuint64_t dims[3] = {(cuuint64_t)kDQK, (cuuint64_t)R, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)kDQK * 2, (cuuint64_t)kDQK * 2 * R};
+  cuuint32_t box[3] = {64, (cuuint32_t)rc, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+MLA_EXPORT int32_t mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+MLA_EXPORT const char* mla_status_string(int32_t s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MLA_ERR_CUDA: return "CUDA runtime error";
+    case MLA_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case MLA_ERR_DEVICE_INDEX: return "device-side index or length out of range";
+    default: return "unknown status";
+  }
+}
+
+MLA_EXPORT size_t mla_decode_workspace_size(const mla_decode_params* p, int32_t num_sms) {
+  if (check_params(p) != MLA_OK) return 0;
+  if (num_sms <= 0) {
+    int dev;
+    if (current_device(&dev) != cudaSuccess) return 0;
+    num_sms = sm_count(dev);
+    if (num_sms <= 0) return 0;
+  }
+  const int R = p->s_q * p->num_heads;
+  return ws_layout(p->batch, R, p->max_seq_len, num_sms).total;
+}
+
+MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, const void* kv_cache,
+                                 const int32_t* block_table, const int32_t* seq_lens,
+                                 float softmax_scale, const float* kv_scale, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  mla_status st = check_params(p);
+  if (st != MLA_OK) return st;
+  const bool fp8 = p->kv_dtype == MLA_KV_FP8_E4M3;
+  if (!q || !kv_cache || !block_table || !seq_lens || !out || !lse || !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (fp8 && !kv_scale) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(workspace, 256))
+    return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale == softmax_scale) || softmax_scale > 3.0e38f || softmax_scale < -3.0e38f)
+    return MLA_ERR_INVALID_ARG;
+
+  int dev;
+  if (current_device(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  const int nsm = sm_count(dev);
+  if (nsm <= 0) return MLA_ERR_CUDA;
+  const int B = p->batch, R = p->s_q * p->num_heads;
+  const int rc = rows_per_group(R);
+  const int G = (R + rc - 1) / rc;
+  const WsLayout w = ws_layout(B, R, p->max_seq_len, nsm);
+  if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (!get_encoder()) return MLA_ERR_CUDA;
+
+  const uint32_t bit = 1u << variant_bit(rc, fp8);
+  if (!(g_prepared[dev].load() & bit)) {
+    if (decode_prepare(rc, fp8) != cudaSuccess) return MLA_ERR_CUDA;
+    g_prepared[dev].fetch_or(bit);
+  }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* hdr = reinterpret_cast<uint32_t*>(ws);
+  int4* batch_info = reinterpret_cast<int4*>(ws + w.batch_off);
+  int32_t* split_list = reinterpret_cast<int32_t*>(ws + w.split_off);
+  int4* items = reinterpret_cast<int4*>(ws + w.items_off);
+  int4* units = reinterpret_cast<int4*>(ws + w.units_off);
+  float* plse = reinterpret_cast<float*>(ws + w.plse_off);
+  float* po = reinterpret_cast<float*>(ws + w.po_off);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  SchedArgs sa{};
+  sa.seq_lens = seq_lens;
+  sa.hdr = hdr;
+  sa.batch_info = batch_info;
+  sa.split_list = split_list;
+  sa.items_tmp = items;
+  sa.units = units;
+  sa.B = B;
+  sa.s_q = p->s_q;
+  sa.G = G;
+  const int64_t cap = (int64_t)p->max_blocks_per_seq * p->page_size;
+  sa.max_len = (int)(cap < p->max_seq_len ? cap : p->max_seq_len);
+  sa.target_units = kUnitsPerSM * nsm;
+  sa.max_items = w.max_items;
+  sa.max_pslots = w.max_pslots;
+  if (launch_schedule(sa, s) != cudaSuccess) return MLA_ERR_CUDA;
+
+  DecodeArgs da;
+  std::memset(&da, 0, sizeof(da));
+  if (!encode_kv_map(&da.tm_kv, kv_cache, (int64_t)p->num_pages * p->page_size, fp8))
+    return MLA_ERR_INVALID_ARG;
+  if (!encode_q_map(&da.tm_q, q, B, R, rc)) return MLA_ERR_INVALID_ARG;
+  da.block_table = block_table;
+  da.batch_info = batch_info;
+  da.units = units;
+  da.hdr = hdr;
+  da.out = static_cast<__nv_bfloat16*>(out);
+  da.lse = lse;
+  da.part_o = po;
+  da.part_lse = plse;
+  da.err = hdr;
+  da.kv_scale = kv_scale;
+  da.s_q = p->s_q;
+  da.H = p->num_heads;
+  da.R = R;
+  da.P = p->page_size;
+  da.MB = p->max_blocks_per_seq;
+  da.num_pages = p->num_pages;
+  da.causal = p->causal;
+  da.softmax_scale = softmax_scale;
+  if (launch_decode(da, rc, fp8, nsm, s) != cudaSuccess) return MLA_ERR_CUDA;
+
+  CombineArgs ca{};
+  ca.hdr = hdr;
+  ca.batch_info = batch_info;
+  ca.split_list = split_list;
+  ca.part_o = po;
+  ca.part_lse = plse;
+  ca.out = static_cast<__nv_bfloat16*>(out);
+  ca.lse = lse;
+  ca.R = R;
+  if (launch_combine(ca, nsm, s) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+MLA_EXPORT mla_status mla_decode_check(const void* workspace, mla_stream_t stream, uint32_t* bits) {
+  if (workspace == nullptr) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MLA_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (bits) *bits = word;
+  if (word & MLA_DEVERR_TIMEOUT) return MLA_ERR_TIMEOUT;
+  if (word) return MLA_ERR_DEVICE_INDEX;
+  return MLA_OK;
+}
+
+MLA_EXPORT mla_status mla_cache_write(const void* latent, const void* rope,
+                                      const int64_t* slot_mapping, int32_t num_tokens,
+                                      void* kv_cache, int32_t num_pages, int32_t page_size,
+                                      int32_t kv_dtype, const float* kv_scale,
+                                      uint32_t* device_error, mla_stream_t stream) {
+  if (num_tokens < 0 || num_pages < 1 || page_size < 1) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  const bool fp8 = kv_dtype == MLA_KV_FP8_E4M3;
+  if (num_tokens == 0) return MLA_OK;
+  if (!latent || !rope || !slot_mapping || !kv_cache) return MLA_ERR_INVALID_ARG;
+  if (fp8 && !kv_scale) return MLA_ERR_INVALID_ARG;
+  if (!aligned(latent, 16) || !aligned(rope, 16) || !aligned(kv_cache, 16) ||
+      !aligned(slot_mapping, 8) || (device_error && !aligned(device_error, 4)))
+    return MLA_ERR_INVALID_ARG;
+  const int64_t total = (int64_t)num_pages * page_size;
+  if (launch_cache_write(latent, rope, slot_mapping, num_tokens, kv_cache, total, fp8, kv_scale,
+                         device_error, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}

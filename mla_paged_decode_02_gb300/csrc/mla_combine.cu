@@ -1,0 +1,66 @@
+// mla_combine.cu — merges the per-split partial outputs of split sequences.
+//
+// A sequence cut into key ranges (split-KV, flash-decoding) yields, per split s, the
+// normalised partial output O_s and its log-sum-exp lse_s. The exact merge is
+//   lse = log(sum_s exp(lse_s)),   out = sum_s exp(lse_s - lse) * O_s.
+// A split with no visible key for a row (possible for causal s_q > 1) carries
+// lse_s = -inf and weight 0.
+//
+// One warp per (split sequence, query row): lane l owns output columns [16l, 16l+16),
+// read as four float4 per split (coalesced 2 KB rows). Persistent grid-stride loop over
+// the task list the scheduler wrote, so nothing launches per sequence.
+#include "mla_internal.h"
+
+namespace mla {
+
+__global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t tasks = (int64_t)a.hdr[2] * a.R;
+  for (int64_t task = warp; task < tasks; task += nwarps) {
+    const int b = a.split_list[task / a.R];
+    const int r = (int)(task % a.R);
+    const int4 bi = a.batch_info[b];
+    const int ns = bi.x, base = bi.y;
+    float m = -INFINITY;
+    for (int s = 0; s < ns; ++s) m = fmaxf(m, a.part_lse[(int64_t)(base + s) * a.R + r]);
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    float wsum = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float ls = a.part_lse[(int64_t)(base + s) * a.R + r];
+      const float w = ls == -INFINITY ? 0.f : __expf(ls - m);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(
+          a.part_o + ((int64_t)(base + s) * a.R + r) * kDV) + lane * 4;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 v = src[k];
+        acc[4 * k + 0] += w * v.x;
+        acc[4 * k + 1] += w * v.y;
+        acc[4 * k + 2] += w * v.z;
+        acc[4 * k + 3] += w * v.w;
+      }
+    }
+    const float inv = 1.f / wsum;
+    uint32_t packed[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+      packed[k] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)b * a.R + r) * kDV) + lane * 2;
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    if (lane == 0) a.lse[(int64_t)b * a.R + r] = m + logf(wsum);
+  }
+}
+
+cudaError_t launch_combine(const CombineArgs& a, int grid, cudaStream_t s) {
+  combine_kernel<<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,110 @@
+// mla_internal.h — workspace layout and kernel argument blocks shared by the host API
+// (mla_api.cu) and the kernels. Not part of the public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace mla {
+
+constexpr int kDQK = 576;          // 512 latent + 64 rope
+constexpr int kDV = 512;
+constexpr int kTileTokens = 128;   // keys per tile: the M of the QK^T MMA (tokens on M)
+constexpr int kMaxSeqLen = 1 << 20;
+constexpr int kMaxRows = 4096;     // s_q * H
+constexpr int kMaxBatch = 1 << 16;
+constexpr int kUnitsPerSM = 2;     // split-KV target: work units per multiprocessor
+
+// Query rows (s_q * H of them per sequence) are processed in groups of RC rows; RC is
+// the N of every MMA. 16/32/64 are instantiated.
+inline int rows_per_group(int rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 : 64; }
+
+// Workspace: [header 256 B][batch_info int4 x B][split_list int32 x B]
+//            [items_tmp int4 x max_items][units int4 x max_items*G]
+//            [part_lse f32 x max_pslots*R][part_o f32 x max_pslots*R*512]
+// header word 0: device error bits; 1: number of units; 2: number of split batches;
+// 3: tiles per split (C).
+struct WsLayout {
+  size_t batch_off, split_off, items_off, units_off, plse_off, po_off, total;
+  int64_t max_items, max_units, max_pslots;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int B, int R, int max_seq_len, int num_sms) {
+  WsLayout w{};
+  const int rc = rows_per_group(R);
+  const int G = (R + rc - 1) / rc;
+  const int64_t max_tiles = (max_seq_len + kTileTokens - 1) / kTileTokens;
+  const int64_t target = (int64_t)kUnitsPerSM * num_sms;
+  // C = max(1, ceil(G * sum(n_b) / target)) tiles per split bounds the number of
+  // splits by target/G + B, and the splits of split batches by 2*target/G + 1.
+  int64_t items = target / G + 1 + B;
+  items = items < (int64_t)B * max_tiles ? items : (int64_t)B * max_tiles;
+  int64_t pslots = 2 * target / G + 2;
+  pslots = pslots < (int64_t)B * max_tiles ? pslots : (int64_t)B * max_tiles;
+  w.max_items = items;
+  w.max_units = items * G;
+  w.max_pslots = pslots;
+  size_t off = 256;
+  w.batch_off = off;  off = align_up(off + sizeof(int4) * (size_t)B, 256);
+  w.split_off = off;  off = align_up(off + sizeof(int32_t) * (size_t)B, 256);
+  w.items_off = off;  off = align_up(off + sizeof(int4) * (size_t)items, 256);
+  w.units_off = off;  off = align_up(off + sizeof(int4) * (size_t)w.max_units, 256);
+  w.plse_off = off;   off = align_up(off + sizeof(float) * (size_t)pslots * R, 256);
+  w.po_off = off;     off = align_up(off + sizeof(float) * (size_t)pslots * R * kDV, 256);
+  w.total = off;
+  return w;
+}
+
+struct SchedArgs {
+  const int32_t* seq_lens;
+  uint32_t* hdr;
+  int4* batch_info;      // (splits, partial-slot base or -1, clamped length, item base)
+  int32_t* split_list;   // batches with >= 2 splits
+  int4* items_tmp;       // (b, split, tile_begin | tile_end << 16, partial slot or -1)
+  int4* units;           // sorted longest-first, G consecutive units per item
+  int32_t B, s_q, G, max_len, target_units;
+  int64_t max_items, max_pslots;
+};
+
+struct DecodeArgs {
+  CUtensorMap tm_kv;     // cache as [Np*P rows][576], 64x64 boxes
+  CUtensorMap tm_q;      // q as [B][R][576], 64 x RC x 1 boxes, 128-byte swizzle
+  const int32_t* block_table;
+  const int4* batch_info;
+  const int4* units;
+  const uint32_t* hdr;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  uint32_t* err;
+  const float* kv_scale;
+  int32_t s_q, H, R, P, MB, num_pages, causal;
+  float softmax_scale;
+};
+
+struct CombineArgs {
+  const uint32_t* hdr;
+  const int4* batch_info;
+  const int32_t* split_list;
+  const float* part_o;
+  const float* part_lse;
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t R;
+};
+
+// Launchers (return the launch error).
+cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, int rc, bool fp8, int grid, cudaStream_t s);
+cudaError_t decode_prepare(int rc, bool fp8);   // per-device kernel attributes
+cudaError_t launch_combine(const CombineArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_cache_write(const void* latent, const void* rope, const int64_t* slots,
+                               int32_t n, void* cache, int64_t total_slots, bool fp8,
+                               const float* kv_scale, uint32_t* err, cudaStream_t s);
+
+}  // namespace mla

@@ -1,0 +1,198 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_harness import GpuCase, compare, oracle_decode, sample_rows, torch_bf16_to_bits
+from mla_paged_decode_02_gb300 import api, synth
+from oracle import fp8_e4m3
+from oracle import mla_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+BF, F8 = synth.KV_BF16, synth.KV_FP8_E4M3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    api.lib()
+
+
+# ---------------------------------------------------------------- cache write
+@pytest.mark.parametrize("kv", [BF, F8])
+def test_cache_write_is_bit_exact(kv):
+    case = synth.make_case(B=3, s_q=1, H=1, page_size=64, seq_lens=[1, 64, 300], seed=21, kv_dtype=kv)
+    case.slot_mapping[5] = -1                       # a padding token is skipped
+    g = GpuCase(case)
+    ref = O.cache_write(case.empty_cache(), case.latent_bits, case.rope_bits, case.slot_mapping,
+                        case.page_size, kv, case.kv_scale)
+    assert np.array_equal(g.cache_numpy(), ref)
+
+
+@pytest.mark.parametrize("scale", [1.0, 3.0 / 448.0, 0.0071, 1.0e-3, 17.25, 2.0 ** -20])
+def test_fp8_cache_write_exhaustive_over_bf16_inputs(scale):
+    """Every one of the 65536 bf16 bit patterns goes through the quantising write."""
+    all_bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    latent = all_bits.reshape(128, 512)
+    rope = np.zeros((128, 64), dtype=np.uint16)
+    slots = np.arange(128, dtype=np.int64)
+    scale = float(np.float32(scale))
+    lat_t = torch.from_numpy(latent.view(np.int16)).view(torch.bfloat16).cuda()
+    rope_t = torch.from_numpy(rope.view(np.int16)).view(torch.bfloat16).cuda()
+    cache = torch.full((2, 64, 576), 0x7F, dtype=torch.uint8, device="cuda")
+    ks = torch.tensor([scale], dtype=torch.float32, device="cuda")
+    api.cache_write(lat_t, rope_t, torch.from_numpy(slots).cuda(), cache, ks)
+    got = cache.cpu().numpy().reshape(128, 576)[:, :512]
+    empty = np.full((2, 64, 576), 0x7F, dtype=np.uint8)
+    ref = O.cache_write(empty, latent, rope, slots, 64, F8, scale).reshape(128, 576)[:, :512]
+    x = O.bf16_bits_to_f64(latent)
+    nan_in = np.isnan(x)
+    # NaN inputs: any NaN code is a correct encoding; everything else must match bit for bit
+    assert np.isnan(fp8_e4m3.decode(got[nan_in])).all()
+    assert np.array_equal(got[~nan_in], ref[~nan_in])
+
+
+def test_cache_write_reports_out_of_range_slots():
+    case = synth.make_case(B=1, s_q=1, H=1, page_size=64, seq_lens=[10], seed=22)
+    g = GpuCase(case, build_cache=False)
+    g.cache = g.empty_cache()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.from_numpy(case.slot_mapping.copy()).cuda()
+    slots[3] = case.num_pages * case.page_size         # one past the pool
+    api.cache_write(torch.from_numpy(case.latent_bits.view(np.int16)).view(torch.bfloat16).cuda(),
+                    torch.from_numpy(case.rope_bits.view(np.int16)).view(torch.bfloat16).cuda(),
+                    slots, g.cache, None, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 0x10
+
+
+# ---------------------------------------------------------------- decode, small
+SMALL = [
+    # B, s_q, H, P, lens, kv, causal
+    (2, 1, 16, 64, [100, 257], BF, True),            # config 1 shape
+    (1, 1, 16, 64, [1], BF, True),                   # a single key
+    (3, 1, 16, 64, [127, 128, 129], BF, True),       # tile edges
+    (2, 1, 16, 128, [63, 64], BF, True),
+    (4, 1, 16, 64, [5000, 17, 640, 2049], BF, True), # several splits, ragged tail
+    (2, 1, 128, 128, [300, 1000], BF, True),         # two row groups of 64
+    (2, 1, 32, 64, [200, 129], BF, True),
+    (2, 1, 20, 64, [77, 333], BF, True),             # a ragged row group
+    (2, 1, 1, 64, [90, 700], BF, True),
+    (2, 4, 128, 64, [1000, 67], F8, True),           # multi-token causal, FP8
+    (3, 4, 16, 64, [4, 5, 130], BF, True),           # s_q = seq_len
+    (2, 2, 16, 128, [300, 129], BF, False),          # non-causal multi-token
+    (2, 1, 16, 64, [100, 257], F8, True),
+    (3, 1, 128, 128, [1500, 130, 2000], F8, True),
+    (2, 1, 64, 64, [4096, 3000], F8, True),
+    (2, 3, 16, 64, [3, 129], F8, True),
+]
+
+
+@pytest.mark.parametrize("B,s_q,H,P,lens,kv,causal", SMALL)
+def test_decode_matches_oracle_small(B, s_q, H, P, lens, kv, causal):
+    case = synth.make_case(B=B, s_q=s_q, H=H, page_size=P, seq_lens=lens, seed=31 + B + H,
+                           kv_dtype=kv, causal=causal)
+    g = GpuCase(case)
+    out, lse = g.decode()
+    torch.cuda.synchronize()
+    st, bits = api.decode_check(g.workspace)
+    assert st == 0 and bits == 0
+    ro, rl = oracle_decode(case, g.cache_numpy())
+    compare(case, out, lse, ro, rl)
+
+
+def test_config1_tiny_full():
+    case = synth.make_config(1)
+    g = GpuCase(case)
+    out, lse = g.decode()
+    ro, rl = oracle_decode(case, g.cache_numpy())
+    compare(case, out, lse, ro, rl)
+
+
+# ---------------------------------------------------------------- properties
+def test_poisoned_unused_pages_and_tails_do_not_change_the_output():
+    case = synth.make_case(B=3, s_q=2, H=16, page_size=64, seq_lens=[70, 129, 500], seed=41)
+    g = GpuCase(case)
+    out0, lse0 = [t.clone() for t in g.decode()]
+    # replace every NaN (never-written) value with a large finite one
+    c = g.cache.view(torch.int16)
+    c[c == synth.BF16_NAN_BITS] = 0x4700       # bf16 32768.0
+    out1, lse1 = g.decode()
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+    assert torch.isfinite(out0.float()).all()
+
+
+def test_page_permutation_is_invisible():
+    case = synth.make_case(B=2, s_q=1, H=16, page_size=64, seq_lens=[400, 900], seed=42)
+    g = GpuCase(case)
+    out0, lse0 = [t.clone() for t in g.decode()]
+    perm = torch.from_numpy(np.random.default_rng(5).permutation(case.num_pages)).cuda()
+    new_cache = torch.empty_like(g.cache)
+    new_cache[perm] = g.cache
+    g.cache = new_cache
+    g.block_table = perm[g.block_table.long()].int()
+    out1, lse1 = g.decode()
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+
+
+def test_garbage_workspace_and_outputs_are_fine():
+    case = synth.make_case(B=4, s_q=1, H=16, page_size=64, seq_lens=[3000, 10, 700, 2500], seed=43)
+    g = GpuCase(case)
+    out0, lse0 = [t.clone() for t in g.decode()]
+    g.workspace.fill_(0xFF)
+    out = torch.full_like(out0, float("nan"))
+    lse = torch.full_like(lse0, float("nan"))
+    out1, lse1 = g.decode(out=out, lse=lse)
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+
+
+def test_repeated_calls_are_deterministic():
+    case = synth.make_case(B=8, s_q=1, H=128, page_size=128, seq_lens=(100, 3000), seed=44, kv_dtype=F8)
+    g = GpuCase(case)
+    a = [t.clone() for t in g.decode()]
+    b = g.decode()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_out_of_range_block_table_entry_is_reported_not_faulted():
+    case = synth.make_case(B=2, s_q=1, H=16, page_size=64, seq_lens=[100, 200], seed=45)
+    g = GpuCase(case)
+    g.block_table[1, 2] = case.num_pages + 7
+    g.decode()
+    st, bits = api.decode_check(g.workspace)
+    assert st == -6
+    assert bits & 0x1
+
+
+def test_bad_arguments_launch_nothing():
+    case = synth.make_case(B=1, s_q=1, H=16, page_size=64, seq_lens=[10], seed=46)
+    g = GpuCase(case)
+    with pytest.raises(api.MLAError) as e:
+        api.decode(g.q, g.cache, g.block_table, g.seq_lens, 0.1, max_seq_len=10,
+                   workspace=g.workspace[:100])
+    assert e.value.status == -3
+
+
+# ---------------------------------------------------------------- full-size configs
+FULL = [(2, None, None), (3, None, None), (4, BF, None), (4, F8, None), (5, None, 1), (5, None, 4)]
+
+
+@pytest.mark.parametrize("cfg,kv,s_q", FULL)
+def test_full_size_configs_sampled_rows(cfg, kv, s_q):
+    case = synth.make_config(cfg, kv_dtype=kv, s_q=s_q)
+    g = GpuCase(case)
+    out, lse = g.decode()
+    torch.cuda.synchronize()
+    st, bits = api.decode_check(g.workspace)
+    assert st == 0 and bits == 0
+    # properties over every row
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    rows = sample_rows(case, n_batches=4 if cfg == 5 else 10, n_heads=4)
+    if cfg == 3:
+        ref_cache = O.cache_write(case.empty_cache(), case.latent_bits, case.rope_bits,
+                                  case.slot_mapping, case.page_size, case.kv_dtype, case.kv_scale)
+        assert np.array_equal(g.cache_numpy(), ref_cache)        # bit-exact FP8 write at full size
+    ro, rl = oracle_decode(case, g.cache_numpy(), rows=rows)
+    compare(case, out, lse, ro, rl, rows=rows)
