@@ -224,8 +224,21 @@ def run_ours(args, rank, local_rank, world):
     if st != 0:
         raise RuntimeError(f"device error word after warm-up: status {st} bits {bits:#x}")
 
-    # ---- device-resident timing: K steps, also the decode call alone per step
+    # ---- device-resident timing: K steps, also the decode call alone per step.
+    # nvidia-smi needs ~0.3 s to start sampling, longer than K steps take, so the same
+    # step loop runs for ~0.5 s before and after the timed region while it samples.
     clocks = ClockSampler(local_rank, not args.no_clocks)
+
+    def soak(seconds):
+        if clocks.proc is None:
+            return
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            for _ in range(8):
+                step()
+            torch.cuda.synchronize()
+
+    soak(0.6)
     barrier(world)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -245,6 +258,7 @@ def run_ours(args, rank, local_rank, world):
         ev[k][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    soak(0.4)
     clk = clocks.stop()
     step_ms = sum(a.elapsed_time(b) for a, b in ev)
     dec_ms = sum(a.elapsed_time(b) for a, b in dec) / args.steps
