@@ -108,7 +108,7 @@ size_t mla_decode_workspace_size(const mla_decode_params* p, int32_t num_sms);
  *   workspace    >= mla_decode_workspace_size(p, 0) bytes, 256-byte aligned; its first
  *                4 bytes hold the device error word after the call
  * Launches a split scheduler, the split-KV decode kernel and the LSE combine on
- * `stream`, in that order; returns without synchronising. Graph-capturable. */
+ * `stream`, in that order; returns without synchronising. */
 mla_status mla_decode(const mla_decode_params* p, const void* q, const void* kv_cache,
                       const int32_t* block_table, const int32_t* seq_lens,
                       float softmax_scale, const float* kv_scale, void* out, float* lse,
@@ -134,6 +134,28 @@ mla_status mla_cache_write(const void* latent, const void* rope, const int64_t* 
                            int32_t num_tokens, void* kv_cache, int32_t num_pages,
                            int32_t page_size, int32_t kv_dtype, const float* kv_scale,
                            uint32_t* device_error, mla_stream_t stream);
+
+/* No-allocation variant of mla_decode. This entry point has no counterpart in the
+ * pages; it exists for callers that cannot allocate device memory — for example a
+ * plugin inside an inference engine whose interface passes only inputs and outputs, or
+ * a runtime that owns all device memory through its own allocator and forbids (or
+ * cannot afford the implicit device synchronisation of) a cudaMalloc.
+ * Same arguments and results as mla_decode without the workspace: the scratch memory
+ * lives in a static device array of the library, MLA_NOALLOC_SCRATCH_BYTES long, that
+ * every GPU which loads the library holds until the process exits. No cudaMalloc,
+ * cudaFree or other allocating call is made.
+ * - Returns MLA_ERR_WORKSPACE_TOO_SMALL, launching nothing, when the parameters need
+ *   more scratch than that (mla_decode_workspace_size(p, 0) > MLA_NOALLOC_SCRATCH_BYTES).
+ * - The first call on a device looks up the array's device address (with that device
+ *   current) and caches it; make that first call before any stream capture.
+ * - All calls share the one array, which keeps the last call's contents (nothing in it
+ *   needs clearing: each call writes every scratch word it reads). Calls that overlap
+ *   on the GPU (other streams, other threads) race on it: serialise them. */
+#define MLA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+mla_status mla_decode_noalloc(const mla_decode_params* p, const void* q, const void* kv_cache,
+                              const int32_t* block_table, const int32_t* seq_lens,
+                              float softmax_scale, const float* kv_scale, void* out, float* lse,
+                              mla_stream_t stream);
 
 /* Static text for a status code. */
 const char* mla_status_string(int32_t status);

@@ -21,7 +21,8 @@ STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED",
           -3: "MLA_ERR_WORKSPACE_TOO_SMALL", -4: "MLA_ERR_CUDA", -5: "MLA_ERR_TIMEOUT",
           -6: "MLA_ERR_DEVICE_INDEX"}
 EXPORTS = ("mla_abi_version", "mla_status_string", "mla_decode_workspace_size", "mla_decode",
-           "mla_decode_check", "mla_cache_write")
+           "mla_decode_check", "mla_cache_write", "mla_decode_noalloc")
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla.so")
 _lib = None
@@ -59,6 +60,9 @@ def lib() -> ctypes.CDLL:
                                  vp, vp, vp, sz, vp]
         L.mla_decode_check.restype = i32
         L.mla_decode_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.mla_decode_noalloc.restype = i32
+        L.mla_decode_noalloc.argtypes = [ctypes.POINTER(DecodeParams), vp, vp, vp, vp, ctypes.c_float,
+                                         vp, vp, vp, vp]
         L.mla_cache_write.restype = i32
         L.mla_cache_write.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, vp, vp, vp]
         _lib = L
@@ -137,6 +141,31 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
                           _ptr(workspace), workspace.numel(), _stream(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_decode")
+    return out, lse
+
+
+def decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                   seq_lens: torch.Tensor, softmax_scale: float, kv_scale: torch.Tensor | None = None,
+                   *, max_seq_len: int, causal: bool = True, out: torch.Tensor | None = None,
+                   lse: torch.Tensor | None = None, stream=None):
+    """decode() without a workspace, for callers that cannot allocate device memory: the
+    library's own static scratch array (NOALLOC_SCRATCH_BYTES) is used instead. Calls
+    must not overlap on the GPU."""
+    B, s_q, H, _ = q.shape
+    Np, P, _ = kv_cache.shape
+    kvd = _kv_dtype_of(kv_cache)
+    params = make_params(B, s_q, H, P, Np, block_table.shape[1], max_seq_len, kvd, causal)
+    if out is None:
+        out = torch.empty((B, s_q, H, D_V), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, s_q, H), dtype=torch.float32, device=q.device)
+    st = lib().mla_decode_noalloc(ctypes.byref(params), _ptr(q), _ptr(kv_cache),
+                                  _ptr(block_table.contiguous()), _ptr(seq_lens),
+                                  ctypes.c_float(softmax_scale),
+                                  _ptr(kv_scale) if kvd == KV_FP8_E4M3 else None, _ptr(out),
+                                  _ptr(lse), _stream(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_noalloc")
     return out, lse
 
 
