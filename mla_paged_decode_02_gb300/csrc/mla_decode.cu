@@ -16,12 +16,14 @@
 // of PV. S^T double-buffers in TMEM (2*RC columns) next to O^T (4*RC columns).
 //
 // Pipeline (one CTA per SM, persistent over the work units the scheduler sorted):
-//   warp 0      TMA producer: Q of the unit, then key/value chunks into a ring of
-//               32 KB slots in the order the MMA consumes them:
-//               K(0) K(1) V(0) K(2) V(1) ... K(T-1) V(T-2) V(T-1); a K tile is 5
-//               slots (chunk pairs {0,1}..{6,7}, {8}), a V tile 4 slots ({0,1}..{6,7}).
-//               Values are fetched a second time for PV (they are L2-resident by then)
-//               so that no slot has to live from QK^T through the softmax to PV.
+//   warp 0      key producer: Q of each unit, then the 9 key chunks (128 rows x 64
+//               columns) of every tile into the K ring, one 16 KB slot per chunk. A K slot
+//               is released as soon as its 4 QK^T MMAs complete, so key prefetch (the
+//               HBM stream) never waits for the softmax.
+//   warp 2      value producer: the 4 value chunk pairs (128 rows x 128 columns) of every
+//               tile into the V ring (32 KB slots), fetched a second time for PV — they
+//               were read from HBM for QK^T moments earlier and are L2-resident — so that
+//               no slot lives from QK^T through the softmax to PV.
 //   warp 1      MMA issuer (lane 0): QK(k+1) is issued before PV(k) so the tensor core
 //               works while the softmax of tile k runs. The whole warp zeroes the value
 //               rows past the sequence end in the last tile (the cache may hold NaN there
@@ -32,9 +34,10 @@
 //               rescaled rarely; the final normalisation uses the same reference, so the
 //               result is exact), P^T to shared memory, epilogue (O^T / l -> output or
 //               split partial plus LSE).
-//   warps 8-11  FP8 cache only: E4M3 -> fp16 dequantisation of every chunk (exact: each
-//               E4M3 value is an fp16 value) from a staging ring into the MMA ring, and
-//               bf16 -> fp16 conversion of Q. The FP8 path multiplies in fp16 with fp32
+//   warps 8-11  FP8 cache only: E4M3 -> fp16 dequantisation (exact: each E4M3 value is
+//               an fp16 value) of every chunk, from the producers' staging rings into the
+//               K and V rings in the order the MMA consumes them, and bf16 -> fp16
+//               conversion of Q. The FP8 path multiplies in fp16 with fp32
 //               accumulation; kv_scale is folded into the score scale and the output.
 //
 // Every wait is bounded (mla_ptx.cuh): a stall sets the device error word and the CTA
@@ -48,35 +51,39 @@
 
 namespace mla {
 
-constexpr int kSlotBytes = 32768;    // ring slot: 2 chunks x 128 rows x 128 B
-constexpr int kChunkBytes = 16384;   // 64 columns x 128 rows (bf16/fp16)
-constexpr int kHalfBytes = 8192;     // 64 columns x 64 rows
-constexpr int kStageBytes = 16384;   // FP8 staging slot: 2 chunks x 128 rows x 64 B
-constexpr int kStageChunk = 8192;
-constexpr int kStageHalf = 4096;
-constexpr int kKSlots = 5;
-constexpr int kVSlots = 4;
+constexpr int kKSlotBytes = 16384;   // one 64-column chunk of a tile: 128 rows x 128 B
+constexpr int kVSlotBytes = 32768;   // two chunks: 128 value columns
+constexpr int kHalfBytes = 8192;     // 64 rows x 128 B (one TMA box)
+constexpr int kKStageBytes = 8192;   // FP8 chunk: 128 rows x 64 B
+constexpr int kVStageBytes = 16384;  // FP8 chunk pair
+constexpr int kStageHalf = 4096;     // 64 rows x 64 B (one TMA box)
+constexpr int kChunksPerTile = 9;
+constexpr int kPairsPerTile = 4;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kSoftmaxBar = 1;          // named barrier of the 4 softmax warps
 constexpr int kSmemLimit = 232448;           // 227 KB per CTA
+constexpr int kStaticBudget = 3072;          // static shared memory (barriers, scratch)
 
+// Ring depths per configuration (RC query rows per unit, FP8 or bf16 cache), chosen to
+// fill shared memory: Q (RC x 1152 B), the P^T buffers, then the rings.
 template <int RC, bool FP8>
 struct Cfg {
   static constexpr int kQBytes = RC * 1152;            // 9 chunks x RC rows x 128 B
-  static constexpr int kPRow = RC * 2;                  // bytes of one P^T row (a key)
+  static constexpr int kPRow = RC * 2;                  // bytes of one P^T row (one key)
   static constexpr int kPBytes = 128 * kPRow;
+  static constexpr int kNumP = RC == 64 ? 1 : 2;        // P^T buffers
   static constexpr uint32_t kPSwz = RC == 64 ? kSwizzle128 : RC == 32 ? kSwizzle64 : kSwizzle32;
   static constexpr int kTmemCols = RC == 64 ? 512 : RC == 32 ? 256 : 128;
   static constexpr int kThreads = FP8 ? 384 : 256;
-  static constexpr int kFixed = kQBytes + 2 * kPBytes + 1024;   // + alignment slack
-  static constexpr int kStatic = 4096;                            // static smem budget
-  static constexpr int kNumStage = FP8 ? (RC == 64 ? 3 : 4) : 0;
-  static constexpr int kNumSlots =
-      (kSmemLimit - kStatic - kFixed - kNumStage * kStageBytes) / kSlotBytes;
-  static constexpr int kDynBytes = kFixed + kNumSlots * kSlotBytes + kNumStage * kStageBytes;
-  static_assert(kNumSlots >= 2, "ring too small");
+  static constexpr int NK = FP8 ? (RC == 16 ? 4 : RC == 32 ? 3 : 2) : (RC == 16 ? 6 : 4);
+  static constexpr int NV = FP8 ? 2 : (RC == 16 ? 3 : RC == 32 ? 3 : 2);
+  static constexpr int NKS = FP8 ? (RC == 16 ? 4 : RC == 32 ? 3 : 2) : 0;
+  static constexpr int NVS = FP8 ? (RC == 64 ? 1 : 2) : 0;
+  static constexpr int kDynBytes = 1024 + kQBytes + kNumP * kPBytes + NK * kKSlotBytes +
+                                   NV * kVSlotBytes + NKS * kKStageBytes + NVS * kVStageBytes;
+  static_assert(kDynBytes + kStaticBudget <= kSmemLimit, "shared memory budget");
 };
 
 struct Unit {
@@ -124,19 +131,65 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
+// Global row (page * P + offset) of the 64-key half `h` of tile `tile`, or -1 when the
+// half lies wholly past the sequence end. A block-table entry outside the pool is
+// flagged and mapped past the end of the tensor, where TMA reads zeros.
+__device__ __forceinline__ int half_row(const DecodeArgs& a, const Unit& U, int tile, int h,
+                                        uint32_t* err) {
+  const int tok = tile * kTileTokens + 64 * h;
+  if (tok >= U.L) return -1;
+  int pg = a.block_table[(int64_t)U.b * a.MB + tok / a.P];
+  if (pg < 0 || pg >= a.num_pages) {
+    atomicOr(err, MLA_DEVERR_BLOCK_TABLE);
+    pg = a.num_pages;
+  }
+  return pg * a.P + (tok % a.P);
+}
+
+// E4M3 -> fp16 of one 64-column chunk (128 rows) from a staging buffer laid out as two
+// 64-row TMA boxes [half][64 rows][64 B] into the 128-byte-swizzled MMA layout
+// [128 rows][128 B]. Rows at or past `valid` are written as zeros. 128 threads.
+__device__ __forceinline__ void dequant_chunk(const uint8_t* src, uint8_t* dst, int valid, int t) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int uidx = it * 128 + t;          // 512 16-byte FP8 units per chunk
+    const int row = uidx >> 2, q4 = uidx & 3;
+    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+    if (row < valid) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src + (row >> 6) * kStageHalf +
+                                                      (row & 63) * 64 + q4 * 16);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t hh[8];
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k2] & 0xFFFFu), __NV_E4M3);
+        __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k2] >> 16), __NV_E4M3);
+        hh[2 * k2] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+        hh[2 * k2 + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+      }
+      o0 = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+      o1 = make_uint4(hh[4], hh[5], hh[6], hh[7]);
+    }
+    uint8_t* drow = dst + (row >> 3) * 1024 + (row & 7) * 128;
+    *reinterpret_cast<uint4*>(drow + (((2 * q4) ^ (row & 7)) << 4)) = o0;
+    *reinterpret_cast<uint4*>(drow + (((2 * q4 + 1) ^ (row & 7)) << 4)) = o1;
+  }
+}
+
 template <int RC, bool FP8>
 __global__ void __launch_bounds__(Cfg<RC, FP8>::kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeArgs a) {
   using C = Cfg<RC, FP8>;
-  constexpr int NS = C::kNumSlots;
-  constexpr int NST = FP8 ? C::kNumStage : 1;
+  constexpr int NK = C::NK, NV = C::NV;
+  constexpr int NKS = FP8 ? C::NKS : 1, NVS = FP8 ? C::NVS : 1;
+  constexpr int NP = C::kNumP;
 
   extern __shared__ uint8_t dsmem_raw[];
-  __shared__ __align__(8) uint64_t bar_full[NS], bar_empty[NS];
-  __shared__ __align__(8) uint64_t bar_sfull[NST], bar_sempty[NST];
+  __shared__ __align__(8) uint64_t bar_kfull[NK], bar_kempty[NK], bar_vfull[NV], bar_vempty[NV];
+  __shared__ __align__(8) uint64_t bar_ksfull[NKS], bar_ksempty[NKS], bar_vsfull[NVS], bar_vsempty[NVS];
   __shared__ __align__(8) uint64_t bar_qfull, bar_qready, bar_qempty;
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_s_empty[2], bar_p_full[2];
-  __shared__ __align__(8) uint64_t bar_pv_done, bar_o_empty, bar_drain;
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_s_empty[2], bar_p_full[NP], bar_pv[NP];
+  __shared__ __align__(8) uint64_t bar_o_empty, bar_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ uint32_t abort_s;
   __shared__ float mref_s[RC], alpha_s[RC], tot_s[RC];
@@ -150,33 +203,46 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = dsmem_raw + (base - raw);
   const uint32_t sQ = base;
-  const uint32_t sP = sQ + C::kQBytes;                 // two P^T buffers
-  const uint32_t sRing = sP + 2 * C::kPBytes;
-  const uint32_t sStage = sRing + NS * kSlotBytes;
+  const uint32_t sP = sQ + C::kQBytes;
+  const uint32_t sK = sP + NP * C::kPBytes;
+  const uint32_t sV = sK + NK * kKSlotBytes;
+  const uint32_t sKS = sV + NV * kVSlotBytes;
+  const uint32_t sVS = sKS + (FP8 ? NKS * kKStageBytes : 0);
   uint8_t* gQ = gbase;
-  uint8_t* gP = gbase + C::kQBytes;
-  uint8_t* gRing = gP + 2 * C::kPBytes;
-  uint8_t* gStage = gRing + NS * kSlotBytes;
+  uint8_t* gP = gbase + (sP - sQ);
+  uint8_t* gK = gbase + (sK - sQ);
+  uint8_t* gV = gbase + (sV - sQ);
+  uint8_t* gKS = gbase + (sKS - sQ);
+  uint8_t* gVS = gbase + (sVS - sQ);
 
-  const uint32_t b_full = smem_u32(bar_full), b_empty = smem_u32(bar_empty);
-  const uint32_t b_sfull = smem_u32(bar_sfull), b_sempty = smem_u32(bar_sempty);
+  const uint32_t b_kfull = smem_u32(bar_kfull), b_kempty = smem_u32(bar_kempty);
+  const uint32_t b_vfull = smem_u32(bar_vfull), b_vempty = smem_u32(bar_vempty);
+  const uint32_t b_ksfull = smem_u32(bar_ksfull), b_ksempty = smem_u32(bar_ksempty);
+  const uint32_t b_vsfull = smem_u32(bar_vsfull), b_vsempty = smem_u32(bar_vsempty);
   const uint32_t b_qfull = smem_u32(&bar_qfull), b_qready = smem_u32(&bar_qready);
   const uint32_t b_qempty = smem_u32(&bar_qempty);
   const uint32_t b_s_full = smem_u32(bar_s_full), b_s_empty = smem_u32(bar_s_empty);
-  const uint32_t b_p_full = smem_u32(bar_p_full);
-  const uint32_t b_pv = smem_u32(&bar_pv_done), b_oempty = smem_u32(&bar_o_empty);
-  const uint32_t b_drain = smem_u32(&bar_drain);
+  const uint32_t b_p_full = smem_u32(bar_p_full), b_pv = smem_u32(bar_pv);
+  const uint32_t b_oempty = smem_u32(&bar_o_empty), b_drain = smem_u32(&bar_drain);
   volatile uint32_t* abort_flag = &abort_s;
   uint32_t* err = a.err;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(b_full + 8 * i, FP8 ? 128 : 1);
-      mbar_init(b_empty + 8 * i, 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(b_kfull + 8 * i, FP8 ? 128 : 1);
+      mbar_init(b_kempty + 8 * i, 1);
     }
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(b_sfull + 8 * i, 1);
-      mbar_init(b_sempty + 8 * i, 128);
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(b_vfull + 8 * i, FP8 ? 128 : 1);
+      mbar_init(b_vempty + 8 * i, 1);
+    }
+    for (int i = 0; i < NKS; ++i) {
+      mbar_init(b_ksfull + 8 * i, 1);
+      mbar_init(b_ksempty + 8 * i, 128);
+    }
+    for (int i = 0; i < NVS; ++i) {
+      mbar_init(b_vsfull + 8 * i, 1);
+      mbar_init(b_vsempty + 8 * i, 128);
     }
     mbar_init(b_qfull, 1);
     mbar_init(b_qready, 128);
@@ -184,9 +250,11 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_s_full + 8 * i, 1);
       mbar_init(b_s_empty + 8 * i, 128);
-      mbar_init(b_p_full + 8 * i, 128);
     }
-    mbar_init(b_pv, 1);
+    for (int i = 0; i < NP; ++i) {
+      mbar_init(b_p_full + 8 * i, 128);
+      mbar_init(b_pv + 8 * i, 1);
+    }
     mbar_init(b_oempty, 128);
     mbar_init(b_drain, 1);
     abort_s = 0u;
@@ -215,12 +283,19 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   auto wait_softmax = [&](uint32_t bar, uint32_t parity) -> bool {
     return !named_bar_or(kSoftmaxBar, 128, !wait(bar, parity));
   };
+  // After an abort: wait (bounded, ignoring the abort flag) until the copies issued into
+  // the last `depth` positions of a ring have landed, so no TMA writes after exit.
+  auto drain_ring = [&](uint32_t full_bars, uint32_t pos, uint32_t depth) {
+    volatile uint32_t no_abort = 0;
+    const uint32_t first = pos > depth ? pos - depth : 0;
+    for (uint32_t p = first; p < pos; ++p)
+      mbar_wait(full_bars + 8 * (p % depth), (p / depth) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
+  };
 
   if (warp == 0) {
-    // ============================================================ TMA producer
+    // ============================================================ key producer
     if (lane == 0) {
-      uint32_t pos = 0;
-      uint32_t ucount = 0;
+      uint32_t pos = 0, ucount = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++ucount) {
         const Unit U = load_unit(a, u);
@@ -229,72 +304,82 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         mbar_arrive_expect_tx(b_qfull, 9 * RC * 128);
         for (int c = 0; c < 9; ++c)
           tma_load_3d(sQ + c * RC * 128, &a.tm_q, b_qfull, c * 64, U.g * RC, U.b);
-        const int T = U.te - U.tb;
-        for (int k = 0; k <= T && ok; ++k) {
-          for (int part = 0; part < 2 && ok; ++part) {
-            // part 0: keys of tile k; part 1: values of tile k-1
-            const bool isK = part == 0;
-            if (isK && k == T) continue;
-            if (!isK && k == 0) continue;
-            const int tile = U.tb + (isK ? k : k - 1);
-            int rowg[2];
-            bool hv[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int tok = tile * kTileTokens + 64 * h;
-              hv[h] = tok < U.L;
-              rowg[h] = 0;
-              if (hv[h]) {
-                int pg = a.block_table[(int64_t)U.b * a.MB + tok / a.P];
-                if (pg < 0 || pg >= a.num_pages) {
-                  atomicOr(err, MLA_DEVERR_BLOCK_TABLE);
-                  pg = a.num_pages;   // past the tensor end: TMA fills zeros
-                }
-                rowg[h] = pg * a.P + (tok % a.P);
-              }
+        for (int tile = U.tb; tile < U.te && ok; ++tile) {
+          const int r0 = half_row(a, U, tile, 0, err), r1 = half_row(a, U, tile, 1, err);
+          const int nh = r1 >= 0 ? 2 : 1;
+          for (int c = 0; c < kChunksPerTile && ok; ++c, ++pos) {
+            if (!FP8) {
+              const uint32_t slot = pos % NK;
+              ok = wait(b_kempty + 8 * slot, ((pos / NK) & 1) ^ 1);
+              if (!ok) break;
+              const uint32_t bar = b_kfull + 8 * slot, dst = sK + slot * kKSlotBytes;
+              mbar_arrive_expect_tx(bar, nh * kHalfBytes);
+              tma_load_2d(dst, &a.tm_kv, bar, c * 64, r0);
+              if (nh == 2) tma_load_2d(dst + kHalfBytes, &a.tm_kv, bar, c * 64, r1);
+            } else {
+              const uint32_t slot = pos % NKS;
+              ok = wait(b_ksempty + 8 * slot, ((pos / NKS) & 1) ^ 1);
+              if (!ok) break;
+              const uint32_t bar = b_ksfull + 8 * slot, dst = sKS + slot * kKStageBytes;
+              mbar_arrive_expect_tx(bar, nh * kStageHalf);
+              tma_load_2d(dst, &a.tm_kv, bar, c * 64, r0);
+              if (nh == 2) tma_load_2d(dst + kStageHalf, &a.tm_kv, bar, c * 64, r1);
             }
-            const int nh = hv[1] ? 2 : 1;
-            const int nslots = isK ? kKSlots : kVSlots;
-            for (int si = 0; si < nslots && ok; ++si, ++pos) {
-              const int nsub = (isK && si == kKSlots - 1) ? 1 : 2;
-              if (!FP8) {
-                const uint32_t slot = pos % NS, ph = (pos / NS) & 1;
-                ok = wait(b_empty + 8 * slot, ph ^ 1);
-                if (!ok) break;
-                mbar_arrive_expect_tx(b_full + 8 * slot, nsub * nh * kHalfBytes);
-                for (int sub = 0; sub < nsub; ++sub)
-                  for (int h = 0; h < nh; ++h)
-                    tma_load_2d(sRing + slot * kSlotBytes + sub * kChunkBytes + h * kHalfBytes,
-                                &a.tm_kv, b_full + 8 * slot, (2 * si + sub) * 64, rowg[h]);
-              } else {
-                const uint32_t ss = pos % NST, ph = (pos / NST) & 1;
-                ok = wait(b_sempty + 8 * ss, ph ^ 1);
-                if (!ok) break;
-                mbar_arrive_expect_tx(b_sfull + 8 * ss, nsub * nh * kStageHalf);
-                for (int sub = 0; sub < nsub; ++sub)
-                  for (int h = 0; h < nh; ++h)
-                    tma_load_2d(sStage + ss * kStageBytes + sub * kStageChunk + h * kStageHalf,
-                                &a.tm_kv, b_sfull + 8 * ss, (2 * si + sub) * 64, rowg[h]);
+          }
+        }
+      }
+      if (!ok) {
+        if (FP8) drain_ring(b_ksfull, pos, NKS);
+        else drain_ring(b_kfull, pos, NK);
+      }
+    }
+  } else if (warp == 2) {
+    // ============================================================ value producer
+    if (lane == 0) {
+      uint32_t pos = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const Unit U = load_unit(a, u);
+        for (int tile = U.tb; tile < U.te && ok; ++tile) {
+          const int r0 = half_row(a, U, tile, 0, err), r1 = half_row(a, U, tile, 1, err);
+          const int nh = r1 >= 0 ? 2 : 1;
+          for (int j = 0; j < kPairsPerTile && ok; ++j, ++pos) {
+            if (!FP8) {
+              const uint32_t slot = pos % NV;
+              ok = wait(b_vempty + 8 * slot, ((pos / NV) & 1) ^ 1);
+              if (!ok) break;
+              const uint32_t bar = b_vfull + 8 * slot, dst = sV + slot * kVSlotBytes;
+              mbar_arrive_expect_tx(bar, 2 * nh * kHalfBytes);
+              for (int sub = 0; sub < 2; ++sub) {
+                tma_load_2d(dst + sub * kKSlotBytes, &a.tm_kv, bar, (2 * j + sub) * 64, r0);
+                if (nh == 2)
+                  tma_load_2d(dst + sub * kKSlotBytes + kHalfBytes, &a.tm_kv, bar, (2 * j + sub) * 64, r1);
+              }
+            } else {
+              const uint32_t slot = pos % NVS;
+              ok = wait(b_vsempty + 8 * slot, ((pos / NVS) & 1) ^ 1);
+              if (!ok) break;
+              const uint32_t bar = b_vsfull + 8 * slot, dst = sVS + slot * kVStageBytes;
+              mbar_arrive_expect_tx(bar, 2 * nh * kStageHalf);
+              for (int sub = 0; sub < 2; ++sub) {
+                tma_load_2d(dst + sub * kKStageBytes, &a.tm_kv, bar, (2 * j + sub) * 64, r0);
+                if (nh == 2)
+                  tma_load_2d(dst + sub * kKStageBytes + kStageHalf, &a.tm_kv, bar, (2 * j + sub) * 64, r1);
               }
             }
           }
         }
       }
       if (!ok) {
-        // drain: let every copy already issued land before the CTA can exit
-        const uint32_t nring = FP8 ? NST : NS;
-        const uint32_t first = pos > nring ? pos - nring : 0;
-        const uint32_t fb = FP8 ? b_sfull : b_full;
-        volatile uint32_t no_abort = 0;
-        for (uint32_t p = first; p < pos; ++p)
-          mbar_wait(fb + 8 * (p % nring), (p / nring) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
+        if (FP8) drain_ring(b_vsfull, pos, NVS);
+        else drain_ring(b_vfull, pos, NV);
       }
     }
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     const uint32_t idesc_qk = make_idesc(128, RC, FP8 ? 0u : 1u, 0, 0);
     const uint32_t idesc_pv = make_idesc(128, RC, FP8 ? 0u : 1u, 1, 1);
-    uint32_t pos = 0, gn = 0, ucount = 0;
+    uint32_t kpos = 0, vpos = 0, gn = 0, ucount = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++ucount) {
       const Unit U = load_unit(a, u);
@@ -304,29 +389,25 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       tc_fence_after();
       for (int k = 0; k <= T && ok; ++k) {
         if (k < T) {
+          // ---- scores of tile k into S buffer n&1
           const uint32_t n = gn + k, sb = n & 1;
           ok = wait_warp(b_s_empty + 8 * sb, ((n >> 1) & 1) ^ 1);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d = tmem + sb * RC;
-          for (int ks = 0; ks < kKSlots && ok; ++ks, ++pos) {
-            const uint32_t slot = pos % NS;
-            ok = wait_warp(b_full + 8 * slot, (pos / NS) & 1);
+          for (int c = 0; c < kChunksPerTile && ok; ++c, ++kpos) {
+            const uint32_t slot = kpos % NK;
+            ok = wait_warp(b_kfull + 8 * slot, (kpos / NK) & 1);
             if (!ok) break;
             tc_fence_after();
             if (lane == 0) {
-              const int nsub = ks == kKSlots - 1 ? 1 : 2;
-              for (int sub = 0; sub < nsub; ++sub) {
-                const int chunk = 2 * ks + sub;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const uint64_t ad = make_sdesc(sRing + slot * kSlotBytes + sub * kChunkBytes + kk * 32,
-                                                 16, 1024, kSwizzle128);
-                  const uint64_t bd = make_sdesc(sQ + chunk * RC * 128 + kk * 32, 16, 1024, kSwizzle128);
-                  umma_f16(d, ad, bd, idesc_qk, (ks | sub | kk) != 0);
-                }
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = make_sdesc(sK + slot * kKSlotBytes + kk * 32, 16, 1024, kSwizzle128);
+                const uint64_t bd = make_sdesc(sQ + c * RC * 128 + kk * 32, 16, 1024, kSwizzle128);
+                umma_f16(d, ad, bd, idesc_qk, (c | kk) != 0);
               }
-              umma_commit(b_empty + 8 * slot);
+              umma_commit(b_kempty + 8 * slot);
             }
             __syncwarp();
           }
@@ -338,18 +419,19 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           __syncwarp();
         }
         if (k >= 1) {
-          const uint32_t n = gn + k - 1, pb = n & 1;
+          // ---- values of tile k-1 times P^T into O^T
+          const uint32_t n = gn + k - 1, pb = n % NP;
           const bool first = (k == 1);
-          ok = wait_warp(b_p_full + 8 * pb, (n >> 1) & 1);
+          ok = wait_warp(b_p_full + 8 * pb, (n / NP) & 1);
           if (!ok) break;
           if (first) ok = wait_warp(b_oempty, (ucount & 1) ^ 1);
           if (!ok) break;
           tc_fence_after();
           const int valid = U.L - (U.tb + k - 1) * kTileTokens;
           const int ksteps = valid >= kTileTokens ? 8 : (valid + 15) / 16;
-          for (int j = 0; j < kVSlots && ok; ++j, ++pos) {
-            const uint32_t slot = pos % NS;
-            ok = wait_warp(b_full + 8 * slot, (pos / NS) & 1);
+          for (int j = 0; j < kPairsPerTile && ok; ++j, ++vpos) {
+            const uint32_t slot = vpos % NV;
+            ok = wait_warp(b_vfull + 8 * slot, (vpos / NV) & 1);
             if (!ok) break;
             if (!FP8 && valid < 16 * ksteps) {
               // zero the value rows [valid, 16*ksteps) of both chunks of this slot
@@ -358,9 +440,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
                 const int sub = i / (zrows * 8);
                 const int rem = i % (zrows * 8);
                 const int row = valid + rem / 8;
-                const int u16 = rem % 8;
-                *reinterpret_cast<uint4*>(gRing + slot * kSlotBytes + sub * kChunkBytes +
-                                          row * 128 + u16 * 16) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(gV + slot * kVSlotBytes + sub * kKSlotBytes + row * 128 +
+                                          (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
               }
               fence_proxy_async_smem();
               __syncwarp();
@@ -368,18 +449,18 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
             tc_fence_after();
             if (lane == 0) {
               for (int kk = 0; kk < ksteps; ++kk) {
-                const uint64_t ad = make_sdesc(sRing + slot * kSlotBytes + kk * 2048,
-                                               kChunkBytes, 1024, kSwizzle128);
+                const uint64_t ad = make_sdesc(sV + slot * kVSlotBytes + kk * 2048, kKSlotBytes, 1024,
+                                               kSwizzle128);
                 const uint64_t bd = make_sdesc(sP + pb * C::kPBytes + kk * 16 * C::kPRow,
                                                8 * C::kPRow, 8 * C::kPRow, C::kPSwz);
                 umma_f16(tmem + (2 + j) * RC, ad, bd, idesc_pv, !(first && kk == 0));
               }
-              umma_commit(b_empty + 8 * slot);
+              umma_commit(b_vempty + 8 * slot);
             }
             __syncwarp();
           }
           if (!ok) break;
-          if (lane == 0) umma_commit(b_pv);
+          if (lane == 0) umma_commit(b_pv + 8 * pb);
           __syncwarp();
         }
       }
@@ -397,20 +478,19 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     const uint32_t lane_addr = (uint32_t)(w4 * 32) << 16;
     const float kvs = FP8 ? __ldg(a.kv_scale) : 1.0f;
     const float c_log2 = a.softmax_scale * kvs * kLog2e;
-    uint32_t gn = 0, ucount = 0;
+    uint32_t gn = 0;
     bool ok = true;
     float lsum[RC];
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++ucount) {
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
       const Unit U = load_unit(a, u);
       const int T = U.te - U.tb;
       if (t < RC) mref_s[t] = -INFINITY;
 #pragma unroll
       for (int r = 0; r < RC; ++r) lsum[r] = 0.f;
       named_bar_sync(kSoftmaxBar, 128);
-      // keys visible to row r: L - s_q + 1 + i(r) when causal, else L
       const int row0 = U.g * RC;
       for (int k = 0; k < T && ok; ++k) {
-        const uint32_t n = gn + k, sb = n & 1;
+        const uint32_t n = gn + k, sb = n & 1, pb = n % NP;
         ok = wait_softmax(b_s_full + 8 * sb, (n >> 1) & 1);
         if (!ok) break;
         tc_fence_after();
@@ -421,6 +501,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         tc_fence_before();
         mbar_arrive(b_s_empty + 8 * sb);
 
+        // keys visible to row r: L - s_q + 1 + i(r) when causal, else L
         const int j = (U.tb + k) * kTileTokens + t;
         bool need = false;
         const bool tail = (U.tb + k + 1) * kTileTokens > U.L - a.s_q + 1;   // any row may mask
@@ -452,7 +533,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           for (int r = 0; r < RC; ++r) lsum[r] *= alpha_s[r];
           rescale = k > 0;
         }
-        // P^T row of this key
+        // P^T row of this key, in registers until its buffer is free
         uint32_t pw[RC / 2];
 #pragma unroll
         for (int r = 0; r < RC; r += 2) {
@@ -462,52 +543,58 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           lsum[r] += p0;          // the normaliser sums the unrounded probabilities
           lsum[r + 1] += p1;
         }
-        uint8_t* prow = gP + (n & 1) * C::kPBytes;
+        // the buffer's previous user, PV(n - NP), must have completed
+        if (n >= (uint32_t)NP) {
+          ok = wait_softmax(b_pv + 8 * pb, ((n / NP) - 1) & 1);
+          if (!ok) break;
+        }
+        uint8_t* prow = gP + pb * C::kPBytes;
 #pragma unroll
         for (int u16 = 0; u16 < C::kPRow / 16; ++u16)
           *reinterpret_cast<uint4*>(prow + p_offset<C::kPRow>(t, u16)) =
               make_uint4(pw[4 * u16], pw[4 * u16 + 1], pw[4 * u16 + 2], pw[4 * u16 + 3]);
         fence_proxy_async_smem();
-        if (k > 0) {
-          ok = wait_softmax(b_pv, (n - 1) & 1);
+        if (rescale) {
+          // O^T holds tiles up to k-1 of this unit: wait for PV(n-1), then scale in place
+          ok = wait_softmax(b_pv + 8 * ((n - 1) % NP), ((n - 1) / NP) & 1);
           if (!ok) break;
           tc_fence_after();
-          if (rescale) {
 #pragma unroll 1
-            for (int jt = 0; jt < 4; ++jt) {
+          for (int jt = 0; jt < 4; ++jt) {
 #pragma unroll
-              for (int c = 0; c < RC / 16; ++c) {
-                float o[16];
-                const uint32_t ta = tmem + lane_addr + (2 + jt) * RC + 16 * c;
-                tmem_ld16(ta, o);
-                tmem_wait_ld();
+            for (int c = 0; c < RC / 16; ++c) {
+              float o[16];
+              const uint32_t ta = tmem + lane_addr + (2 + jt) * RC + 16 * c;
+              tmem_ld16(ta, o);
+              tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) o[i] *= alpha_s[16 * c + i];
-                tmem_st16(ta, o);
-              }
+              for (int i = 0; i < 16; ++i) o[i] *= alpha_s[16 * c + i];
+              tmem_st16(ta, o);
             }
-            tmem_wait_st();
           }
+          tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(b_p_full + 8 * (n & 1));
+        mbar_arrive(b_p_full + 8 * pb);
       }
       if (!ok) break;
-      // ---- epilogue
-      ok = wait_softmax(b_pv, (gn + T - 1) & 1);
-      if (!ok) break;
+      // ---- epilogue: wait for the unit's last PV
+      {
+        const uint32_t nl = gn + T - 1;
+        ok = wait_softmax(b_pv + 8 * (nl % NP), (nl / NP) & 1);
+        if (!ok) break;
+      }
       tc_fence_after();
-      float* red = reinterpret_cast<float*>(gP);          // both P^T buffers are idle now
+      // row sums: warp butterfly per row, then the 4 warp partials through shared memory
 #pragma unroll
-      for (int r = 0; r < RC; r += 4)
-        *reinterpret_cast<float4*>(red + t * RC + r) =
-            make_float4(lsum[r], lsum[r + 1], lsum[r + 2], lsum[r + 3]);
-      named_bar_sync(kSoftmaxBar, 128);
-      if (t < RC) {
-        float tot = 0.f;
-        for (int x = 0; x < 128; ++x) tot += red[x * RC + t];
-        tot_s[t] = tot;
+      for (int r = 0; r < RC; ++r) {
+        float v = lsum[r];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == (r & 31)) wmax_s[w4 * RC + r] = v;
       }
+      named_bar_sync(kSoftmaxBar, 128);
+      if (t < RC) tot_s[t] = (wmax_s[t] + wmax_s[RC + t]) + (wmax_s[2 * RC + t] + wmax_s[3 * RC + t]);
       named_bar_sync(kSoftmaxBar, 128);
       const bool direct = U.slot < 0;
 #pragma unroll 1
@@ -547,7 +634,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   } else if (FP8 && warp >= 8) {
     // ============================================================ FP8 dequant
     const int t = threadIdx.x - 256;                    // 0..127
-    uint32_t pos = 0, ucount = 0;
+    uint32_t kpos = 0, vpos = 0, ucount = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++ucount) {
       const Unit U = load_unit(a, u);
@@ -572,56 +659,36 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       if (q_bad) atomicOr(err, MLA_DEVERR_Q_RANGE);
       fence_proxy_async_smem();
       mbar_arrive(b_qready);
+      // chunks in the order the MMA consumes them: K(k) before V(k-1)
       for (int k = 0; k <= T && ok; ++k) {
-        for (int part = 0; part < 2 && ok; ++part) {
-          const bool isK = part == 0;
-          if (isK && k == T) continue;
-          if (!isK && k == 0) continue;
-          const int tile = U.tb + (isK ? k : k - 1);
-          const int valid = U.L - tile * kTileTokens;
-          const int nslots = isK ? kKSlots : kVSlots;
-          for (int si = 0; si < nslots && ok; ++si, ++pos) {
-            const int nsub = (isK && si == kKSlots - 1) ? 1 : 2;
-            const uint32_t ss = pos % NST, sph = (pos / NST) & 1;
-            const uint32_t slot = pos % NS, ph = (pos / NS) & 1;
-            ok = wait(b_sfull + 8 * ss, sph);
+        if (k < T) {
+          const int valid = U.L - (U.tb + k) * kTileTokens;
+          for (int c = 0; c < kChunksPerTile && ok; ++c, ++kpos) {
+            const uint32_t ss = kpos % NKS, slot = kpos % NK;
+            ok = wait(b_ksfull + 8 * ss, (kpos / NKS) & 1);
             if (!ok) break;
-            ok = wait(b_empty + 8 * slot, ph ^ 1);
+            ok = wait(b_kempty + 8 * slot, ((kpos / NK) & 1) ^ 1);
             if (!ok) break;
-            const uint8_t* src = gStage + ss * kStageBytes;
-            uint8_t* dst = gRing + slot * kSlotBytes;
-            for (int sub = 0; sub < nsub; ++sub) {
-#pragma unroll
-              for (int it = 0; it < 4; ++it) {
-                const int uidx = it * 128 + t;          // 512 16-byte FP8 units per chunk
-                const int row = uidx >> 2, q4 = uidx & 3;
-                uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-                if (row < valid) {
-                  const uint4 v = *reinterpret_cast<const uint4*>(
-                      src + sub * kStageChunk + (row >> 6) * kStageHalf + (row & 63) * 64 + q4 * 16);
-                  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                  uint32_t h[8];
-#pragma unroll
-                  for (int k2 = 0; k2 < 4; ++k2) {
-                    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
-                        (__nv_fp8x2_storage_t)(w[k2] & 0xFFFFu), __NV_E4M3);
-                    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
-                        (__nv_fp8x2_storage_t)(w[k2] >> 16), __NV_E4M3);
-                    h[2 * k2] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-                    h[2 * k2 + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
-                  }
-                  o0 = make_uint4(h[0], h[1], h[2], h[3]);
-                  o1 = make_uint4(h[4], h[5], h[6], h[7]);
-                }
-                uint8_t* drow = dst + sub * kChunkBytes + (row >> 3) * 1024 + (row & 7) * 128;
-                const int u0 = 2 * q4, u1 = 2 * q4 + 1;
-                *reinterpret_cast<uint4*>(drow + ((u0 ^ (row & 7)) << 4)) = o0;
-                *reinterpret_cast<uint4*>(drow + ((u1 ^ (row & 7)) << 4)) = o1;
-              }
-            }
+            dequant_chunk(gKS + ss * kKStageBytes, gK + slot * kKSlotBytes, valid, t);
             fence_proxy_async_smem();
-            mbar_arrive(b_sempty + 8 * ss);
-            mbar_arrive(b_full + 8 * slot);
+            mbar_arrive(b_ksempty + 8 * ss);
+            mbar_arrive(b_kfull + 8 * slot);
+          }
+        }
+        if (k >= 1) {
+          const int valid = U.L - (U.tb + k - 1) * kTileTokens;
+          for (int j = 0; j < kPairsPerTile && ok; ++j, ++vpos) {
+            const uint32_t ss = vpos % NVS, slot = vpos % NV;
+            ok = wait(b_vsfull + 8 * ss, (vpos / NVS) & 1);
+            if (!ok) break;
+            ok = wait(b_vempty + 8 * slot, ((vpos / NV) & 1) ^ 1);
+            if (!ok) break;
+            for (int sub = 0; sub < 2; ++sub)
+              dequant_chunk(gVS + ss * kVStageBytes + sub * kKStageBytes,
+                            gV + slot * kVSlotBytes + sub * kKSlotBytes, valid, t);
+            fence_proxy_async_smem();
+            mbar_arrive(b_vsempty + 8 * ss);
+            mbar_arrive(b_vfull + 8 * slot);
           }
         }
       }
@@ -644,7 +711,7 @@ static cudaError_t prepare_one() {
   cudaFuncAttributes attr;
   e = cudaFuncGetAttributes(&attr, decode_kernel<RC, FP8>);
   if (e != cudaSuccess) return e;
-  if ((int)attr.sharedSizeBytes > C::kStatic) return cudaErrorInvalidConfiguration;
+  if ((int)attr.sharedSizeBytes > kStaticBudget) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
 
