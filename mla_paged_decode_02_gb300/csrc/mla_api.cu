@@ -71,15 +71,13 @@ mla_status check_params(const mla_decode_params* p) {
   return MLA_OK;
 }
 
-bool encode_kv_map(CUtensorMap* m, const void* cache, int64_t rows, bool fp8) {
-  cuuint64_t dims[2] = {(cuuint64_t)kDQK, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kDQK * (fp8 ? 1 : 2)};
-  cuuint32_t box[2] = {64, 64};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                        const_cast<void*>(cache), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+bool encode_kv_map(CUtensorMap* m, const void* cache, int64_t rows, uint32_t chunks) {
+  cuuint64_t dims[4] = {64, 8, 9, (cuuint64_t)(rows / 8)};
+  cuuint64_t strides[3] = {(cuuint64_t)kDQK * 2, 128, (cuuint64_t)kDQK * 2 * 8};
+  cuuint32_t box[4] = {64, 8, chunks, 8};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides,
+                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -189,9 +187,14 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
 
   DecodeArgs da;
   std::memset(&da, 0, sizeof(da));
-  if (!encode_kv_map(&da.tm_kv, kv_cache, (int64_t)p->num_pages * p->page_size, fp8))
-    return MLA_ERR_INVALID_ARG;
   if (!encode_q_map(&da.tm_q, q, B, R, rc)) return MLA_ERR_INVALID_ARG;
+  if (!fp8) {
+    const int64_t rows = (int64_t)p->num_pages * p->page_size;
+    if (!encode_kv_map(&da.tm_k, kv_cache, rows, (uint32_t)decode_key_chunks_per_slot(rc, false)) ||
+        !encode_kv_map(&da.tm_v, kv_cache, rows, 2))
+      return MLA_ERR_INVALID_ARG;
+  }
+  da.kv_cache = kv_cache;
   da.block_table = block_table;
   da.batch_info = batch_info;
   da.units = units;

@@ -16,58 +16,67 @@
 // of PV. S^T double-buffers in TMEM (2*RC columns) next to O^T (4*RC columns).
 //
 // Pipeline (one CTA per SM, persistent over the work units the scheduler sorted):
-//   warp 0      key producer: Q of each unit, then the 9 key chunks (128 rows x 64
-//               columns) of every tile into the K ring, one 16 KB slot per chunk. A K slot
-//               is released as soon as its 4 QK^T MMAs complete, so key prefetch (the
-//               HBM stream) never waits for the softmax.
-//   warp 2      value producer: the 4 value chunk pairs (128 rows x 128 columns) of every
-//               tile into the V ring (32 KB slots), fetched a second time for PV — they
-//               were read from HBM for QK^T moments earlier and are L2-resident — so that
-//               no slot lives from QK^T through the softmax to PV.
-//   warp 1      MMA issuer (lane 0): QK(k+1) is issued before PV(k) so the tensor core
-//               works while the softmax of tile k runs. The whole warp zeroes the value
-//               rows past the sequence end in the last tile (the cache may hold NaN there
-//               and 0 * NaN is NaN inside the MMA).
+//   loaders     the key chunks (128 rows x 64 columns) of every tile into the K ring
+//               (16 KB slots) and the value chunk pairs (128 x 128) into the V ring (32 KB
+//               slots), by cp.async straight into the swizzled MMA layout: every thread
+//               computes the page address of its own 16-byte pieces from the block table.
+//               (Small TMA boxes — one 64-row page strip of 128 bytes — move only ~40 GB/s
+//               per SM even from L2, below the per-SM share of HBM bandwidth, while
+//               cp.async moves ~110 GB/s per SM from L2 and saturates HBM.) Values are
+//               read a second time for PV — they are L2-resident by then — so that no
+//               slot lives from QK^T through the softmax to PV. Key and value streams have
+//               their own warps, so key prefetch never waits for the softmax.
+//               bf16 cache: warps 0 and 2 load keys, warp 3 values. FP8 cache: warps 8-9
+//               (keys) and 10-11 (values) prefetch the E4M3 rows into small staging rings
+//               and dequantise them to fp16 (exact: every E4M3 value is an fp16 value);
+//               warps 2-3 convert Q from bf16 to fp16. The FP8 path multiplies in fp16
+//               with fp32 accumulation; kv_scale is folded into the score scale and the
+//               output.
+//   warp 1      MMA issuer (one thread) with two independent cursors, one over the QK^T
+//               chunks and one over the PV chunk pairs. It polls both sides and issues
+//               whichever has its inputs ready; QK^T may run up to two tiles ahead (the
+//               S^T double buffer). It also loads Q of each unit (TMA).
 //   warps 4-7   softmax (one thread per key of the tile = one TMEM lane): scale, causal
 //               mask, online softmax with a lazily-rescaled running max (the reference
 //               max moves only when a score exceeds it by more than 2^8, so O^T is
 //               rescaled rarely; the final normalisation uses the same reference, so the
 //               result is exact), P^T to shared memory, epilogue (O^T / l -> output or
 //               split partial plus LSE).
-//   warps 8-11  FP8 cache only: E4M3 -> fp16 dequantisation (exact: each E4M3 value is
-//               an fp16 value) of every chunk, from the producers' staging rings into the
-//               K and V rings in the order the MMA consumes them, and bf16 -> fp16
-//               conversion of Q. The FP8 path multiplies in fp16 with fp32
-//               accumulation; kv_scale is folded into the score scale and the output.
 //
 // Every wait is bounded (mla_ptx.cuh): a stall sets the device error word and the CTA
-// drains its in-flight copies and MMAs, frees its tensor memory and exits.
+// waits for its in-flight copies and MMAs, frees its tensor memory and exits. Value rows
+// past the sequence end are written as zeros by the loaders (the cache may hold NaN
+// there and 0 * NaN is NaN inside the MMA).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
+#include <type_traits>
 #include "mla_internal.h"
 #include "mla_ptx.cuh"
 #include "../../include/mla.h"
 
 namespace mla {
 
-constexpr int kKSlotBytes = 16384;   // one 64-column chunk of a tile: 128 rows x 128 B
+constexpr int kChunkBytes = 16384;   // one 64-column chunk of a tile: 128 rows x 128 B
 constexpr int kVSlotBytes = 32768;   // two chunks: 128 value columns
-constexpr int kHalfBytes = 8192;     // 64 rows x 128 B (one TMA box)
-constexpr int kKStageBytes = 8192;   // FP8 chunk: 128 rows x 64 B
-constexpr int kVStageBytes = 16384;  // FP8 chunk pair
-constexpr int kStageHalf = 4096;     // 64 rows x 64 B (one TMA box)
+constexpr int kKStageBytes = 8192;   // FP8 chunk: [128 rows][64 B]
+constexpr int kVStageBytes = 16384;  // FP8 chunk pair: [2][128 rows][64 B]
 constexpr int kChunksPerTile = 9;
 constexpr int kPairsPerTile = 4;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kSoftmaxBar = 1;          // named barrier of the 4 softmax warps
+constexpr uint32_t kKLoadBar = 2;            // FP8 key load/dequant warps
+constexpr uint32_t kVLoadBar = 3;            // FP8 value load/dequant warps
+constexpr int kFp8Group = 64;                // threads per FP8 load/dequant group
 constexpr int kSmemLimit = 232448;           // 227 KB per CTA
 constexpr int kStaticBudget = 3072;          // static shared memory (barriers, scratch)
 
 // Ring depths per configuration (RC query rows per unit, FP8 or bf16 cache), chosen to
-// fill shared memory: Q (RC x 1152 B), the P^T buffers, then the rings.
+// fill shared memory: Q (RC x 1152 B), the P^T buffers, then the rings. A key slot holds
+// KC chunks: every slot costs the issuing thread one barrier wait, one proxy fence and
+// one commit, which are worth amortising over several chunks.
 template <int RC, bool FP8>
 struct Cfg {
   static constexpr int kQBytes = RC * 1152;            // 9 chunks x RC rows x 128 B
@@ -77,10 +86,24 @@ struct Cfg {
   static constexpr uint32_t kPSwz = RC == 64 ? kSwizzle128 : RC == 32 ? kSwizzle64 : kSwizzle32;
   static constexpr int kTmemCols = RC == 64 ? 512 : RC == 32 ? 256 : 128;
   static constexpr int kThreads = FP8 ? 384 : 256;
-  static constexpr int NK = FP8 ? (RC == 16 ? 4 : RC == 32 ? 3 : 2) : (RC == 16 ? 6 : 4);
-  static constexpr int NV = FP8 ? 2 : (RC == 16 ? 3 : RC == 32 ? 3 : 2);
-  static constexpr int NKS = FP8 ? (RC == 16 ? 4 : RC == 32 ? 3 : 2) : 0;
-  static constexpr int NVS = FP8 ? (RC == 64 ? 1 : 2) : 0;
+  static constexpr int kPvWarp = FP8 ? 0 : 3;           // warp of the PV issuing thread
+  static constexpr int KC = FP8 ? 1 : 3;                // key chunks per K ring slot
+  static constexpr int kKSlotBytes = KC * kChunkBytes;
+  static constexpr int kSlotsPerTile = 9 / KC;
+  // Ring layouts, as strides of the MMA operand descriptors. bf16 (TMA boxes): a key slot
+  // is [16 row groups][KC chunks][8 rows x 128 B], a value slot [16 groups][2 chunks][...].
+  // FP8 (written by the dequantising threads): [chunk][16 groups][8 rows x 128 B].
+  static constexpr uint32_t kKGroupStride = FP8 ? 1024 : KC * 1024;    // key operand SBO
+  static constexpr uint32_t kKChunkStride = FP8 ? kChunkBytes : 1024;
+  static constexpr uint32_t kVChunkStride = FP8 ? kChunkBytes : 1024;  // value operand LBO
+  static constexpr uint32_t kVGroupStride = FP8 ? 1024 : 2048;         // value operand SBO
+  static constexpr int NK = 2;
+  static constexpr int NV = FP8 ? (RC == 64 ? 1 : 2) : (RC == 16 ? 3 : RC == 32 ? 2 : 1);
+  static constexpr int NKS = FP8 ? (RC == 16 ? 8 : RC == 32 ? 5 : 4) : 0;   // staging depth
+  static constexpr int NVS = FP8 ? 2 : 0;
+  static constexpr int kKLoaders = FP8 ? kFp8Group : 1;   // arrivals that fill a K slot
+  static constexpr int kVLoaders = FP8 ? kFp8Group : 1;
+  static_assert(kSlotsPerTile * KC == 9, "a tile is 9 chunks");
   static constexpr int kDynBytes = 1024 + kQBytes + kNumP * kPBytes + NK * kKSlotBytes +
                                    NV * kVSlotBytes + NKS * kKStageBytes + NVS * kVStageBytes;
   static_assert(kDynBytes + kStaticBudget <= kSmemLimit, "shared memory budget");
@@ -131,33 +154,86 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
-// Global row (page * P + offset) of the 64-key half `h` of tile `tile`, or -1 when the
-// half lies wholly past the sequence end. A block-table entry outside the pool is
-// flagged and mapped past the end of the tensor, where TMA reads zeros.
-__device__ __forceinline__ int half_row(const DecodeArgs& a, const Unit& U, int tile, int h,
-                                        uint32_t* err) {
-  const int tok = tile * kTileTokens + 64 * h;
-  if (tok >= U.L) return -1;
-  int pg = a.block_table[(int64_t)U.b * a.MB + tok / a.P];
-  if (pg < 0 || pg >= a.num_pages) {
-    atomicOr(err, MLA_DEVERR_BLOCK_TABLE);
-    pg = a.num_pages;
-  }
-  return pg * a.P + (tok % a.P);
+// ------------------------------------------------------------------------ cp.async
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's most recent cp.async groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
 }
 
-// E4M3 -> fp16 of one 64-column chunk (128 rows) from a staging buffer laid out as two
-// 64-row TMA boxes [half][64 rows][64 B] into the 128-byte-swizzled MMA layout
-// [128 rows][128 B]. Rows at or past `valid` are written as zeros. 128 threads.
+// Walks the key tiles of this CTA's units in the order every role consumes them, with
+// the first global cache row of each 64-key half of the current tile: >= 0 a row, -1 a
+// half wholly past the sequence end. A block-table entry outside the pool is flagged in
+// the error word and its half reads page 0 instead.
+struct TileIter {
+  int u;
+  Unit U;
+  int tile;
+  int64_t rb0, rb1;
+  __device__ __forceinline__ int64_t row_base(int row) const { return row < 64 ? rb0 : rb1; }
+};
+
+__device__ __forceinline__ void iter_rows(TileIter& it, const DecodeArgs& a, uint32_t* err,
+                                          bool report) {
+  const int32_t* bt = a.block_table + (int64_t)it.U.b * a.MB;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int tok = it.tile * kTileTokens + 64 * h;
+    int64_t r = -1;
+    if (tok < it.U.L) {
+      const int pg = __ldg(bt + tok / a.P);
+      if (pg < 0 || pg >= a.num_pages) {
+        if (report) atomicOr(err, MLA_DEVERR_BLOCK_TABLE);
+        r = tok % a.P;
+      } else {
+        r = (int64_t)pg * a.P + tok % a.P;
+      }
+    }
+    if (h == 0) it.rb0 = r;
+    else it.rb1 = r;
+  }
+}
+
+__device__ __forceinline__ bool iter_begin(TileIter& it, const DecodeArgs& a, int num_units,
+                                           uint32_t* err, bool report) {
+  it.u = blockIdx.x;
+  if (it.u >= num_units) return false;
+  it.U = load_unit(a, it.u);
+  it.tile = it.U.tb;
+  iter_rows(it, a, err, report);
+  return true;
+}
+
+__device__ __forceinline__ bool iter_next(TileIter& it, const DecodeArgs& a, int num_units,
+                                          uint32_t* err, bool report) {
+  if (++it.tile == it.U.te) {
+    it.u += gridDim.x;
+    if (it.u >= num_units) return false;
+    it.U = load_unit(a, it.u);
+    it.tile = it.U.tb;
+  }
+  iter_rows(it, a, err, report);
+  return true;
+}
+
+// E4M3 -> fp16 of one 64-column chunk (128 rows) from a row-major staging buffer
+// [128 rows][64 B] into the 128-byte-swizzled MMA layout [128 rows][128 B]. Rows at or
+// past `valid` are written as zeros (and their staging bytes never read). G threads.
+template <int G>
 __device__ __forceinline__ void dequant_chunk(const uint8_t* src, uint8_t* dst, int valid, int t) {
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int uidx = it * 128 + t;          // 512 16-byte FP8 units per chunk
+  for (int it = 0; it < 512 / G; ++it) {
+    const int uidx = it * G + t;          // 512 16-byte FP8 units per chunk
     const int row = uidx >> 2, q4 = uidx & 3;
     uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
     if (row < valid) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src + (row >> 6) * kStageHalf +
-                                                      (row & 63) * 64 + q4 * 16);
+      const uint4 v = *reinterpret_cast<const uint4*>(src + row * 64 + q4 * 16);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       uint32_t hh[8];
 #pragma unroll
@@ -186,13 +262,14 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
 
   extern __shared__ uint8_t dsmem_raw[];
   __shared__ __align__(8) uint64_t bar_kfull[NK], bar_kempty[NK], bar_vfull[NV], bar_vempty[NV];
-  __shared__ __align__(8) uint64_t bar_ksfull[NKS], bar_ksempty[NKS], bar_vsfull[NVS], bar_vsempty[NVS];
   __shared__ __align__(8) uint64_t bar_qfull, bar_qready, bar_qempty;
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_s_empty[2], bar_p_full[NP], bar_pv[NP];
-  __shared__ __align__(8) uint64_t bar_o_empty, bar_drain;
+  __shared__ __align__(8) uint64_t bar_o_empty, bar_drain[2], bar_vaux;
   __shared__ uint32_t tmem_base_s;
   __shared__ uint32_t abort_s;
-  __shared__ float mref_s[RC], alpha_s[RC], tot_s[RC];
+  __shared__ __align__(16) float mref_s[RC];
+  __shared__ float alpha_s[RC], tot_s[RC];
+  __shared__ int nvis_s[RC];
   __shared__ float wmax_s[4 * RC];
 
   const int warp = threadIdx.x >> 5;
@@ -205,7 +282,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const uint32_t sQ = base;
   const uint32_t sP = sQ + C::kQBytes;
   const uint32_t sK = sP + NP * C::kPBytes;
-  const uint32_t sV = sK + NK * kKSlotBytes;
+  const uint32_t sV = sK + NK * C::kKSlotBytes;
   const uint32_t sKS = sV + NV * kVSlotBytes;
   const uint32_t sVS = sKS + (FP8 ? NKS * kKStageBytes : 0);
   uint8_t* gQ = gbase;
@@ -217,35 +294,26 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
 
   const uint32_t b_kfull = smem_u32(bar_kfull), b_kempty = smem_u32(bar_kempty);
   const uint32_t b_vfull = smem_u32(bar_vfull), b_vempty = smem_u32(bar_vempty);
-  const uint32_t b_ksfull = smem_u32(bar_ksfull), b_ksempty = smem_u32(bar_ksempty);
-  const uint32_t b_vsfull = smem_u32(bar_vsfull), b_vsempty = smem_u32(bar_vsempty);
   const uint32_t b_qfull = smem_u32(&bar_qfull), b_qready = smem_u32(&bar_qready);
   const uint32_t b_qempty = smem_u32(&bar_qempty);
   const uint32_t b_s_full = smem_u32(bar_s_full), b_s_empty = smem_u32(bar_s_empty);
   const uint32_t b_p_full = smem_u32(bar_p_full), b_pv = smem_u32(bar_pv);
-  const uint32_t b_oempty = smem_u32(&bar_o_empty), b_drain = smem_u32(&bar_drain);
+  const uint32_t b_oempty = smem_u32(&bar_o_empty), b_drain = smem_u32(bar_drain);
+  const uint32_t b_vaux = smem_u32(&bar_vaux);
   volatile uint32_t* abort_flag = &abort_s;
   uint32_t* err = a.err;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NK; ++i) {
-      mbar_init(b_kfull + 8 * i, FP8 ? 128 : 1);
+      mbar_init(b_kfull + 8 * i, C::kKLoaders);
       mbar_init(b_kempty + 8 * i, 1);
     }
     for (int i = 0; i < NV; ++i) {
-      mbar_init(b_vfull + 8 * i, FP8 ? 128 : 1);
+      mbar_init(b_vfull + 8 * i, C::kVLoaders);
       mbar_init(b_vempty + 8 * i, 1);
     }
-    for (int i = 0; i < NKS; ++i) {
-      mbar_init(b_ksfull + 8 * i, 1);
-      mbar_init(b_ksempty + 8 * i, 128);
-    }
-    for (int i = 0; i < NVS; ++i) {
-      mbar_init(b_vsfull + 8 * i, 1);
-      mbar_init(b_vsempty + 8 * i, 128);
-    }
     mbar_init(b_qfull, 1);
-    mbar_init(b_qready, 128);
+    mbar_init(b_qready, kFp8Group);
     mbar_init(b_qempty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_s_full + 8 * i, 1);
@@ -257,10 +325,15 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     }
     mbar_init(b_oempty, 128);
     mbar_init(b_drain, 1);
+    mbar_init(b_drain + 8, 1);
+    mbar_init(b_vaux, 1);
     abort_s = 0u;
     fence_mbarrier_init();
-    tma_prefetch_desc(&a.tm_kv);
     tma_prefetch_desc(&a.tm_q);
+    if (!FP8) {
+      tma_prefetch_desc(&a.tm_k);
+      tma_prefetch_desc(&a.tm_v);
+    }
   }
   if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), C::kTmemCols);
   tc_fence_before();
@@ -283,194 +356,179 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   auto wait_softmax = [&](uint32_t bar, uint32_t parity) -> bool {
     return !named_bar_or(kSoftmaxBar, 128, !wait(bar, parity));
   };
-  // After an abort: wait (bounded, ignoring the abort flag) until the copies issued into
-  // the last `depth` positions of a ring have landed, so no TMA writes after exit.
-  auto drain_ring = [&](uint32_t full_bars, uint32_t pos, uint32_t depth) {
-    volatile uint32_t no_abort = 0;
-    const uint32_t first = pos > depth ? pos - depth : 0;
-    for (uint32_t p = first; p < pos; ++p)
-      mbar_wait(full_bars + 8 * (p % depth), (p / depth) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
-  };
-
-  if (warp == 0) {
-    // ============================================================ key producer
+  const uint8_t* cache = static_cast<const uint8_t*>(a.kv_cache);
+  if (!FP8 && warp == 0) {
+    // ============================================================ key producer (bf16)
+    // One thread: every key slot of every tile is two TMA boxes (one per 64-row page
+    // half) of KC chunks; a half wholly past the sequence end is not loaded (its scores
+    // are masked).
     if (lane == 0) {
-      uint32_t pos = 0, ucount = 0;
+      TileIter it;
+      bool more = iter_begin(it, a, num_units, err, true);
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++ucount) {
-        const Unit U = load_unit(a, u);
-        ok = wait(b_qempty, (ucount & 1) ^ 1);
-        if (!ok) break;
-        mbar_arrive_expect_tx(b_qfull, 9 * RC * 128);
-        for (int c = 0; c < 9; ++c)
-          tma_load_3d(sQ + c * RC * 128, &a.tm_q, b_qfull, c * 64, U.g * RC, U.b);
-        for (int tile = U.tb; tile < U.te && ok; ++tile) {
-          const int r0 = half_row(a, U, tile, 0, err), r1 = half_row(a, U, tile, 1, err);
-          const int nh = r1 >= 0 ? 2 : 1;
-          for (int c = 0; c < kChunksPerTile && ok; ++c, ++pos) {
-            if (!FP8) {
-              const uint32_t slot = pos % NK;
-              ok = wait(b_kempty + 8 * slot, ((pos / NK) & 1) ^ 1);
-              if (!ok) break;
-              const uint32_t bar = b_kfull + 8 * slot, dst = sK + slot * kKSlotBytes;
-              mbar_arrive_expect_tx(bar, nh * kHalfBytes);
-              tma_load_2d(dst, &a.tm_kv, bar, c * 64, r0);
-              if (nh == 2) tma_load_2d(dst + kHalfBytes, &a.tm_kv, bar, c * 64, r1);
-            } else {
-              const uint32_t slot = pos % NKS;
-              ok = wait(b_ksempty + 8 * slot, ((pos / NKS) & 1) ^ 1);
-              if (!ok) break;
-              const uint32_t bar = b_ksfull + 8 * slot, dst = sKS + slot * kKStageBytes;
-              mbar_arrive_expect_tx(bar, nh * kStageHalf);
-              tma_load_2d(dst, &a.tm_kv, bar, c * 64, r0);
-              if (nh == 2) tma_load_2d(dst + kStageHalf, &a.tm_kv, bar, c * 64, r1);
-            }
-          }
+      uint32_t p = 0;
+      while (more && ok) {
+        const uint32_t nbox = (it.rb0 >= 0 ? 1u : 0u) + (it.rb1 >= 0 ? 1u : 0u);
+        for (int sl = 0; sl < C::kSlotsPerTile; ++sl, ++p) {
+          const uint32_t slot = p % NK;
+          ok = wait(b_kempty + 8 * slot, ((p / NK) & 1) ^ 1);
+          if (!ok) break;
+          const uint32_t bar = b_kfull + 8 * slot, dst = sK + slot * C::kKSlotBytes;
+          mbar_arrive_expect_tx(bar, nbox * (C::kKSlotBytes / 2));
+          if (it.rb0 >= 0) tma_load_4d(dst, &a.tm_k, bar, 0, 0, sl * C::KC, (int32_t)(it.rb0 >> 3));
+          if (it.rb1 >= 0)
+            tma_load_4d(dst + C::kKSlotBytes / 2, &a.tm_k, bar, 0, 0, sl * C::KC, (int32_t)(it.rb1 >> 3));
         }
+        if (ok) more = iter_next(it, a, num_units, err, true);
       }
-      if (!ok) {
-        if (FP8) drain_ring(b_ksfull, pos, NKS);
-        else drain_ring(b_kfull, pos, NK);
-      }
+      // the last loads issued have landed before the CTA may exit
+      volatile uint32_t no_abort = 0;
+      for (uint32_t q = p > (uint32_t)NK ? p - NK : 0; q < p; ++q)
+        mbar_wait(b_kfull + 8 * (q % NK), (q / NK) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
     }
-  } else if (warp == 2) {
-    // ============================================================ value producer
-    if (lane == 0) {
-      uint32_t pos = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const Unit U = load_unit(a, u);
-        for (int tile = U.tb; tile < U.te && ok; ++tile) {
-          const int r0 = half_row(a, U, tile, 0, err), r1 = half_row(a, U, tile, 1, err);
-          const int nh = r1 >= 0 ? 2 : 1;
-          for (int j = 0; j < kPairsPerTile && ok; ++j, ++pos) {
-            if (!FP8) {
-              const uint32_t slot = pos % NV;
-              ok = wait(b_vempty + 8 * slot, ((pos / NV) & 1) ^ 1);
-              if (!ok) break;
-              const uint32_t bar = b_vfull + 8 * slot, dst = sV + slot * kVSlotBytes;
-              mbar_arrive_expect_tx(bar, 2 * nh * kHalfBytes);
-              for (int sub = 0; sub < 2; ++sub) {
-                tma_load_2d(dst + sub * kKSlotBytes, &a.tm_kv, bar, (2 * j + sub) * 64, r0);
-                if (nh == 2)
-                  tma_load_2d(dst + sub * kKSlotBytes + kHalfBytes, &a.tm_kv, bar, (2 * j + sub) * 64, r1);
-              }
-            } else {
-              const uint32_t slot = pos % NVS;
-              ok = wait(b_vsempty + 8 * slot, ((pos / NVS) & 1) ^ 1);
-              if (!ok) break;
-              const uint32_t bar = b_vsfull + 8 * slot, dst = sVS + slot * kVStageBytes;
-              mbar_arrive_expect_tx(bar, 2 * nh * kStageHalf);
-              for (int sub = 0; sub < 2; ++sub) {
-                tma_load_2d(dst + sub * kKStageBytes, &a.tm_kv, bar, (2 * j + sub) * 64, r0);
-                if (nh == 2)
-                  tma_load_2d(dst + sub * kKStageBytes + kStageHalf, &a.tm_kv, bar, (2 * j + sub) * 64, r1);
-              }
-            }
+  } else if (!FP8 && warp == 2) {
+    // ============================================================ value producer (bf16)
+    // Every value chunk pair: two TMA boxes (re-read from L2, so that no slot lives from
+    // QK^T to PV). On the last tile of a unit the rows from the sequence end up to the end
+    // of the last 16-key MMA step are overwritten with zeros (the cache may hold NaN there
+    // and 0 * NaN is NaN inside the MMA); rows past that step are never read.
+    TileIter it;
+    bool more = iter_begin(it, a, num_units, err, false);
+    bool ok = true;
+    uint32_t p = 0, aux = 0;
+    while (more && ok) {
+      const int valid = it.U.L - it.tile * kTileTokens;
+      const bool tail = valid < kTileTokens;
+      const uint32_t nbox = (it.rb0 >= 0 ? 1u : 0u) + (it.rb1 >= 0 ? 1u : 0u);
+      for (int j = 0; j < kPairsPerTile; ++j, ++p) {
+        const uint32_t slot = p % NV;
+        ok = wait_warp(b_vempty + 8 * slot, ((p / NV) & 1) ^ 1);
+        if (!ok) break;
+        const uint32_t dst = sV + slot * kVSlotBytes;
+        const uint32_t bar = tail ? b_vaux : b_vfull + 8 * slot;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, nbox * (kVSlotBytes / 2));
+          if (it.rb0 >= 0) tma_load_4d(dst, &a.tm_v, bar, 0, 0, 2 * j, (int32_t)(it.rb0 >> 3));
+          if (it.rb1 >= 0) tma_load_4d(dst + kVSlotBytes / 2, &a.tm_v, bar, 0, 0, 2 * j, (int32_t)(it.rb1 >> 3));
+        }
+        if (tail) {
+          ok = wait_warp(b_vaux, aux & 1);
+          ++aux;
+          if (!ok) break;
+          const int nrow = min(kTileTokens, (valid + 15) & ~15) - valid;   // 0..15 rows
+          uint8_t* g = gV + slot * kVSlotBytes;
+          for (int idx = lane; idx < nrow * 16; idx += 32) {   // per row: 2 chunks x 8 units
+            const int row = valid + (idx >> 4), c = (idx >> 3) & 1, u16 = idx & 7;
+            *reinterpret_cast<uint4*>(g + (row >> 3) * 2048 + c * 1024 + (row & 7) * 128 + u16 * 16) =
+                make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_vfull + 8 * slot);
         }
       }
-      if (!ok) {
-        if (FP8) drain_ring(b_vsfull, pos, NVS);
-        else drain_ring(b_vfull, pos, NV);
-      }
+      if (ok) more = iter_next(it, a, num_units, err, false);
+    }
+    if (lane == 0) {
+      volatile uint32_t no_abort = 0;
+      for (uint32_t q = p > (uint32_t)NV ? p - NV : 0; q < p; ++q)
+        mbar_wait(b_vfull + 8 * (q % NV), (q / NV) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
     }
   } else if (warp == 1) {
-    // ============================================================ MMA issuer
-    const uint32_t idesc_qk = make_idesc(128, RC, FP8 ? 0u : 1u, 0, 0);
-    const uint32_t idesc_pv = make_idesc(128, RC, FP8 ? 0u : 1u, 1, 1);
-    uint32_t kpos = 0, vpos = 0, gn = 0, ucount = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++ucount) {
-      const Unit U = load_unit(a, u);
-      const int T = U.te - U.tb;
-      ok = wait_warp(FP8 ? b_qready : b_qfull, ucount & 1);
-      if (!ok) break;
-      tc_fence_after();
-      for (int k = 0; k <= T && ok; ++k) {
-        if (k < T) {
-          // ---- scores of tile k into S buffer n&1
-          const uint32_t n = gn + k, sb = n & 1;
-          ok = wait_warp(b_s_empty + 8 * sb, ((n >> 1) & 1) ^ 1);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t d = tmem + sb * RC;
-          for (int c = 0; c < kChunksPerTile && ok; ++c, ++kpos) {
-            const uint32_t slot = kpos % NK;
-            ok = wait_warp(b_kfull + 8 * slot, (kpos / NK) & 1);
+    // ============================================================ QK^T issuer
+    // One thread, in program order: per unit the Q load (TMA), per tile the S^T buffer,
+    // then every key slot: wait full, 4*KC MMAs, release the slot when they complete.
+    if (lane == 0) {
+      const uint32_t idesc_qk = make_idesc(128, RC, FP8 ? 0u : 1u, 0, 0);
+      // descriptors built once, advanced by constants (the start field counts 16 B units)
+      const uint64_t dK0 = make_sdesc(sK, 16, C::kKGroupStride, kSwizzle128);
+      const uint64_t dQ0 = make_sdesc(sQ, 16, 1024, kSwizzle128);
+      uint32_t n = 0, kp = 0, uc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++uc) {
+        const Unit U = load_unit(a, u);
+        // Q of the unit, once the previous unit's QK^T MMAs have released the buffer
+        ok = wait(b_qempty, (uc & 1) ^ 1);
+        if (!ok) break;
+        mbar_arrive_expect_tx(b_qfull, 9 * RC * 128);
+        for (int c = 0; c < 9; ++c) tma_load_3d(sQ + c * RC * 128, &a.tm_q, b_qfull, c * 64, U.g * RC, U.b);
+        ok = wait(FP8 ? b_qready : b_qfull, uc & 1);
+        for (int k = 0; k < U.te - U.tb && ok; ++k, ++n) {
+          ok = wait(b_s_empty + 8 * (n & 1), ((n >> 1) & 1) ^ 1);
+          const uint32_t d = tmem + (n & 1) * RC;
+          for (int sl = 0; sl < C::kSlotsPerTile && ok; ++sl, ++kp) {
+            const uint32_t ks = kp % NK;
+            ok = wait(b_kfull + 8 * ks, (kp / NK) & 1);
             if (!ok) break;
             tc_fence_after();
-            if (lane == 0) {
+            const uint64_t ad0 = dK0 + (uint64_t)(ks * (C::kKSlotBytes >> 4));
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = make_sdesc(sK + slot * kKSlotBytes + kk * 32, 16, 1024, kSwizzle128);
-                const uint64_t bd = make_sdesc(sQ + c * RC * 128 + kk * 32, 16, 1024, kSwizzle128);
-                umma_f16(d, ad, bd, idesc_qk, (c | kk) != 0);
-              }
-              umma_commit(b_kempty + 8 * slot);
+            for (int cc = 0; cc < C::KC; ++cc) {
+              const int c = sl * C::KC + cc;
+              const uint64_t ad = ad0 + (uint64_t)(cc * (C::kKChunkStride >> 4));
+              const uint64_t bd = dQ0 + (uint64_t)(c * (RC * 128 >> 4));
+              umma_f16(d, ad, bd, idesc_qk, c != 0);
+              umma_f16(d, ad + 2, bd + 2, idesc_qk, 1);
+              umma_f16(d, ad + 4, bd + 4, idesc_qk, 1);
+              umma_f16(d, ad + 6, bd + 6, idesc_qk, 1);
             }
-            __syncwarp();
+            umma_commit(b_kempty + 8 * ks);
           }
-          if (!ok) break;
-          if (lane == 0) {
-            umma_commit(b_s_full + 8 * sb);
-            if (k == T - 1) umma_commit(b_qempty);
-          }
-          __syncwarp();
+          if (ok) umma_commit(b_s_full + 8 * (n & 1));
         }
-        if (k >= 1) {
-          // ---- values of tile k-1 times P^T into O^T
-          const uint32_t n = gn + k - 1, pb = n % NP;
-          const bool first = (k == 1);
-          ok = wait_warp(b_p_full + 8 * pb, (n / NP) & 1);
-          if (!ok) break;
-          if (first) ok = wait_warp(b_oempty, (ucount & 1) ^ 1);
-          if (!ok) break;
-          tc_fence_after();
-          const int valid = U.L - (U.tb + k - 1) * kTileTokens;
+        if (ok) umma_commit(b_qempty);
+      }
+      // drain: every MMA issued has completed before tensor memory is released
+      umma_commit(b_drain);
+      volatile uint32_t no_abort = 0;
+      mbar_wait(b_drain, 0, &no_abort, err, MLA_DEVERR_TIMEOUT);
+    }
+  } else if (warp == C::kPvWarp) {
+    // ============================================================ PV issuer
+    // One thread, in program order: per tile the softmax's P^T (and, for the first tile of
+    // a unit, the epilogue's release of O^T), then every value chunk pair: wait full,
+    // 8 MMAs (fewer on a partial last tile), release the slot when they complete.
+    if (lane == 0) {
+      const uint32_t idesc_pv = make_idesc(128, RC, FP8 ? 0u : 1u, 1, 1);
+      const uint64_t dV0 = make_sdesc(sV, C::kVChunkStride, C::kVGroupStride, kSwizzle128);
+      const uint64_t dP0 = make_sdesc(sP, 8 * C::kPRow, 8 * C::kPRow, C::kPSwz);
+      uint32_t n = 0, vp = 0, uc = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++uc) {
+        const Unit U = load_unit(a, u);
+        for (int k = 0; k < U.te - U.tb && ok; ++k, ++n) {
+          const uint32_t pb = n % NP;
+          ok = wait(b_p_full + 8 * pb, (n / NP) & 1);
+          if (ok && k == 0) ok = wait(b_oempty, (uc & 1) ^ 1);
+          const int valid = U.L - (U.tb + k) * kTileTokens;
           const int ksteps = valid >= kTileTokens ? 8 : (valid + 15) / 16;
-          for (int j = 0; j < kPairsPerTile && ok; ++j, ++vpos) {
-            const uint32_t slot = vpos % NV;
-            ok = wait_warp(b_vfull + 8 * slot, (vpos / NV) & 1);
+          const uint64_t bd0 = dP0 + (uint64_t)(pb * (C::kPBytes >> 4));
+          for (int j = 0; j < kPairsPerTile && ok; ++j, ++vp) {
+            const uint32_t vs = vp % NV;
+            ok = wait(b_vfull + 8 * vs, (vp / NV) & 1);
             if (!ok) break;
-            if (!FP8 && valid < 16 * ksteps) {
-              // zero the value rows [valid, 16*ksteps) of both chunks of this slot
-              const int zrows = 16 * ksteps - valid;
-              for (int i = lane; i < 2 * zrows * 8; i += 32) {
-                const int sub = i / (zrows * 8);
-                const int rem = i % (zrows * 8);
-                const int row = valid + rem / 8;
-                *reinterpret_cast<uint4*>(gV + slot * kVSlotBytes + sub * kKSlotBytes + row * 128 +
-                                          (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-            }
             tc_fence_after();
-            if (lane == 0) {
-              for (int kk = 0; kk < ksteps; ++kk) {
-                const uint64_t ad = make_sdesc(sV + slot * kVSlotBytes + kk * 2048, kKSlotBytes, 1024,
-                                               kSwizzle128);
-                const uint64_t bd = make_sdesc(sP + pb * C::kPBytes + kk * 16 * C::kPRow,
-                                               8 * C::kPRow, 8 * C::kPRow, C::kPSwz);
-                umma_f16(tmem + (2 + j) * RC, ad, bd, idesc_pv, !(first && kk == 0));
-              }
-              umma_commit(b_vempty + 8 * slot);
+            const uint64_t ad0 = dV0 + (uint64_t)(vs * (kVSlotBytes >> 4));
+            const uint32_t d = tmem + (2 + j) * RC;
+            if (ksteps == 8) {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_f16(d, ad0 + kk * (2 * C::kVGroupStride >> 4), bd0 + kk * (16 * C::kPRow >> 4), idesc_pv,
+                         !(k == 0 && kk == 0));
+            } else {
+              for (int kk = 0; kk < ksteps; ++kk)
+                umma_f16(d, ad0 + kk * (2 * C::kVGroupStride >> 4), bd0 + kk * (16 * C::kPRow >> 4), idesc_pv,
+                         !(k == 0 && kk == 0));
             }
-            __syncwarp();
+            umma_commit(b_vempty + 8 * vs);
           }
-          if (!ok) break;
-          if (lane == 0) umma_commit(b_pv + 8 * pb);
-          __syncwarp();
+          if (ok) umma_commit(b_pv + 8 * pb);
         }
       }
-      gn += T;
+      umma_commit(b_drain + 8);
+      volatile uint32_t no_abort = 0;
+      mbar_wait(b_drain + 8, 0, &no_abort, err, MLA_DEVERR_TIMEOUT);
     }
-    // drain: every MMA issued has completed before tensor memory is released
-    if (lane == 0) umma_commit(b_drain);
-    __syncwarp();
-    volatile uint32_t no_abort = 0;
-    mbar_wait(b_drain, 0, &no_abort, err, MLA_DEVERR_TIMEOUT);
   } else if (warp >= 4 && warp < 8) {
     // ============================================================ softmax / epilogue
     const int w4 = warp - 4;
@@ -484,11 +542,17 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
       const Unit U = load_unit(a, u);
       const int T = U.te - U.tb;
-      if (t < RC) mref_s[t] = -INFINITY;
+      const int row0 = U.g * RC;
+      // keys visible to row r: L - s_q + 1 + i(r) when causal (i = the row's new-token
+      // index), else L; only tiles that reach past L - s_q + 1 (or L) need the mask
+      if (t < RC) {
+        mref_s[t] = -INFINITY;
+        nvis_s[t] = a.causal ? min(U.L, U.L - a.s_q + 1 + (row0 + t) / a.H) : U.L;
+      }
+      const int mask_from = a.causal ? U.L - a.s_q + 1 : U.L;
 #pragma unroll
       for (int r = 0; r < RC; ++r) lsum[r] = 0.f;
       named_bar_sync(kSoftmaxBar, 128);
-      const int row0 = U.g * RC;
       for (int k = 0; k < T && ok; ++k) {
         const uint32_t n = gn + k, sb = n & 1, pb = n % NP;
         ok = wait_softmax(b_s_full + 8 * sb, (n >> 1) & 1);
@@ -501,17 +565,26 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         tc_fence_before();
         mbar_arrive(b_s_empty + 8 * sb);
 
-        // keys visible to row r: L - s_q + 1 + i(r) when causal, else L
         const int j = (U.tb + k) * kTileTokens + t;
-        bool need = false;
-        const bool tail = (U.tb + k + 1) * kTileTokens > U.L - a.s_q + 1;   // any row may mask
+        float mr[RC];
 #pragma unroll
-        for (int r = 0; r < RC; ++r) {
-          int nvis = U.L;
-          if (tail && a.causal) nvis = min(U.L, U.L - a.s_q + 1 + (row0 + r) / a.H);
-          const float x = j < nvis ? s[r] * c_log2 : -INFINITY;
-          s[r] = x;
-          need |= x > mref_s[r] + kRescaleLog2;
+        for (int r = 0; r < RC; r += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(mref_s + r);
+          mr[r] = v.x; mr[r + 1] = v.y; mr[r + 2] = v.z; mr[r + 3] = v.w;
+        }
+        bool need = false;
+        if ((U.tb + k + 1) * kTileTokens <= mask_from) {
+#pragma unroll
+          for (int r = 0; r < RC; ++r) {
+            s[r] *= c_log2;
+            need |= s[r] > mr[r] + kRescaleLog2;
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < RC; ++r) {
+            s[r] = j < nvis_s[r] ? s[r] * c_log2 : -INFINITY;
+            need |= s[r] > mr[r] + kRescaleLog2;
+          }
         }
         bool rescale = false;
         if (named_bar_or(kSoftmaxBar, 128, need)) {
@@ -530,15 +603,18 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           }
           named_bar_sync(kSoftmaxBar, 128);
 #pragma unroll
-          for (int r = 0; r < RC; ++r) lsum[r] *= alpha_s[r];
+          for (int r = 0; r < RC; ++r) {
+            lsum[r] *= alpha_s[r];
+            mr[r] = mref_s[r];
+          }
           rescale = k > 0;
         }
         // P^T row of this key, in registers until its buffer is free
         uint32_t pw[RC / 2];
 #pragma unroll
         for (int r = 0; r < RC; r += 2) {
-          const float p0 = s[r] == -INFINITY ? 0.f : ex2_approx(s[r] - mref_s[r]);
-          const float p1 = s[r + 1] == -INFINITY ? 0.f : ex2_approx(s[r + 1] - mref_s[r + 1]);
+          const float p0 = s[r] == -INFINITY ? 0.f : ex2_approx(s[r] - mr[r]);
+          const float p1 = s[r + 1] == -INFINITY ? 0.f : ex2_approx(s[r + 1] - mr[r + 1]);
           pw[r / 2] = pack2<FP8>(p0, p1);
           lsum[r] += p0;          // the normaliser sums the unrounded probabilities
           lsum[r + 1] += p1;
@@ -631,21 +707,16 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       named_bar_sync(kSoftmaxBar, 128);
       gn += T;
     }
-  } else if (FP8 && warp >= 8) {
-    // ============================================================ FP8 dequant
-    const int t = threadIdx.x - 256;                    // 0..127
-    uint32_t kpos = 0, vpos = 0, ucount = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++ucount) {
-      const Unit U = load_unit(a, u);
-      const int T = U.te - U.tb;
-      // Q: bf16 -> fp16 in place (same swizzled positions)
-      ok = wait(b_qfull, ucount & 1);
-      if (!ok) break;
+  } else if (FP8 && (warp == 2 || warp == 3)) {
+    // ============================================================ Q bf16 -> fp16 (FP8)
+    const int gi = threadIdx.x - 64;                    // 0..63
+    uint32_t ucount = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++ucount) {
+      if (!wait(b_qfull, ucount & 1)) break;
       bool q_bad = false;
-      for (int i = t; i < C::kQBytes / 16; i += 128) {
-        uint4* p = reinterpret_cast<uint4*>(gQ + 16 * i);
-        uint4 v = *p;
+      for (int i = gi; i < C::kQBytes / 16; i += kFp8Group) {
+        uint4* q = reinterpret_cast<uint4*>(gQ + 16 * i);
+        uint4 v = *q;
         uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -654,45 +725,92 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           __half2 h = __floats2half2_rn(lo, hi);
           w[k] = *reinterpret_cast<uint32_t*>(&h);
         }
-        *p = make_uint4(w[0], w[1], w[2], w[3]);
+        *q = make_uint4(w[0], w[1], w[2], w[3]);
       }
       if (q_bad) atomicOr(err, MLA_DEVERR_Q_RANGE);
       fence_proxy_async_smem();
       mbar_arrive(b_qready);
-      // chunks in the order the MMA consumes them: K(k) before V(k-1)
-      for (int k = 0; k <= T && ok; ++k) {
-        if (k < T) {
-          const int valid = U.L - (U.tb + k) * kTileTokens;
-          for (int c = 0; c < kChunksPerTile && ok; ++c, ++kpos) {
-            const uint32_t ss = kpos % NKS, slot = kpos % NK;
-            ok = wait(b_ksfull + 8 * ss, (kpos / NKS) & 1);
-            if (!ok) break;
-            ok = wait(b_kempty + 8 * slot, ((kpos / NK) & 1) ^ 1);
-            if (!ok) break;
-            dequant_chunk(gKS + ss * kKStageBytes, gK + slot * kKSlotBytes, valid, t);
-            fence_proxy_async_smem();
-            mbar_arrive(b_ksempty + 8 * ss);
-            mbar_arrive(b_kfull + 8 * slot);
-          }
-        }
-        if (k >= 1) {
-          const int valid = U.L - (U.tb + k - 1) * kTileTokens;
-          for (int j = 0; j < kPairsPerTile && ok; ++j, ++vpos) {
-            const uint32_t ss = vpos % NVS, slot = vpos % NV;
-            ok = wait(b_vsfull + 8 * ss, (vpos / NVS) & 1);
-            if (!ok) break;
-            ok = wait(b_vempty + 8 * slot, ((vpos / NV) & 1) ^ 1);
-            if (!ok) break;
-            for (int sub = 0; sub < 2; ++sub)
-              dequant_chunk(gVS + ss * kVStageBytes + sub * kKStageBytes,
-                            gV + slot * kVSlotBytes + sub * kKSlotBytes, valid, t);
-            fence_proxy_async_smem();
-            mbar_arrive(b_vsempty + 8 * ss);
-            mbar_arrive(b_vfull + 8 * slot);
-          }
+    }
+  } else if (FP8 && warp >= 8) {
+    // ============================================================ FP8 load + dequant
+    // Warps 8-9: key chunks; warps 10-11: value chunk pairs. Each group prefetches its
+    // E4M3 rows with cp.async into a staging ring (NKS / NVS positions deep), then
+    // converts position p into the fp16 MMA ring and arrives on its slot.
+    const bool keys = warp < 10;
+    const int gi = threadIdx.x - (keys ? 256 : 320);    // 0..63
+    const uint32_t gbar = keys ? kKLoadBar : kVLoadBar;
+    constexpr int G = kFp8Group;
+    // Issue the copies of one position (chunk c of a tile for keys, pair c for values).
+    // thread gi owns staging rows gi/4 + 16k (k = 0..7) at 16-byte column gi%4.
+    const int fr0 = gi >> 2, fq = gi & 3;
+    auto issue = [&](const TileIter& it, int c, uint32_t stage) {
+      const int valid = it.U.L - it.tile * kTileTokens;
+      const uint8_t* s0 = cache + (it.rb0 + fr0) * kDQK + fq * 16;
+      const uint8_t* s1 = cache + (it.rb1 + fr0) * kDQK + fq * 16;
+      const uint32_t d0 = stage + gi * 16;
+#pragma unroll
+      for (int sub = 0; sub < (keys ? 1 : 2); ++sub) {
+        const int chunk = keys ? c : 2 * c + sub;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int row = fr0 + 16 * k;
+          if (row < valid && (k < 4 ? it.rb0 : it.rb1) >= 0)
+            cp_async16(d0 + sub * kKStageBytes + k * 1024,
+                       (k < 4 ? s0 : s1) + (16 * (k & 3)) * kDQK + chunk * 64);
         }
       }
-    }
+    };
+    auto run = [&](auto NS_T, auto ND_T, uint32_t full, uint32_t empty, uint32_t ring,
+                   uint8_t* gring, uint32_t slot_bytes, uint32_t stage0, uint8_t* gstage0,
+                   uint32_t stage_bytes, int per_tile) {
+      constexpr int NS = decltype(NS_T)::value;      // staging depth
+      constexpr int ND = decltype(ND_T)::value;      // fp16 ring depth
+      TileIter ii, ci;                               // issue / consume cursors
+      bool imore = iter_begin(ii, a, num_units, err, false);
+      bool cmore = iter_begin(ci, a, num_units, err, false);
+      int ic = 0, cc = 0;
+      uint32_t ip = 0, cp = 0;
+      bool ok = true;
+      for (int k = 0; k < NS - 1; ++k) {             // prologue: NS-1 positions ahead
+        if (imore) {
+          issue(ii, ic, stage0 + (ip % NS) * stage_bytes);
+          if (++ic == per_tile) { ic = 0; imore = iter_next(ii, a, num_units, err, false); }
+          ++ip;
+        }
+        cp_async_commit();
+      }
+      while (cmore && ok) {
+        if (imore) {
+          issue(ii, ic, stage0 + (ip % NS) * stage_bytes);
+          if (++ic == per_tile) { ic = 0; imore = iter_next(ii, a, num_units, err, false); }
+          ++ip;
+        }
+        cp_async_commit();
+        cp_async_wait<NS - 1>();                     // this thread's copies of position cp
+        named_bar_sync(gbar, G);                     // everyone's copies of position cp
+        const uint32_t slot = cp % ND;
+        ok = wait(empty + 8 * slot, ((cp / ND) & 1) ^ 1);
+        if (ok) {
+          const int valid = ci.U.L - ci.tile * kTileTokens;
+          const uint8_t* src = gstage0 + (cp % NS) * stage_bytes;
+          uint8_t* dst = gring + slot * slot_bytes;
+          dequant_chunk<G>(src, dst, valid, gi);
+          if (!keys) dequant_chunk<G>(src + kKStageBytes, dst + kChunkBytes, valid, gi);
+          fence_proxy_async_smem();
+          mbar_arrive(full + 8 * slot);
+        }
+        ok = !named_bar_or(gbar, G, !ok);            // staging slot free for reuse; agree on ok
+        if (++cc == per_tile) { cc = 0; cmore = iter_next(ci, a, num_units, err, false); }
+        ++cp;
+      }
+      cp_async_wait<0>();
+    };
+    if (keys)
+      run(std::integral_constant<int, NKS>{}, std::integral_constant<int, NK>{}, b_kfull, b_kempty, sK, gK,
+          C::kKSlotBytes, sKS, gKS, kKStageBytes, kChunksPerTile);
+    else
+      run(std::integral_constant<int, NVS>{}, std::integral_constant<int, NV>{}, b_vfull, b_vempty, sV, gV,
+          kVSlotBytes, sVS, gVS, kVStageBytes, kPairsPerTile);
   }
 
   // ============================================================ teardown
@@ -720,6 +838,18 @@ static cudaError_t launch_one(const DecodeArgs& a, int grid, cudaStream_t s) {
   using C = Cfg<RC, FP8>;
   decode_kernel<RC, FP8><<<grid, C::kThreads, C::kDynBytes, s>>>(a);
   return cudaGetLastError();
+}
+
+int decode_key_chunks_per_slot(int rc, bool fp8) {
+  switch (rc * 2 + (fp8 ? 1 : 0)) {
+    case 32: return Cfg<16, false>::KC;
+    case 33: return Cfg<16, true>::KC;
+    case 64: return Cfg<32, false>::KC;
+    case 65: return Cfg<32, true>::KC;
+    case 128: return Cfg<64, false>::KC;
+    case 129: return Cfg<64, true>::KC;
+    default: return 0;
+  }
 }
 
 cudaError_t decode_prepare(int rc, bool fp8) {

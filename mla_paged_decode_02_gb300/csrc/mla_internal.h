@@ -71,8 +71,12 @@ struct SchedArgs {
 };
 
 struct DecodeArgs {
-  CUtensorMap tm_kv;     // cache as [Np*P rows][576], 64x64 boxes
   CUtensorMap tm_q;      // q as [B][R][576], 64 x RC x 1 boxes, 128-byte swizzle
+  // bf16 cache viewed as [Np*P/8 row groups][9 chunks][8 rows][64 columns] (strides 9216,
+  // 128, 1152 bytes): a box of KC (keys) or 2 (values) chunks x 64 rows lands in shared
+  // memory as [group][chunk][8 rows x 128 B], 128-byte swizzle
+  CUtensorMap tm_k, tm_v;
+  const void* kv_cache;  // [Np][P][576] bf16 or E4M3 bytes
   const int32_t* block_table;
   const int4* batch_info;
   const int4* units;
@@ -102,6 +106,7 @@ struct CombineArgs {
 cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, int rc, bool fp8, int grid, cudaStream_t s);
 cudaError_t decode_prepare(int rc, bool fp8);   // per-device kernel attributes
+int decode_key_chunks_per_slot(int rc, bool fp8);  // chunks in one key TMA box
 cudaError_t launch_combine(const CombineArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_cache_write(const void* latent, const void* rope, const int64_t* slots,
                                int32_t n, void* cache, int64_t total_slots, bool fp8,
