@@ -122,7 +122,7 @@ MLA_EXPORT size_t mla_decode_workspace_size(const mla_decode_params* p, int32_t 
     if (num_sms <= 0) return 0;
   }
   const int R = p->s_q * p->num_heads;
-  return ws_layout(p->batch, R, p->max_seq_len, num_sms).total;
+  return ws_layout(p->batch, R, num_sms).total;
 }
 
 MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, const void* kv_cache,
@@ -148,7 +148,7 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   const int B = p->batch, R = p->s_q * p->num_heads;
   const int rc = rows_per_group(R);
   const int G = (R + rc - 1) / rc;
-  const WsLayout w = ws_layout(B, R, p->max_seq_len, nsm);
+  const WsLayout w = ws_layout(B, R, nsm);
   if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
   if (!get_encoder()) return MLA_ERR_CUDA;
 
@@ -161,8 +161,8 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* hdr = reinterpret_cast<uint32_t*>(ws);
   int4* batch_info = reinterpret_cast<int4*>(ws + w.batch_off);
-  int32_t* split_list = reinterpret_cast<int32_t*>(ws + w.split_off);
-  int4* items = reinterpret_cast<int4*>(ws + w.items_off);
+  int32_t* cta_first = reinterpret_cast<int32_t*>(ws + w.cta_off);
+  int4* split_list = reinterpret_cast<int4*>(ws + w.split_off);
   int4* units = reinterpret_cast<int4*>(ws + w.units_off);
   float* plse = reinterpret_cast<float*>(ws + w.plse_off);
   float* po = reinterpret_cast<float*>(ws + w.po_off);
@@ -172,17 +172,18 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   sa.seq_lens = seq_lens;
   sa.hdr = hdr;
   sa.batch_info = batch_info;
+  sa.cta_first = cta_first;
   sa.split_list = split_list;
-  sa.items_tmp = items;
   sa.units = units;
   sa.B = B;
   sa.s_q = p->s_q;
   sa.G = G;
   const int64_t cap = (int64_t)p->max_blocks_per_seq * p->page_size;
   sa.max_len = (int)(cap < p->max_seq_len ? cap : p->max_seq_len);
-  sa.target_units = kUnitsPerSM * nsm;
-  sa.max_items = w.max_items;
-  sa.max_pslots = w.max_pslots;
+  sa.grid = nsm;
+  sa.max_units = w.max_units;
+  sa.max_split = w.max_split;
+  sa.max_slots = w.max_slots;
   if (launch_schedule(sa, s) != cudaSuccess) return MLA_ERR_CUDA;
 
   DecodeArgs da;
@@ -198,6 +199,7 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   da.block_table = block_table;
   da.batch_info = batch_info;
   da.units = units;
+  da.cta_first = cta_first;
   da.hdr = hdr;
   da.out = static_cast<__nv_bfloat16*>(out);
   da.lse = lse;
@@ -217,13 +219,13 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
 
   CombineArgs ca{};
   ca.hdr = hdr;
-  ca.batch_info = batch_info;
   ca.split_list = split_list;
   ca.part_o = po;
   ca.part_lse = plse;
   ca.out = static_cast<__nv_bfloat16*>(out);
   ca.lse = lse;
   ca.R = R;
+  ca.RC = rc;
   if (launch_combine(ca, nsm, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -6,9 +6,11 @@
 // A split with no visible key for a row (possible for causal s_q > 1) carries
 // lse_s = -inf and weight 0.
 //
-// One warp per (split sequence, query row): lane l owns output columns [16l, 16l+16),
-// read as four float4 per split (coalesced 2 KB rows). Persistent grid-stride loop over
-// the task list the scheduler wrote, so nothing launches per sequence.
+// The scheduler cuts (sequence, row group) streams at CTA boundaries; each cut stream
+// has `pieces` consecutive partial slots of RC rows. One warp per (cut stream, row):
+// lane l owns output columns [16l, 16l+16), read as four float4 per piece (coalesced
+// 2 KB rows). Persistent grid-stride loop over the list the scheduler wrote, so nothing
+// launches per sequence.
 #include "mla_internal.h"
 
 namespace mla {
@@ -17,24 +19,25 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int64_t tasks = (int64_t)a.hdr[2] * a.R;
+  const int64_t tasks = (int64_t)a.hdr[2] * a.RC;
   for (int64_t task = warp; task < tasks; task += nwarps) {
-    const int b = a.split_list[task / a.R];
-    const int r = (int)(task % a.R);
-    const int4 bi = a.batch_info[b];
-    const int ns = bi.x, base = bi.y;
+    const int4 st = a.split_list[task / a.RC];
+    const int r = (int)(task % a.RC);
+    const int b = st.x, ns = st.z, base = st.w;
+    const int rg = st.y * a.RC + r;          // row within the sequence
+    if (rg >= a.R) continue;
     float m = -INFINITY;
-    for (int s = 0; s < ns; ++s) m = fmaxf(m, a.part_lse[(int64_t)(base + s) * a.R + r]);
+    for (int s = 0; s < ns; ++s) m = fmaxf(m, a.part_lse[(int64_t)(base + s) * a.RC + r]);
     float acc[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) acc[k] = 0.f;
     float wsum = 0.f;
     for (int s = 0; s < ns; ++s) {
-      const float ls = a.part_lse[(int64_t)(base + s) * a.R + r];
+      const float ls = a.part_lse[(int64_t)(base + s) * a.RC + r];
       const float w = ls == -INFINITY ? 0.f : __expf(ls - m);
       wsum += w;
       const float4* src = reinterpret_cast<const float4*>(
-          a.part_o + ((int64_t)(base + s) * a.R + r) * kDV) + lane * 4;
+          a.part_o + ((int64_t)(base + s) * a.RC + r) * kDV) + lane * 4;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float4 v = src[k];
@@ -51,10 +54,10 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
       __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * k] * inv, acc[2 * k + 1] * inv);
       packed[k] = *reinterpret_cast<uint32_t*>(&h);
     }
-    uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)b * a.R + r) * kDV) + lane * 2;
+    uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)b * a.R + rg) * kDV) + lane * 2;
     dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-    if (lane == 0) a.lse[(int64_t)b * a.R + r] = m + logf(wsum);
+    if (lane == 0) a.lse[(int64_t)b * a.R + rg] = m + logf(wsum);
   }
 }
 

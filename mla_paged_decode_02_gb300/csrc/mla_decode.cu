@@ -82,12 +82,12 @@ struct Cfg {
   static constexpr int kQBytes = RC * 1152;            // 9 chunks x RC rows x 128 B
   static constexpr int kPRow = RC * 2;                  // bytes of one P^T row (one key)
   static constexpr int kPBytes = 128 * kPRow;
-  static constexpr int kNumP = RC == 64 ? 1 : 2;        // P^T buffers
+  static constexpr int kNumP = RC == 64 && FP8 ? 1 : 2;  // P^T buffers
   static constexpr uint32_t kPSwz = RC == 64 ? kSwizzle128 : RC == 32 ? kSwizzle64 : kSwizzle32;
   static constexpr int kTmemCols = RC == 64 ? 512 : RC == 32 ? 256 : 128;
   static constexpr int kThreads = FP8 ? 384 : 256;
   static constexpr int kPvWarp = FP8 ? 0 : 3;           // warp of the PV issuing thread
-  static constexpr int KC = FP8 ? 1 : 3;                // key chunks per K ring slot
+  static constexpr int KC = FP8 || RC == 64 ? 1 : 3;     // key chunks per K ring slot
   static constexpr int kKSlotBytes = KC * kChunkBytes;
   static constexpr int kSlotsPerTile = 9 / KC;
   // Ring layouts, as strides of the MMA operand descriptors. bf16 (TMA boxes): a key slot
@@ -97,8 +97,8 @@ struct Cfg {
   static constexpr uint32_t kKChunkStride = FP8 ? kChunkBytes : 1024;
   static constexpr uint32_t kVChunkStride = FP8 ? kChunkBytes : 1024;  // value operand LBO
   static constexpr uint32_t kVGroupStride = FP8 ? 1024 : 2048;         // value operand SBO
-  static constexpr int NK = 2;
-  static constexpr int NV = FP8 ? (RC == 64 ? 1 : 2) : (RC == 16 ? 3 : RC == 32 ? 2 : 1);
+  static constexpr int NK = FP8 || RC < 64 ? 2 : 3;
+  static constexpr int NV = FP8 ? (RC == 64 ? 1 : 2) : (RC == 16 ? 3 : 2);
   static constexpr int NKS = FP8 ? (RC == 16 ? 8 : RC == 32 ? 5 : 4) : 0;   // staging depth
   static constexpr int NVS = FP8 ? 2 : 0;
   static constexpr int kKLoaders = FP8 ? kFp8Group : 1;   // arrivals that fill a K slot
@@ -200,21 +200,20 @@ __device__ __forceinline__ void iter_rows(TileIter& it, const DecodeArgs& a, uin
   }
 }
 
-__device__ __forceinline__ bool iter_begin(TileIter& it, const DecodeArgs& a, int num_units,
+__device__ __forceinline__ bool iter_begin(TileIter& it, const DecodeArgs& a, int u0, int u1,
                                            uint32_t* err, bool report) {
-  it.u = blockIdx.x;
-  if (it.u >= num_units) return false;
+  it.u = u0;
+  if (it.u >= u1) return false;
   it.U = load_unit(a, it.u);
   it.tile = it.U.tb;
   iter_rows(it, a, err, report);
   return true;
 }
 
-__device__ __forceinline__ bool iter_next(TileIter& it, const DecodeArgs& a, int num_units,
+__device__ __forceinline__ bool iter_next(TileIter& it, const DecodeArgs& a, int u1,
                                           uint32_t* err, bool report) {
   if (++it.tile == it.U.te) {
-    it.u += gridDim.x;
-    if (it.u >= num_units) return false;
+    if (++it.u >= u1) return false;
     it.U = load_unit(a, it.u);
     it.tile = it.U.tb;
   }
@@ -341,7 +340,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
-  const int num_units = (int)a.hdr[1];
+  // this CTA's units: a contiguous range of the scheduler's list
+  const int u0 = a.cta_first[blockIdx.x], u1 = a.cta_first[blockIdx.x + 1];
   const int R = a.R;
 
   auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -364,7 +364,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     // are masked).
     if (lane == 0) {
       TileIter it;
-      bool more = iter_begin(it, a, num_units, err, true);
+      bool more = iter_begin(it, a, u0, u1, err, true);
       bool ok = true;
       uint32_t p = 0;
       while (more && ok) {
@@ -379,7 +379,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           if (it.rb1 >= 0)
             tma_load_4d(dst + C::kKSlotBytes / 2, &a.tm_k, bar, 0, 0, sl * C::KC, (int32_t)(it.rb1 >> 3));
         }
-        if (ok) more = iter_next(it, a, num_units, err, true);
+        if (ok) more = iter_next(it, a, u1, err, true);
       }
       // the last loads issued have landed before the CTA may exit
       volatile uint32_t no_abort = 0;
@@ -393,7 +393,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     // of the last 16-key MMA step are overwritten with zeros (the cache may hold NaN there
     // and 0 * NaN is NaN inside the MMA); rows past that step are never read.
     TileIter it;
-    bool more = iter_begin(it, a, num_units, err, false);
+    bool more = iter_begin(it, a, u0, u1, err, false);
     bool ok = true;
     uint32_t p = 0, aux = 0;
     while (more && ok) {
@@ -427,7 +427,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           if (lane == 0) mbar_arrive(b_vfull + 8 * slot);
         }
       }
-      if (ok) more = iter_next(it, a, num_units, err, false);
+      if (ok) more = iter_next(it, a, u1, err, false);
     }
     if (lane == 0) {
       volatile uint32_t no_abort = 0;
@@ -445,7 +445,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       const uint64_t dQ0 = make_sdesc(sQ, 16, 1024, kSwizzle128);
       uint32_t n = 0, kp = 0, uc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++uc) {
+      for (int u = u0; u < u1 && ok; ++u, ++uc) {
         const Unit U = load_unit(a, u);
         // Q of the unit, once the previous unit's QK^T MMAs have released the buffer
         ok = wait(b_qempty, (uc & 1) ^ 1);
@@ -494,7 +494,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       const uint64_t dP0 = make_sdesc(sP, 8 * C::kPRow, 8 * C::kPRow, C::kPSwz);
       uint32_t n = 0, vp = 0, uc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++uc) {
+      for (int u = u0; u < u1 && ok; ++u, ++uc) {
         const Unit U = load_unit(a, u);
         for (int k = 0; k < U.te - U.tb && ok; ++k, ++n) {
           const uint32_t pb = n % NP;
@@ -539,7 +539,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     uint32_t gn = 0;
     bool ok = true;
     float lsum[RC];
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+    for (int u = u0; u < u1 && ok; ++u) {
       const Unit U = load_unit(a, u);
       const int T = U.te - U.tb;
       const int row0 = U.g * RC;
@@ -670,28 +670,57 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         if (lane == (r & 31)) wmax_s[w4 * RC + r] = v;
       }
       named_bar_sync(kSoftmaxBar, 128);
-      if (t < RC) tot_s[t] = (wmax_s[t] + wmax_s[RC + t]) + (wmax_s[2 * RC + t] + wmax_s[3 * RC + t]);
+      if (t < RC) {
+        const float tot = (wmax_s[t] + wmax_s[RC + t]) + (wmax_s[2 * RC + t] + wmax_s[3 * RC + t]);
+        tot_s[t] = tot;
+        alpha_s[t] = tot > 0.f ? kvs / tot : 0.f;     // the row's output factor
+      }
       named_bar_sync(kSoftmaxBar, 128);
       const bool direct = U.slot < 0;
+      // Each warp holds output columns 128 jt + 32 w4 + lane (its TMEM lanes) of 16 rows
+      // per load. It transposes them through 2 KB of the (now idle) P^T buffers, 16-byte
+      // blocks XOR-swizzled by row, so that each lane stores 16 consecutive columns of one
+      // row: 16-byte vector stores instead of one 2-byte store per row.
+      float* stage = reinterpret_cast<float*>(gP) + w4 * 512;
+      const int si = lane >> 1, sh = lane & 1;
 #pragma unroll 1
       for (int jt = 0; jt < 4; ++jt) {
-        const int dv = 128 * jt + t;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < RC / 16; ++c) {
           float o[16];
           tmem_ld16(tmem + lane_addr + (2 + jt) * RC + 16 * c, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int r = 16 * c + i;
-            const int rg = row0 + r;
-            if (rg < R) {
-              const float tot = tot_s[r];
-              const float v = tot > 0.f ? o[i] * (kvs / tot) : 0.f;
-              if (direct)
-                a.out[((int64_t)U.b * R + rg) * kDV + dv] = __float2bfloat16_rn(v);
-              else
-                a.part_o[((int64_t)U.slot * R + rg) * kDV + dv] = v;
+          for (int i = 0; i < 16; ++i)
+            stage[i * 32 + ((((lane >> 2) ^ (i & 7)) << 2) | (lane & 3))] = o[i] * alpha_s[16 * c + i];
+          __syncwarp();
+          float v[16];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float4 x = *reinterpret_cast<const float4*>(stage + si * 32 + (((4 * sh + m) ^ (si & 7)) << 2));
+            v[4 * m] = x.x;
+            v[4 * m + 1] = x.y;
+            v[4 * m + 2] = x.z;
+            v[4 * m + 3] = x.w;
+          }
+          __syncwarp();
+          const int r = 16 * c + si, rg = row0 + r;
+          const int col = 128 * jt + 32 * w4 + 16 * sh;
+          if (rg < R) {
+            if (direct) {
+              uint32_t w[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+                w[k] = *reinterpret_cast<uint32_t*>(&h);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)U.b * R + rg) * kDV + col);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+              float4* dst = reinterpret_cast<float4*>(a.part_o + ((int64_t)U.slot * RC + r) * kDV + col);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) dst[m] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
             }
           }
         }
@@ -700,7 +729,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         const float tot = tot_s[t];
         const float l = tot > 0.f ? (mref_s[t] + __log2f(tot)) * kLn2 : -INFINITY;
         if (direct) a.lse[(int64_t)U.b * R + row0 + t] = l;
-        else a.part_lse[(int64_t)U.slot * R + row0 + t] = l;
+        else a.part_lse[(int64_t)U.slot * RC + t] = l;
       }
       tc_fence_before();
       mbar_arrive(b_oempty);
@@ -711,7 +740,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     // ============================================================ Q bf16 -> fp16 (FP8)
     const int gi = threadIdx.x - 64;                    // 0..63
     uint32_t ucount = 0;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++ucount) {
+    for (int u = u0; u < u1; ++u, ++ucount) {
       if (!wait(b_qfull, ucount & 1)) break;
       bool q_bad = false;
       for (int i = gi; i < C::kQBytes / 16; i += kFp8Group) {
@@ -766,15 +795,15 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       constexpr int NS = decltype(NS_T)::value;      // staging depth
       constexpr int ND = decltype(ND_T)::value;      // fp16 ring depth
       TileIter ii, ci;                               // issue / consume cursors
-      bool imore = iter_begin(ii, a, num_units, err, false);
-      bool cmore = iter_begin(ci, a, num_units, err, false);
+      bool imore = iter_begin(ii, a, u0, u1, err, false);
+      bool cmore = iter_begin(ci, a, u0, u1, err, false);
       int ic = 0, cc = 0;
       uint32_t ip = 0, cp = 0;
       bool ok = true;
       for (int k = 0; k < NS - 1; ++k) {             // prologue: NS-1 positions ahead
         if (imore) {
           issue(ii, ic, stage0 + (ip % NS) * stage_bytes);
-          if (++ic == per_tile) { ic = 0; imore = iter_next(ii, a, num_units, err, false); }
+          if (++ic == per_tile) { ic = 0; imore = iter_next(ii, a, u1, err, false); }
           ++ip;
         }
         cp_async_commit();
@@ -782,7 +811,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       while (cmore && ok) {
         if (imore) {
           issue(ii, ic, stage0 + (ip % NS) * stage_bytes);
-          if (++ic == per_tile) { ic = 0; imore = iter_next(ii, a, num_units, err, false); }
+          if (++ic == per_tile) { ic = 0; imore = iter_next(ii, a, u1, err, false); }
           ++ip;
         }
         cp_async_commit();
@@ -800,7 +829,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           mbar_arrive(full + 8 * slot);
         }
         ok = !named_bar_or(gbar, G, !ok);            // staging slot free for reuse; agree on ok
-        if (++cc == per_tile) { cc = 0; cmore = iter_next(ci, a, num_units, err, false); }
+        if (++cc == per_tile) { cc = 0; cmore = iter_next(ci, a, u1, err, false); }
         ++cp;
       }
       cp_async_wait<0>();

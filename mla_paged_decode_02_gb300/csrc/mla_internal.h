@@ -15,46 +15,39 @@ constexpr int kTileTokens = 128;   // keys per tile: the M of the QK^T MMA (toke
 constexpr int kMaxSeqLen = 1 << 20;
 constexpr int kMaxRows = 4096;     // s_q * H
 constexpr int kMaxBatch = 1 << 16;
-constexpr int kUnitsPerSM = 2;     // split-KV target: work units per multiprocessor
 
 // Query rows (s_q * H of them per sequence) are processed in groups of RC rows; RC is
 // the N of every MMA. 16/32/64 are instantiated.
 inline int rows_per_group(int rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 : 64; }
 
-// Workspace: [header 256 B][batch_info int4 x B][split_list int32 x B]
-//            [items_tmp int4 x max_items][units int4 x max_items*G]
-//            [part_lse f32 x max_pslots*R][part_o f32 x max_pslots*R*512]
-// header word 0: device error bits; 1: number of units; 2: number of split batches;
-// 3: tiles per split (C).
+// Workspace: [header 256 B][batch_info int4 x B][cta_first int32 x (grid + 1)]
+//            [split_list int4 x max_split][units int4 x max_units]
+//            [part_lse f32 x max_slots*RC][part_o f32 x max_slots*RC*512]
+// header word 0: device error bits; 1: number of units; 2: number of split streams;
+// 3: tiles per CTA (q). The bounds follow from the partition (mla_schedule.cu): every
+// CTA boundary cuts at most one (sequence, row group) stream, so there are at most
+// B*G + grid - 1 units, grid - 1 split streams and 2*(grid - 1) partial slots.
 struct WsLayout {
-  size_t batch_off, split_off, items_off, units_off, plse_off, po_off, total;
-  int64_t max_items, max_units, max_pslots;
+  size_t batch_off, cta_off, split_off, units_off, plse_off, po_off, total;
+  int64_t max_units, max_split, max_slots;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout ws_layout(int B, int R, int max_seq_len, int num_sms) {
+inline WsLayout ws_layout(int B, int R, int grid) {
   WsLayout w{};
   const int rc = rows_per_group(R);
-  const int G = (R + rc - 1) / rc;
-  const int64_t max_tiles = (max_seq_len + kTileTokens - 1) / kTileTokens;
-  const int64_t target = (int64_t)kUnitsPerSM * num_sms;
-  // C = max(1, ceil(G * sum(n_b) / target)) tiles per split bounds the number of
-  // splits by target/G + B, and the splits of split batches by 2*target/G + 1.
-  int64_t items = target / G + 1 + B;
-  items = items < (int64_t)B * max_tiles ? items : (int64_t)B * max_tiles;
-  int64_t pslots = 2 * target / G + 2;
-  pslots = pslots < (int64_t)B * max_tiles ? pslots : (int64_t)B * max_tiles;
-  w.max_items = items;
-  w.max_units = items * G;
-  w.max_pslots = pslots;
+  const int64_t G = (R + rc - 1) / rc;
+  w.max_units = (int64_t)B * G + grid;
+  w.max_split = grid;
+  w.max_slots = 2 * (int64_t)grid;
   size_t off = 256;
   w.batch_off = off;  off = align_up(off + sizeof(int4) * (size_t)B, 256);
-  w.split_off = off;  off = align_up(off + sizeof(int32_t) * (size_t)B, 256);
-  w.items_off = off;  off = align_up(off + sizeof(int4) * (size_t)items, 256);
+  w.cta_off = off;    off = align_up(off + sizeof(int32_t) * (size_t)(grid + 1), 256);
+  w.split_off = off;  off = align_up(off + sizeof(int4) * (size_t)w.max_split, 256);
   w.units_off = off;  off = align_up(off + sizeof(int4) * (size_t)w.max_units, 256);
-  w.plse_off = off;   off = align_up(off + sizeof(float) * (size_t)pslots * R, 256);
-  w.po_off = off;     off = align_up(off + sizeof(float) * (size_t)pslots * R * kDV, 256);
+  w.plse_off = off;   off = align_up(off + sizeof(float) * (size_t)w.max_slots * rc, 256);
+  w.po_off = off;     off = align_up(off + sizeof(float) * (size_t)w.max_slots * rc * kDV, 256);
   w.total = off;
   return w;
 }
@@ -62,12 +55,12 @@ inline WsLayout ws_layout(int B, int R, int max_seq_len, int num_sms) {
 struct SchedArgs {
   const int32_t* seq_lens;
   uint32_t* hdr;
-  int4* batch_info;      // (splits, partial-slot base or -1, clamped length, item base)
-  int32_t* split_list;   // batches with >= 2 splits
-  int4* items_tmp;       // (b, split, tile_begin | tile_end << 16, partial slot or -1)
-  int4* units;           // sorted longest-first, G consecutive units per item
-  int32_t B, s_q, G, max_len, target_units;
-  int64_t max_items, max_pslots;
+  int4* batch_info;      // (tiles, 0, clamped length, 0)
+  int32_t* cta_first;    // first unit of each CTA; [grid] = number of units
+  int4* split_list;      // (b, g, pieces, first partial slot) of every cut stream
+  int4* units;           // (b, g, tile_begin | tile_end << 16, partial slot or -1)
+  int32_t B, s_q, G, max_len, grid;
+  int64_t max_units, max_split, max_slots;
 };
 
 struct DecodeArgs {
@@ -80,6 +73,7 @@ struct DecodeArgs {
   const int32_t* block_table;
   const int4* batch_info;
   const int4* units;
+  const int32_t* cta_first;
   const uint32_t* hdr;
   __nv_bfloat16* out;
   float* lse;
@@ -93,13 +87,12 @@ struct DecodeArgs {
 
 struct CombineArgs {
   const uint32_t* hdr;
-  const int4* batch_info;
-  const int32_t* split_list;
+  const int4* split_list;
   const float* part_o;
   const float* part_lse;
   __nv_bfloat16* out;
   float* lse;
-  int32_t R;
+  int32_t R, RC;
 };
 
 // Launchers (return the launch error).

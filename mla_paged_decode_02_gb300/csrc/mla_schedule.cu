@@ -5,144 +5,145 @@
 // cache_seqlens, num_heads, headdim, page_size, causal, ...), which turns the
 // per-sequence lengths into a work partition before the attention kernel runs. This is
 // our own version of that step, computed on the device from seq_lens so that the whole
-// decode stays free of host synchronisation:
+// decode stays free of host synchronisation.
 //
-//   n_b  = ceil(L_b / 128)                      key tiles of sequence b
-//   C    = max(1, ceil(G * sum_b n_b / target)) tiles per split, target = 2 * #SMs
-//   ns_b = ceil(n_b / C)                        splits of sequence b; split s covers
-//          tiles [floor(s n_b / ns_b), floor((s+1) n_b / ns_b))
-//
-// Every split becomes G units (one per group of query rows). Units are emitted
-// longest-first (a counting sort on the tile count) so that the persistent decode grid,
-// which walks them with a static stride, finishes evenly. Sequences with ns_b >= 2
-// get partial-output slots for the LSE combine; the others write the final output.
+// Work is counted in (key tile, row group) pairs. Sequence b has n_b = ceil(L_b / 128)
+// key tiles and G groups of query rows; each (g, b) is a stream of n_b tiles, and the
+// streams are laid end to end, group-major:
+//   pos(g, b) = g * N + sum_{b' < b} n_b',    N = sum_b n_b,    W = G * N,
+// so that the G streams that read the same keys run at the same time on CTAs about
+// grid / G apart, and the second reader finds the keys in L2.
+// The persistent decode grid has one CTA per SM; CTA c takes the positions
+// [c q, (c + 1) q) with q = ceil(W / grid), so no CTA has more than one tile more work
+// than another whatever the length mix. A stream that a CTA boundary cuts becomes one
+// unit per CTA it touches; each such piece writes a partial output (normalised, with
+// its log-sum-exp) to its own slot, and the combine kernel merges the pieces. Streams
+// inside one CTA write the final output directly. Units are stored in position order,
+// so the units of CTA c are the contiguous range [cta_first[c], cta_first[c + 1]).
 #include "mla_internal.h"
 #include "../../include/mla.h"
 
 namespace mla {
 
 constexpr int kSchedThreads = 1024;
-constexpr int kMaxTilesPerSeq = kMaxSeqLen / kTileTokens;   // 8192
 
+// Exclusive prefix sum over the block's threads (warp shuffles, then the 32 warp totals).
 __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* tmp, int64_t* total) {
-  const int tid = threadIdx.x;
-  tmp[tid] = v;
-  __syncthreads();
-  for (int off = 1; off < kSchedThreads; off <<= 1) {
-    int64_t add = tid >= off ? tmp[tid - off] : 0;
-    __syncthreads();
-    tmp[tid] += add;
-    __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
   }
-  const int64_t incl = tmp[tid];
-  *total = tmp[kSchedThreads - 1];
+  if (lane == 31) tmp[warp] = x;
   __syncthreads();
-  return incl - v;
+  if (warp == 0) {
+    int64_t w = tmp[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    tmp[lane] = w;                         // inclusive totals of warps 0..lane
+  }
+  __syncthreads();
+  const int64_t before = (warp > 0 ? tmp[warp - 1] : 0) + x - v;
+  *total = tmp[31];
+  __syncthreads();
+  return before;
+}
+
+__device__ __forceinline__ int clamped_len(const SchedArgs& a, int b, bool report) {
+  const int L = a.seq_lens[b];
+  const int Lc = L < a.s_q ? a.s_q : (L > a.max_len ? a.max_len : L);
+  if (report && Lc != L) atomicOr(a.hdr, MLA_DEVERR_SEQ_LEN);
+  return Lc;
 }
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
-  __shared__ int64_t scan_tmp[kSchedThreads];
-  __shared__ int32_t hist[kMaxTilesPerSeq + 1];
+  static_assert(kSchedThreads == 1024, "the scan assumes 32 warps");
+  __shared__ int64_t scan_tmp[32];
   const int tid = threadIdx.x;
   if (tid == 0) a.hdr[0] = 0u;
-  for (int i = tid; i <= kMaxTilesPerSeq; i += kSchedThreads) hist[i] = 0;
   __syncthreads();
 
   const int chunk = (a.B + kSchedThreads - 1) / kSchedThreads;
   const int b0 = tid * chunk;
   const int b1 = min(a.B, b0 + chunk);
-  const int max_len = a.max_len;
+  const int G = a.G;
 
-  // 1. tiles per sequence (lengths clamped into the valid range; bad ones flagged)
+  // 1. key tiles per sequence (lengths clamped into the valid range; bad ones flagged)
   int64_t my_tiles = 0;
-  for (int b = b0; b < b1; ++b) {
-    int L = a.seq_lens[b];
-    int Lc = L < a.s_q ? a.s_q : (L > max_len ? max_len : L);
-    if (Lc != L) atomicOr(a.hdr, MLA_DEVERR_SEQ_LEN);
-    my_tiles += (Lc + kTileTokens - 1) / kTileTokens;
-  }
-  int64_t sum_tiles;
-  block_exclusive_scan(my_tiles, scan_tmp, &sum_tiles);
-  int64_t C = (a.G * sum_tiles + a.target_units - 1) / a.target_units;
-  if (C < 1) C = 1;
+  for (int b = b0; b < b1; ++b) my_tiles += (clamped_len(a, b, true) + kTileTokens - 1) / kTileTokens;
+  int64_t n_tiles;
+  const int64_t tile_off = block_exclusive_scan(my_tiles, scan_tmp, &n_tiles);
+  const int64_t W = (int64_t)G * n_tiles;
+  const int64_t q = (W + a.grid - 1) / a.grid;   // >= 1: every sequence has a tile
 
-  // 2. splits, partial slots and split batches per thread, then block scans
-  int64_t my_items = 0, my_pslots = 0, my_splitb = 0;
-  for (int b = b0; b < b1; ++b) {
-    int L = a.seq_lens[b];
-    int Lc = L < a.s_q ? a.s_q : (L > max_len ? max_len : L);
-    int n = (Lc + kTileTokens - 1) / kTileTokens;
-    int ns = (int)((n + C - 1) / C);
-    my_items += ns;
-    if (ns >= 2) { my_pslots += ns; my_splitb += 1; }
-  }
-  int64_t n_items, n_pslots, n_splitb;
-  int64_t item_off = block_exclusive_scan(my_items, scan_tmp, &n_items);
-  int64_t pslot_off = block_exclusive_scan(my_pslots, scan_tmp, &n_pslots);
-  int64_t splitb_off = block_exclusive_scan(my_splitb, scan_tmp, &n_splitb);
-  const bool fits = n_items <= a.max_items && n_pslots <= a.max_pslots;
-  if (!fits) {
-    // cannot happen for the sizes mla_decode_workspace_size returns; refuse to overflow
-    if (tid == 0) { atomicOr(a.hdr, MLA_DEVERR_SEQ_LEN); a.hdr[1] = 0; a.hdr[2] = 0; }
-    return;
-  }
-
-  // 3. per-batch info, split list, unsorted items, size histogram
-  for (int b = b0; b < b1; ++b) {
-    int L = a.seq_lens[b];
-    int Lc = L < a.s_q ? a.s_q : (L > max_len ? max_len : L);
-    int n = (Lc + kTileTokens - 1) / kTileTokens;
-    int ns = (int)((n + C - 1) / C);
-    int pbase = ns >= 2 ? (int)pslot_off : -1;
-    a.batch_info[b] = make_int4(ns, pbase, Lc, (int)item_off);
-    if (ns >= 2) a.split_list[splitb_off++] = b;
-    for (int s = 0; s < ns; ++s) {
-      int tb = (int)((int64_t)s * n / ns);
-      int te = (int)((int64_t)(s + 1) * n / ns);
-      a.items_tmp[item_off + s] = make_int4(b, s, tb | (te << 16), ns >= 2 ? pbase + s : -1);
-      atomicAdd(&hist[te - tb], 1);
+  // 2. per group g (in position order): units, cut streams and partial slots of this
+  //    thread's sequences, and their offsets; then the units themselves
+  int64_t unit_base = 0, split_base = 0, slot_base = 0;
+  for (int g = 0; g < G; ++g) {
+    int64_t my_units = 0, my_split = 0, my_slots = 0;
+    int64_t pre = (int64_t)g * n_tiles + tile_off;
+    for (int b = b0; b < b1; ++b) {
+      const int n = (clamped_len(a, b, false) + kTileTokens - 1) / kTileTokens;
+      const int64_t ns = (pre + n - 1) / q - pre / q + 1;
+      my_units += ns;
+      if (ns >= 2) { my_split += 1; my_slots += ns; }
+      pre += n;
     }
-    item_off += ns;
-    if (ns >= 2) pslot_off += ns;
-  }
-  __syncthreads();
-
-  // 4. start offset of each size class, largest sizes first
-  {
-    constexpr int kPer = (kMaxTilesPerSeq + 1 + kSchedThreads - 1) / kSchedThreads;   // 9
-    // thread tid owns sizes [hi_size - kPer*(tid+1) + 1, hi_size - kPer*tid] in descending order
-    int64_t local = 0;
-    int sz[kPer];
-    for (int k = 0; k < kPer; ++k) {
-      int s = kMaxTilesPerSeq - (tid * kPer + k);
-      sz[k] = s;
-      local += s >= 1 ? hist[s] : 0;
+    int64_t g_units, g_split, g_slots;
+    int64_t unit_off = unit_base + block_exclusive_scan(my_units, scan_tmp, &g_units);
+    int64_t split_off = split_base + block_exclusive_scan(my_split, scan_tmp, &g_split);
+    int64_t slot_off = slot_base + block_exclusive_scan(my_slots, scan_tmp, &g_slots);
+    unit_base += g_units;
+    split_base += g_split;
+    slot_base += g_slots;
+    if (unit_base > a.max_units || split_base > a.max_split || slot_base > a.max_slots) {
+      // cannot happen for the sizes mla_decode_workspace_size returns; refuse to overflow
+      for (int c = tid; c <= a.grid; c += kSchedThreads) a.cta_first[c] = 0;
+      if (tid == 0) { atomicOr(a.hdr, MLA_DEVERR_SEQ_LEN); a.hdr[1] = 0; a.hdr[2] = 0; }
+      return;
     }
-    int64_t tot;
-    int64_t run = block_exclusive_scan(local, scan_tmp, &tot);
-    for (int k = 0; k < kPer; ++k) {
-      int s = sz[k];
-      if (s >= 1) {
-        int h = hist[s];
-        hist[s] = (int)run;
-        run += h;
+    if (g == 0) {
+      // the first unit of each CTA is set below; a CTA whose range starts at or past W
+      // has no work. The number of units is known only at the end: patched there.
+      for (int c = tid; c <= a.grid; c += kSchedThreads) a.cta_first[c] = -1;
+      __syncthreads();
+    }
+    // units in position order; the unit starting at c q is the first of CTA c
+    pre = (int64_t)g * n_tiles + tile_off;
+    for (int b = b0; b < b1; ++b) {
+      const int Lc = clamped_len(a, b, false);
+      const int n = (Lc + kTileTokens - 1) / kTileTokens;
+      if (g == 0) a.batch_info[b] = make_int4(n, 0, Lc, 0);
+      const int64_t c_lo = pre / q;
+      const int ns = (int)((pre + n - 1) / q - c_lo + 1);
+      const int slot0 = ns >= 2 ? (int)slot_off : -1;
+      if (ns >= 2) a.split_list[split_off++] = make_int4(b, g, ns, slot0);
+      for (int k = 0; k < ns; ++k) {
+        const int64_t c = c_lo + k;
+        const int64_t s0 = pre > c * q ? pre : c * q;
+        const int64_t s1 = pre + n < (c + 1) * q ? pre + n : (c + 1) * q;
+        const int tb = (int)(s0 - pre), te = (int)(s1 - pre);
+        a.units[unit_off] = make_int4(b, g, tb | (te << 16), ns >= 2 ? slot0 + k : -1);
+        if (s0 == c * q) a.cta_first[c] = (int32_t)unit_off;
+        ++unit_off;
       }
+      if (ns >= 2) slot_off += ns;
+      pre += n;
     }
   }
   __syncthreads();
-
-  // 5. scatter items into sorted order; each expands into G consecutive units
-  for (int64_t it = tid; it < n_items; it += kSchedThreads) {
-    int4 v = a.items_tmp[it];
-    int tb = v.z & 0xFFFF, te = (int)((unsigned)v.z >> 16);
-    int pos = atomicAdd(&hist[te - tb], 1);
-    for (int g = 0; g < a.G; ++g)
-      a.units[(int64_t)pos * a.G + g] = make_int4(v.x, g, v.z, v.w);
-  }
+  for (int c = tid; c <= a.grid; c += kSchedThreads)
+    if (a.cta_first[c] < 0) a.cta_first[c] = (int32_t)unit_base;
+  const int64_t n_units = unit_base, n_split = split_base;
   if (tid == 0) {
-    a.hdr[1] = (uint32_t)(n_items * a.G);
-    a.hdr[2] = (uint32_t)n_splitb;
-    a.hdr[3] = (uint32_t)C;
+    a.hdr[1] = (uint32_t)n_units;
+    a.hdr[2] = (uint32_t)n_split;
+    a.hdr[3] = (uint32_t)(q < 0xFFFFFFFFll ? q : 0xFFFFFFFFll);
   }
 }
 
