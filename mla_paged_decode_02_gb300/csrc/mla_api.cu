@@ -71,13 +71,22 @@ mla_status check_params(const mla_decode_params* p) {
   return MLA_OK;
 }
 
-bool encode_kv_map(CUtensorMap* m, const void* cache, int64_t rows, uint32_t chunks) {
+// The cache as [rows / 8 groups][9 chunks][8 rows][64 elements] (strides 8 rows, one
+// chunk, one row): a box of `chunks` chunks x 8 groups (64 rows) lands in shared memory
+// as [group][chunk][8 rows][64 elements]. bf16 rows (128 B) are 128-byte swizzled for
+// the MMA. E4M3 key rows (64 B) are 64-byte swizzled, so that 32 threads reading one
+// row each hit distinct banks; E4M3 value rows are left plain.
+bool encode_kv_map(CUtensorMap* m, const void* cache, int64_t rows, uint32_t chunks, bool fp8,
+                   bool keys) {
+  const cuuint64_t es = fp8 ? 1 : 2;
   cuuint64_t dims[4] = {64, 8, 9, (cuuint64_t)(rows / 8)};
-  cuuint64_t strides[3] = {(cuuint64_t)kDQK * 2, 128, (cuuint64_t)kDQK * 2 * 8};
+  cuuint64_t strides[3] = {kDQK * es, 64 * es, kDQK * es * 8};
   cuuint32_t box[4] = {64, 8, chunks, 8};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides,
-                        box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                        const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        !fp8 ? CU_TENSOR_MAP_SWIZZLE_128B
+                             : keys ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -189,10 +198,10 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   DecodeArgs da;
   std::memset(&da, 0, sizeof(da));
   if (!encode_q_map(&da.tm_q, q, B, R, rc)) return MLA_ERR_INVALID_ARG;
-  if (!fp8) {
+  {
     const int64_t rows = (int64_t)p->num_pages * p->page_size;
-    if (!encode_kv_map(&da.tm_k, kv_cache, rows, (uint32_t)decode_key_chunks_per_slot(rc, false)) ||
-        !encode_kv_map(&da.tm_v, kv_cache, rows, 2))
+    if (!encode_kv_map(&da.tm_k, kv_cache, rows, (uint32_t)decode_key_chunks_per_slot(rc, fp8), fp8, true) ||
+        !encode_kv_map(&da.tm_v, kv_cache, rows, 2, fp8, false))
       return MLA_ERR_INVALID_ARG;
   }
   da.kv_cache = kv_cache;

@@ -59,17 +59,14 @@ namespace mla {
 
 constexpr int kChunkBytes = 16384;   // one 64-column chunk of a tile: 128 rows x 128 B
 constexpr int kVSlotBytes = 32768;   // two chunks: 128 value columns
-constexpr int kKStageBytes = 8192;   // FP8 chunk: [128 rows][64 B]
-constexpr int kVStageBytes = 16384;  // FP8 chunk pair: [2][128 rows][64 B]
-constexpr int kChunksPerTile = 9;
+constexpr int kVStageBytes = 16384;  // raw FP8 pair: 2 halves x [8 groups][2 chunks][8 rows][64 B]
 constexpr int kPairsPerTile = 4;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kSoftmaxBar = 1;          // named barrier of the 4 softmax warps
-constexpr uint32_t kKLoadBar = 2;            // FP8 key load/dequant warps
-constexpr uint32_t kVLoadBar = 3;            // FP8 value load/dequant warps
-constexpr int kFp8Group = 64;                // threads per FP8 load/dequant group
+constexpr uint32_t kDequantBar = 2;          // FP8 dequantising warps 8-11
+constexpr int kDequantThreads = 128;
 constexpr int kSmemLimit = 232448;           // 227 KB per CTA
 constexpr int kStaticBudget = 3072;          // static shared memory (barriers, scratch)
 
@@ -84,10 +81,10 @@ struct Cfg {
   static constexpr int kPBytes = 128 * kPRow;
   static constexpr int kNumP = RC == 64 && FP8 ? 1 : 2;  // P^T buffers
   static constexpr uint32_t kPSwz = RC == 64 ? kSwizzle128 : RC == 32 ? kSwizzle64 : kSwizzle32;
-  static constexpr int kTmemCols = RC == 64 ? 512 : RC == 32 ? 256 : 128;
+  static constexpr int kTmemCols = FP8 || RC == 64 ? 512 : RC == 32 ? 256 : 128;
   static constexpr int kThreads = FP8 ? 384 : 256;
   static constexpr int kPvWarp = FP8 ? 0 : 3;           // warp of the PV issuing thread
-  static constexpr int KC = FP8 || RC == 64 ? 1 : 3;     // key chunks per K ring slot
+  static constexpr int KC = RC == 64 ? 1 : 3;            // key chunks per K ring slot
   static constexpr int kKSlotBytes = KC * kChunkBytes;
   static constexpr int kSlotsPerTile = 9 / KC;
   // Ring layouts, as strides of the MMA operand descriptors. bf16 (TMA boxes): a key slot
@@ -97,14 +94,20 @@ struct Cfg {
   static constexpr uint32_t kKChunkStride = FP8 ? kChunkBytes : 1024;
   static constexpr uint32_t kVChunkStride = FP8 ? kChunkBytes : 1024;  // value operand LBO
   static constexpr uint32_t kVGroupStride = FP8 ? 1024 : 2048;         // value operand SBO
-  static constexpr int NK = FP8 || RC < 64 ? 2 : 3;
-  static constexpr int NV = FP8 ? (RC == 64 ? 1 : 2) : (RC == 16 ? 3 : 2);
-  static constexpr int NKS = FP8 ? (RC == 16 ? 8 : RC == 32 ? 5 : 4) : 0;   // staging depth
+  // FP8: the dequantised key slots live in tensor memory after S^T (2 RC columns) and
+  // O^T (4 RC columns), KC chunks x 32 columns each (two fp16 per 32-bit column)
+  static constexpr int kKTmemBase = 6 * RC;
+  static constexpr int kKTmemSlotCols = KC * 32;
+  static constexpr int NK = FP8 ? (RC == 32 ? 3 : 4) : (RC < 64 ? 2 : 3);
+  static constexpr int NV = RC == 16 ? 3 : 2;
+  static constexpr int kKStageBytes = KC * 8192;        // raw FP8 key position: 2 halves x KC x 4 KB
+  static constexpr int NKS = FP8 ? (RC == 64 ? 3 : 2) : 0;   // raw staging depths
   static constexpr int NVS = FP8 ? 2 : 0;
-  static constexpr int kKLoaders = FP8 ? kFp8Group : 1;   // arrivals that fill a K slot
-  static constexpr int kVLoaders = FP8 ? kFp8Group : 1;
+  static constexpr int kKLoaders = FP8 ? 4 : 1;         // arrivals that fill a K slot
+  static constexpr int kVLoaders = FP8 ? 4 : 1;
+  static_assert(!FP8 || kKTmemBase + NK * kKTmemSlotCols <= 512, "tensor memory budget");
   static_assert(kSlotsPerTile * KC == 9, "a tile is 9 chunks");
-  static constexpr int kDynBytes = 1024 + kQBytes + kNumP * kPBytes + NK * kKSlotBytes +
+  static constexpr int kDynBytes = 1024 + kQBytes + kNumP * kPBytes + (FP8 ? 0 : NK * kKSlotBytes) +
                                    NV * kVSlotBytes + NKS * kKStageBytes + NVS * kVStageBytes;
   static_assert(kDynBytes + kStaticBudget <= kSmemLimit, "shared memory budget");
 };
@@ -152,19 +155,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
   }
-}
-
-// ------------------------------------------------------------------------ cp.async
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-// Wait until at most N of this thread's most recent cp.async groups are still pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
 }
 
 // Walks the key tiles of this CTA's units in the order every role consumes them, with
@@ -221,36 +211,6 @@ __device__ __forceinline__ bool iter_next(TileIter& it, const DecodeArgs& a, int
   return true;
 }
 
-// E4M3 -> fp16 of one 64-column chunk (128 rows) from a row-major staging buffer
-// [128 rows][64 B] into the 128-byte-swizzled MMA layout [128 rows][128 B]. Rows at or
-// past `valid` are written as zeros (and their staging bytes never read). G threads.
-template <int G>
-__device__ __forceinline__ void dequant_chunk(const uint8_t* src, uint8_t* dst, int valid, int t) {
-#pragma unroll
-  for (int it = 0; it < 512 / G; ++it) {
-    const int uidx = it * G + t;          // 512 16-byte FP8 units per chunk
-    const int row = uidx >> 2, q4 = uidx & 3;
-    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-    if (row < valid) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src + row * 64 + q4 * 16);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t hh[8];
-#pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2) {
-        __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k2] & 0xFFFFu), __NV_E4M3);
-        __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k2] >> 16), __NV_E4M3);
-        hh[2 * k2] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-        hh[2 * k2 + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
-      }
-      o0 = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-      o1 = make_uint4(hh[4], hh[5], hh[6], hh[7]);
-    }
-    uint8_t* drow = dst + (row >> 3) * 1024 + (row & 7) * 128;
-    *reinterpret_cast<uint4*>(drow + (((2 * q4) ^ (row & 7)) << 4)) = o0;
-    *reinterpret_cast<uint4*>(drow + (((2 * q4 + 1) ^ (row & 7)) << 4)) = o1;
-  }
-}
-
 template <int RC, bool FP8>
 __global__ void __launch_bounds__(Cfg<RC, FP8>::kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeArgs a) {
@@ -262,6 +222,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ uint8_t dsmem_raw[];
   __shared__ __align__(8) uint64_t bar_kfull[NK], bar_kempty[NK], bar_vfull[NV], bar_vempty[NV];
   __shared__ __align__(8) uint64_t bar_qfull, bar_qready, bar_qempty;
+  __shared__ __align__(8) uint64_t bar_kstage[NKS], bar_vstage[NVS];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_s_empty[2], bar_p_full[NP], bar_pv[NP];
   __shared__ __align__(8) uint64_t bar_o_empty, bar_drain[2], bar_vaux;
   __shared__ uint32_t tmem_base_s;
@@ -281,12 +242,11 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const uint32_t sQ = base;
   const uint32_t sP = sQ + C::kQBytes;
   const uint32_t sK = sP + NP * C::kPBytes;
-  const uint32_t sV = sK + NK * C::kKSlotBytes;
+  const uint32_t sV = sK + (FP8 ? 0 : NK * C::kKSlotBytes);
   const uint32_t sKS = sV + NV * kVSlotBytes;
-  const uint32_t sVS = sKS + (FP8 ? NKS * kKStageBytes : 0);
+  const uint32_t sVS = sKS + (FP8 ? NKS * C::kKStageBytes : 0);
   uint8_t* gQ = gbase;
   uint8_t* gP = gbase + (sP - sQ);
-  uint8_t* gK = gbase + (sK - sQ);
   uint8_t* gV = gbase + (sV - sQ);
   uint8_t* gKS = gbase + (sKS - sQ);
   uint8_t* gVS = gbase + (sVS - sQ);
@@ -295,6 +255,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const uint32_t b_vfull = smem_u32(bar_vfull), b_vempty = smem_u32(bar_vempty);
   const uint32_t b_qfull = smem_u32(&bar_qfull), b_qready = smem_u32(&bar_qready);
   const uint32_t b_qempty = smem_u32(&bar_qempty);
+  const uint32_t b_kstage = smem_u32(bar_kstage), b_vstage = smem_u32(bar_vstage);
   const uint32_t b_s_full = smem_u32(bar_s_full), b_s_empty = smem_u32(bar_s_empty);
   const uint32_t b_p_full = smem_u32(bar_p_full), b_pv = smem_u32(bar_pv);
   const uint32_t b_oempty = smem_u32(&bar_o_empty), b_drain = smem_u32(bar_drain);
@@ -312,7 +273,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       mbar_init(b_vempty + 8 * i, 1);
     }
     mbar_init(b_qfull, 1);
-    mbar_init(b_qready, kFp8Group);
+    mbar_init(b_qready, 64);
+    for (int i = 0; i < NKS; ++i) mbar_init(b_kstage + 8 * i, 1);
+    for (int i = 0; i < NVS; ++i) mbar_init(b_vstage + 8 * i, 1);
     mbar_init(b_qempty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_s_full + 8 * i, 1);
@@ -329,10 +292,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     abort_s = 0u;
     fence_mbarrier_init();
     tma_prefetch_desc(&a.tm_q);
-    if (!FP8) {
-      tma_prefetch_desc(&a.tm_k);
-      tma_prefetch_desc(&a.tm_v);
-    }
+    tma_prefetch_desc(&a.tm_k);
+    tma_prefetch_desc(&a.tm_v);
   }
   if (warp == 0) tmem_alloc(smem_u32(&tmem_base_s), C::kTmemCols);
   tc_fence_before();
@@ -356,7 +317,6 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   auto wait_softmax = [&](uint32_t bar, uint32_t parity) -> bool {
     return !named_bar_or(kSoftmaxBar, 128, !wait(bar, parity));
   };
-  const uint8_t* cache = static_cast<const uint8_t*>(a.kv_cache);
   if (!FP8 && warp == 0) {
     // ============================================================ key producer (bf16)
     // One thread: every key slot of every tile is two TMA boxes (one per 64-row page
@@ -461,16 +421,31 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
             ok = wait(b_kfull + 8 * ks, (kp / NK) & 1);
             if (!ok) break;
             tc_fence_after();
-            const uint64_t ad0 = dK0 + (uint64_t)(ks * (C::kKSlotBytes >> 4));
+            if (FP8) {
+              // keys dequantised into tensor memory: 8 columns per K = 16 step
+              const uint32_t at0 = tmem + C::kKTmemBase + ks * C::kKTmemSlotCols;
 #pragma unroll
-            for (int cc = 0; cc < C::KC; ++cc) {
-              const int c = sl * C::KC + cc;
-              const uint64_t ad = ad0 + (uint64_t)(cc * (C::kKChunkStride >> 4));
-              const uint64_t bd = dQ0 + (uint64_t)(c * (RC * 128 >> 4));
-              umma_f16(d, ad, bd, idesc_qk, c != 0);
-              umma_f16(d, ad + 2, bd + 2, idesc_qk, 1);
-              umma_f16(d, ad + 4, bd + 4, idesc_qk, 1);
-              umma_f16(d, ad + 6, bd + 6, idesc_qk, 1);
+              for (int cc = 0; cc < C::KC; ++cc) {
+                const int c = sl * C::KC + cc;
+                const uint64_t bd = dQ0 + (uint64_t)(c * (RC * 128 >> 4));
+                const uint32_t at = at0 + cc * 32;
+                umma_f16_ts(d, at, bd, idesc_qk, c != 0);
+                umma_f16_ts(d, at + 8, bd + 2, idesc_qk, 1);
+                umma_f16_ts(d, at + 16, bd + 4, idesc_qk, 1);
+                umma_f16_ts(d, at + 24, bd + 6, idesc_qk, 1);
+              }
+            } else {
+              const uint64_t ad0 = dK0 + (uint64_t)(ks * (C::kKSlotBytes >> 4));
+#pragma unroll
+              for (int cc = 0; cc < C::KC; ++cc) {
+                const int c = sl * C::KC + cc;
+                const uint64_t ad = ad0 + (uint64_t)(cc * (C::kKChunkStride >> 4));
+                const uint64_t bd = dQ0 + (uint64_t)(c * (RC * 128 >> 4));
+                umma_f16(d, ad, bd, idesc_qk, c != 0);
+                umma_f16(d, ad + 2, bd + 2, idesc_qk, 1);
+                umma_f16(d, ad + 4, bd + 4, idesc_qk, 1);
+                umma_f16(d, ad + 6, bd + 6, idesc_qk, 1);
+              }
             }
             umma_commit(b_kempty + 8 * ks);
           }
@@ -741,9 +716,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     const int gi = threadIdx.x - 64;                    // 0..63
     uint32_t ucount = 0;
     for (int u = u0; u < u1; ++u, ++ucount) {
-      if (!wait(b_qfull, ucount & 1)) break;
+      if (!wait_warp(b_qfull, ucount & 1)) break;
       bool q_bad = false;
-      for (int i = gi; i < C::kQBytes / 16; i += kFp8Group) {
+      for (int i = gi; i < C::kQBytes / 16; i += 64) {
         uint4* q = reinterpret_cast<uint4*>(gQ + 16 * i);
         uint4 v = *q;
         uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -762,84 +737,151 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     }
   } else if (FP8 && warp >= 8) {
     // ============================================================ FP8 load + dequant
-    // Warps 8-9: key chunks; warps 10-11: value chunk pairs. Each group prefetches its
-    // E4M3 rows with cp.async into a staging ring (NKS / NVS positions deep), then
-    // converts position p into the fp16 MMA ring and arrives on its slot.
-    const bool keys = warp < 10;
-    const int gi = threadIdx.x - (keys ? 256 : 320);    // 0..63
-    const uint32_t gbar = keys ? kKLoadBar : kVLoadBar;
-    constexpr int G = kFp8Group;
-    // Issue the copies of one position (chunk c of a tile for keys, pair c for values).
-    // thread gi owns staging rows gi/4 + 16k (k = 0..7) at 16-byte column gi%4.
-    const int fr0 = gi >> 2, fq = gi & 3;
-    auto issue = [&](const TileIter& it, int c, uint32_t stage) {
-      const int valid = it.U.L - it.tile * kTileTokens;
-      const uint8_t* s0 = cache + (it.rb0 + fr0) * kDQK + fq * 16;
-      const uint8_t* s1 = cache + (it.rb1 + fr0) * kDQK + fq * 16;
-      const uint32_t d0 = stage + gi * 16;
-#pragma unroll
-      for (int sub = 0; sub < (keys ? 1 : 2); ++sub) {
-        const int chunk = keys ? c : 2 * c + sub;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int row = fr0 + 16 * k;
-          if (row < valid && (k < 4 ? it.rb0 : it.rb1) >= 0)
-            cp_async16(d0 + sub * kKStageBytes + k * 1024,
-                       (k < 4 ? s0 : s1) + (16 * (k & 3)) * kDQK + chunk * 64);
-        }
+    // Warps 8-11, one thread per key row of the tile (thread gi = tensor-memory lane gi).
+    // Per tile n: the key positions of tile n (KC chunks each) are converted from the raw
+    // staging ring into a tensor-memory key slot (the QK^T MMAs read A from there), then
+    // the value chunk pairs of tile n-1 are converted into the fp16 value ring in shared
+    // memory. Raw rows are fetched by thread 0 with TMA boxes (one per 64-row page half)
+    // as far ahead as the staging rings allow; E4M3 -> fp16 is exact. Value rows past the
+    // sequence end are written as zeros; key rows past it are masked by the softmax.
+    const int gi = threadIdx.x - 256;                   // 0..127 = key row = TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(warp & 3) << 21);   // (32 * (warp % 4)) << 16
+    TileIter kc, vc, ki, vi;                            // key/value consume and issue cursors
+    bool kmore = iter_begin(kc, a, u0, u1, err, false);
+    bool vmore = iter_begin(vc, a, u0, u1, err, false);
+    bool kimore = gi == 0 && iter_begin(ki, a, u0, u1, err, false);
+    bool vimore = gi == 0 && iter_begin(vi, a, u0, u1, err, false);
+    int kic = 0, vic = 0;
+    uint32_t kip = 0, vip = 0, kcp = 0, vcp = 0;        // positions issued / consumed
+    // thread 0 keeps both staging rings full: a slot is free once its position is consumed
+    auto top_up = [&]() {
+      while (kimore && kip < kcp + NKS) {
+        const uint32_t sl = kip % NKS, bar = b_kstage + 8 * sl, dst = sKS + sl * C::kKStageBytes;
+        const uint32_t nbox = (ki.rb0 >= 0 ? 1u : 0u) + (ki.rb1 >= 0 ? 1u : 0u);
+        mbar_arrive_expect_tx(bar, nbox * (C::kKStageBytes / 2));
+        if (ki.rb0 >= 0) tma_load_4d(dst, &a.tm_k, bar, 0, 0, kic * C::KC, (int32_t)(ki.rb0 >> 3));
+        if (ki.rb1 >= 0)
+          tma_load_4d(dst + C::kKStageBytes / 2, &a.tm_k, bar, 0, 0, kic * C::KC, (int32_t)(ki.rb1 >> 3));
+        if (++kic == C::kSlotsPerTile) { kic = 0; kimore = iter_next(ki, a, u1, err, false); }
+        ++kip;
+      }
+      while (vimore && vip < vcp + NVS) {
+        const uint32_t sl = vip % NVS, bar = b_vstage + 8 * sl, dst = sVS + sl * kVStageBytes;
+        const uint32_t nbox = (vi.rb0 >= 0 ? 1u : 0u) + (vi.rb1 >= 0 ? 1u : 0u);
+        mbar_arrive_expect_tx(bar, nbox * (kVStageBytes / 2));
+        if (vi.rb0 >= 0) tma_load_4d(dst, &a.tm_v, bar, 0, 0, 2 * vic, (int32_t)(vi.rb0 >> 3));
+        if (vi.rb1 >= 0) tma_load_4d(dst + kVStageBytes / 2, &a.tm_v, bar, 0, 0, 2 * vic, (int32_t)(vi.rb1 >> 3));
+        if (++vic == kPairsPerTile) { vic = 0; vimore = iter_next(vi, a, u1, err, false); }
+        ++vip;
       }
     };
-    auto run = [&](auto NS_T, auto ND_T, uint32_t full, uint32_t empty, uint32_t ring,
-                   uint8_t* gring, uint32_t slot_bytes, uint32_t stage0, uint8_t* gstage0,
-                   uint32_t stage_bytes, int per_tile) {
-      constexpr int NS = decltype(NS_T)::value;      // staging depth
-      constexpr int ND = decltype(ND_T)::value;      // fp16 ring depth
-      TileIter ii, ci;                               // issue / consume cursors
-      bool imore = iter_begin(ii, a, u0, u1, err, false);
-      bool cmore = iter_begin(ci, a, u0, u1, err, false);
-      int ic = 0, cc = 0;
-      uint32_t ip = 0, cp = 0;
-      bool ok = true;
-      for (int k = 0; k < NS - 1; ++k) {             // prologue: NS-1 positions ahead
-        if (imore) {
-          issue(ii, ic, stage0 + (ip % NS) * stage_bytes);
-          if (++ic == per_tile) { ic = 0; imore = iter_next(ii, a, u1, err, false); }
-          ++ip;
+    bool ok = true, first = true;
+    // staging row gi of a key position: half gi/64, group (gi/8)%8, row gi%8; its four
+    // 16-byte units are 64-byte swizzled by row (TMA swizzle mode of the key map)
+    const int kr7 = gi & 7;
+    const uint32_t krow_off = (uint32_t)(gi >> 6) * (C::kKStageBytes / 2) + ((gi >> 3) & 7) * (C::KC * 512) + kr7 * 64;
+    while (ok) {
+      const bool doK = kmore;
+      if (doK) {
+        for (int sl = 0; sl < C::kSlotsPerTile && ok; ++sl) {
+          if (gi == 0) top_up();
+          const uint32_t st = kcp % NKS, ks = kcp % NK;
+          ok = wait(b_kstage + 8 * st, (kcp / NKS) & 1);
+          ok = ok && wait(b_kempty + 8 * ks, ((kcp / NK) & 1) ^ 1);
+          if (ok) {
+            tc_fence_after();
+            const uint8_t* src = gKS + st * C::kKStageBytes + krow_off;
+            const uint32_t tbase = lane_base + C::kKTmemBase + ks * C::kKTmemSlotCols;
+#pragma unroll
+            for (int cc = 0; cc < C::KC; ++cc) {
+              uint32_t w[32];
+#pragma unroll
+              for (int u16 = 0; u16 < 4; ++u16) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + cc * 512 + ((u16 ^ ((kr7 >> 1) & 3)) << 4));
+                const uint32_t b4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) {
+                  __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b4[k2] & 0xFFFFu), __NV_E4M3);
+                  __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b4[k2] >> 16), __NV_E4M3);
+                  w[8 * u16 + 2 * k2] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+                  w[8 * u16 + 2 * k2 + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+                }
+              }
+              tmem_st16u(tbase + cc * 32, w);
+              tmem_st16u(tbase + cc * 32 + 16, w + 16);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_kfull + 8 * ks);
+          }
+          ok = !named_bar_or(kDequantBar, kDequantThreads, !ok);   // staging slot released
+          ++kcp;
         }
-        cp_async_commit();
+        if (ok) kmore = iter_next(kc, a, u1, err, false);
       }
-      while (cmore && ok) {
-        if (imore) {
-          issue(ii, ic, stage0 + (ip % NS) * stage_bytes);
-          if (++ic == per_tile) { ic = 0; imore = iter_next(ii, a, u1, err, false); }
-          ++ip;
+      const bool doV = ok && vmore && (!first || !doK);   // values lag the keys by one tile
+      if (doV) {
+        const int valid = vc.U.L - vc.tile * kTileTokens;
+        for (int j = 0; j < kPairsPerTile && ok; ++j) {
+          if (gi == 0) top_up();
+          const uint32_t st = vcp % NVS, vs = vcp % NV;
+          ok = wait(b_vstage + 8 * st, (vcp / NVS) & 1);
+          ok = ok && wait(b_vempty + 8 * vs, ((vcp / NV) & 1) ^ 1);
+          if (ok) {
+            // unit idx: chunk idx / 512, row (idx % 512) / 4, 16-byte column idx % 4;
+            // staging row r of chunk c at half r / 64, group (r / 8) % 8, row r % 8
+            const uint8_t* src = gVS + st * kVStageBytes;
+            uint8_t* dst = gV + vs * kVSlotBytes;
+#pragma unroll 1
+            for (int base = gi; base < 1024; base += 4 * kDequantThreads) {
+              uint4 v[4];
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                const int idx = base + jj * kDequantThreads, row = (idx & 511) >> 2;
+                v[jj] = make_uint4(0, 0, 0, 0);
+                if (row < valid)
+                  v[jj] = *reinterpret_cast<const uint4*>(src + (row >> 6) * (kVStageBytes / 2) +
+                                                          ((row >> 3) & 7) * 1024 + (idx >> 9) * 512 +
+                                                          (row & 7) * 64 + (idx & 3) * 16);
+              }
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                const int idx = base + jj * kDequantThreads, row = (idx & 511) >> 2, q4 = idx & 3;
+                const uint32_t b4[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+                uint32_t hh[8];
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) {
+                  __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b4[k2] & 0xFFFFu), __NV_E4M3);
+                  __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b4[k2] >> 16), __NV_E4M3);
+                  hh[2 * k2] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+                  hh[2 * k2 + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+                }
+                uint8_t* drow = dst + (idx >> 9) * kChunkBytes + (row >> 3) * 1024 + (row & 7) * 128;
+                *reinterpret_cast<uint4*>(drow + (((2 * q4) ^ (row & 7)) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                *reinterpret_cast<uint4*>(drow + (((2 * q4 + 1) ^ (row & 7)) << 4)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_vfull + 8 * vs);
+          }
+          ok = !named_bar_or(kDequantBar, kDequantThreads, !ok);
+          ++vcp;
         }
-        cp_async_commit();
-        cp_async_wait<NS - 1>();                     // this thread's copies of position cp
-        named_bar_sync(gbar, G);                     // everyone's copies of position cp
-        const uint32_t slot = cp % ND;
-        ok = wait(empty + 8 * slot, ((cp / ND) & 1) ^ 1);
-        if (ok) {
-          const int valid = ci.U.L - ci.tile * kTileTokens;
-          const uint8_t* src = gstage0 + (cp % NS) * stage_bytes;
-          uint8_t* dst = gring + slot * slot_bytes;
-          dequant_chunk<G>(src, dst, valid, gi);
-          if (!keys) dequant_chunk<G>(src + kKStageBytes, dst + kChunkBytes, valid, gi);
-          fence_proxy_async_smem();
-          mbar_arrive(full + 8 * slot);
-        }
-        ok = !named_bar_or(gbar, G, !ok);            // staging slot free for reuse; agree on ok
-        if (++cc == per_tile) { cc = 0; cmore = iter_next(ci, a, u1, err, false); }
-        ++cp;
+        if (ok) vmore = iter_next(vc, a, u1, err, false);
       }
-      cp_async_wait<0>();
-    };
-    if (keys)
-      run(std::integral_constant<int, NKS>{}, std::integral_constant<int, NK>{}, b_kfull, b_kempty, sK, gK,
-          C::kKSlotBytes, sKS, gKS, kKStageBytes, kChunksPerTile);
-    else
-      run(std::integral_constant<int, NVS>{}, std::integral_constant<int, NV>{}, b_vfull, b_vempty, sV, gV,
-          kVSlotBytes, sVS, gVS, kVStageBytes, kPairsPerTile);
+      first = false;
+      if (!doK && !doV) break;
+    }
+    // loads issued but not consumed (only after a failed wait) land before exit
+    if (gi == 0) {
+      volatile uint32_t no_abort = 0;
+      for (uint32_t q = kcp; q < kip; ++q)
+        mbar_wait(b_kstage + 8 * (q % NKS), (q / NKS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
+      for (uint32_t q = vcp; q < vip; ++q)
+        mbar_wait(b_vstage + 8 * (q % NVS), (q / NVS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
+    }
   }
 
   // ============================================================ teardown

@@ -65,9 +65,9 @@ struct SchedArgs {
 
 struct DecodeArgs {
   CUtensorMap tm_q;      // q as [B][R][576], 64 x RC x 1 boxes, 128-byte swizzle
-  // bf16 cache viewed as [Np*P/8 row groups][9 chunks][8 rows][64 columns] (strides 9216,
-  // 128, 1152 bytes): a box of KC (keys) or 2 (values) chunks x 64 rows lands in shared
-  // memory as [group][chunk][8 rows x 128 B], 128-byte swizzle
+  // the cache viewed as [Np*P/8 row groups][9 chunks][8 rows][64 columns]: a box of KC
+  // (keys) or 2 (values) chunks x 64 rows lands in shared memory as
+  // [group][chunk][8 rows][64 columns] (bf16: 128-byte swizzle; E4M3: plain)
   CUtensorMap tm_k, tm_v;
   const void* kv_cache;  // [Np][P][576] bf16 or E4M3 bytes
   const int32_t* block_table;

@@ -46,36 +46,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test: has the phase of `bar` with the given parity completed?
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+// The same, but a thread whose phase is still open is suspended (it issues nothing) until
+// the phase completes or `hint_ns` nanoseconds have passed.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile("{\n\t.reg .pred p;\n\t"
-               "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
                "selp.u32 %0, 1, 0, p;\n\t}"
-               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+               : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
   return ok != 0;
 }
 
-// Wait for the phase of `bar` with the given parity to complete. Bounded: after
-// `kWaitLimitNs` of wall time the wait gives up, ORs `timeout_bit` into the global
-// error word, raises the CTA-wide abort flag and returns false. A raised abort flag
-// also ends every other wait at once, so a stalled pipeline never hangs the GPU.
+// Wait for the phase of `bar` with the given parity to complete. The waiting thread
+// sleeps in the barrier (woken when the phase completes) rather than spinning, so that
+// waiting warps take no issue slots from working ones. Bounded: after `kWaitLimitNs` of
+// wall time the wait gives up, ORs `timeout_bit` into the global error word, raises the
+// CTA-wide abort flag and returns false. A raised abort flag also ends every other wait
+// (within one sleep period), so a stalled pipeline never hangs the GPU.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr uint32_t kSleepHintNs = 200000u;         // longest single sleep: 0.2 ms
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile uint32_t* abort_flag,
                                           uint32_t* err_word, uint32_t timeout_bit) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1u;
-        atomicOr(err_word, timeout_bit);
-        return false;
-      }
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1u;
+      atomicOr(err_word, timeout_bit);
+      return false;
     }
   }
 }
@@ -177,6 +179,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// The same store for 16 raw 32-bit words.
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+               "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                  "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
+                  "r"(v[13]), "r"(v[14]), "r"(v[15])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -189,6 +200,16 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
                "setp.ne.b32 p, %4, 0;\n\t"
                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
                :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+               : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]: A is M lanes x K (two 16-bit values per 32-bit
+// column, K-ordered), so one K = 16 step spans 8 columns.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "setp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+               :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
                : "memory");
 }
 // Arrive once on `bar` when every tcgen05 op this thread issued so far has completed.

@@ -10,6 +10,10 @@
 //      with the second chunk LBO = 16 KB away and 8-key groups SBO = 1 KB apart
 //   P: written by threads (thread = key row) with the swizzle of an N*2-byte row: MN-major B
 //   8 MMAs of K = 16 keys, advancing 2 KB (A) and 16 rows (B).
+// mode 2 ("scores, A in tensor memory"): D[128 x N] = A[128 x 64] . B[N x 64]^T with A
+//   written by the threads into tensor memory (thread t = row t = TMEM lane t, two bf16
+//   per 32-bit column, columns 64..95) and B as in mode 0; 4 MMAs of K = 16, the A
+//   address advancing 8 columns.
 // All waits are bounded; out-of-range modes return an error before launching.
 #include <cstdint>
 #include <cstring>
@@ -56,7 +60,22 @@ __global__ void __launch_bounds__(128, 1) probe_kernel(const __grid_constant__ C
   const uint32_t tmem = tmem_s;
   volatile uint32_t* ab = &abort_s;
 
-  if (mode == 0) {
+  if (mode == 2) {
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(bt, N * 128);
+      tma_load_2d(sB, &tma_b, bt, 0, 0);
+    }
+    const int t = threadIdx.x;
+    uint32_t w[32];
+    const uint32_t* arow = reinterpret_cast<const uint32_t*>(p_glob + t * 64);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = arow[i];
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    tmem_st16u(lane_base + 64, w);
+    tmem_st16u(lane_base + 80, w + 16);
+    tmem_wait_st();
+    tc_fence_before();
+  } else if (mode == 0) {
     if (threadIdx.x == 0) {
       mbar_arrive_expect_tx(bt, 2 * 8192 + N * 128);
       tma_load_2d(sA, &tma_a, bt, 0, 0);
@@ -81,7 +100,13 @@ __global__ void __launch_bounds__(128, 1) probe_kernel(const __grid_constant__ C
   bool ok = mbar_wait(bt, 0, ab, err, 1u);
   if (ok && threadIdx.x == 0) {
     tc_fence_after();
-    if (mode == 0) {
+    if (mode == 2) {
+      const uint32_t idesc = make_idesc(128, N, 1, 0, 0);
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t bd = make_sdesc(sB + kk * 32, 16, 1024, kSwizzle128);
+        umma_f16_ts(tmem, tmem + 64 + kk * 8, bd, idesc, kk > 0);
+      }
+    } else if (mode == 0) {
       const uint32_t idesc = make_idesc(128, N, 1, 0, 0);
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t ad = make_sdesc(sA + kk * 32, 16, 1024, kSwizzle128);
@@ -146,18 +171,22 @@ static int make_map(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t row
 extern "C" __attribute__((visibility("default"))) int umma_probe(int mode, int n, const void* a,
                                                                  const void* b, float* d,
                                                                  uint32_t* err, cudaStream_t s) {
-  if ((mode != 0 && mode != 1) || (n != 16 && n != 32 && n != 64) || !a || !b || !d || !err) return -1;
+  if ((mode < 0 || mode > 2) || (n != 16 && n != 32 && n != 64) || !a || !b || !d || !err) return -1;
   if (!encoder()) return -2;
   CUtensorMap ta, tb;
   std::memset(&tb, 0, sizeof(tb));
+  const __nv_bfloat16* pg = static_cast<const __nv_bfloat16*>(b);
   if (mode == 0) {
     if (make_map(&ta, a, 64, 128, 64, 64) || make_map(&tb, b, 64, n, 64, n)) return -3;
+  } else if (mode == 2) {
+    if (make_map(&tb, b, 64, n, 64, n)) return -3;
+    ta = tb;
+    pg = static_cast<const __nv_bfloat16*>(a);
   } else {
     if (make_map(&ta, a, 128, 128, 64, 64)) return -3;
     tb = ta;
   }
   const int smem = 32768 + 16384 + 1024;
-  const __nv_bfloat16* pg = static_cast<const __nv_bfloat16*>(b);
   cudaError_t e;
   switch (n) {
     case 16:

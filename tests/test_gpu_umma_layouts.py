@@ -2,6 +2,8 @@
 
 Scores: K-major A and B with 128-byte swizzle, K advanced inside the swizzle atom.
 Values: MN-major A (two 64-column chunks) and MN-major B written with the P^T row swizzle.
+Scores with A in tensor memory: the rows written by the threads into TMEM lanes, two
+16-bit values per 32-bit column (the FP8 path's dequantised keys).
 A failure here localises a decode mismatch to one operand layout.
 """
 import ctypes
@@ -53,4 +55,14 @@ def test_values_layout(probe, n):
     p = torch.rand(128, n, generator=g).to(torch.bfloat16).cuda()
     d = run(probe, 1, n, v, p)
     ref = v.double().T @ p.double()
+    assert torch.allclose(d.double(), ref, atol=1e-3, rtol=1e-4), (d - ref).abs().max()
+
+
+@pytest.mark.parametrize("n", [16, 32, 64])
+def test_scores_layout_a_in_tensor_memory(probe, n):
+    g = torch.Generator().manual_seed(200 + n)
+    a = torch.randn(128, 64, generator=g).to(torch.bfloat16).cuda()
+    b = torch.randn(n, 64, generator=g).to(torch.bfloat16).cuda()
+    d = run(probe, 2, n, a, b)
+    ref = a.double() @ b.double().T
     assert torch.allclose(d.double(), ref, atol=1e-3, rtol=1e-4), (d - ref).abs().max()
