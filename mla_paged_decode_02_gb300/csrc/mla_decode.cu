@@ -65,8 +65,11 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kSoftmaxBar = 1;          // named barrier of the 4 softmax warps
-constexpr uint32_t kDequantBar = 2;          // FP8 dequantising warps 8-11
-constexpr int kDequantThreads = 128;
+constexpr uint32_t kKeyDqBar = 2;            // FP8 key dequantising warps 8-11
+constexpr uint32_t kValDqBar = 3;            // FP8 value dequantising warps 2-3
+constexpr int kKeyDqThreads = 128;
+constexpr int kValDqThreads = 64;
+constexpr float kValueDqScale = 256.f;       // FP8 values are converted as value * 2^-8
 constexpr int kSmemLimit = 232448;           // 227 KB per CTA
 constexpr int kStaticBudget = 3072;          // static shared memory (barriers, scratch)
 
@@ -104,7 +107,7 @@ struct Cfg {
   static constexpr int NKS = FP8 ? (RC == 64 ? 3 : 2) : 0;   // raw staging depths
   static constexpr int NVS = FP8 ? 2 : 0;
   static constexpr int kKLoaders = FP8 ? 4 : 1;         // arrivals that fill a K slot
-  static constexpr int kVLoaders = FP8 ? 4 : 1;
+  static constexpr int kVLoaders = 1;
   static_assert(!FP8 || kKTmemBase + NK * kKTmemSlotCols <= 512, "tensor memory budget");
   static_assert(kSlotsPerTile * KC == 9, "a tile is 9 chunks");
   static constexpr int kDynBytes = 1024 + kQBytes + kNumP * kPBytes + (FP8 ? 0 : NK * kKSlotBytes) +
@@ -211,6 +214,48 @@ __device__ __forceinline__ bool iter_next(TileIter& it, const DecodeArgs& a, int
   return true;
 }
 
+// One raw E4M3 value chunk pair (staging [half][8 groups][2 chunks][8 rows][64 B]) into an
+// fp16 value slot ([chunk][16 groups][8 rows][128 B], 128-byte swizzle), G threads. The
+// conversion is integer-only, so it does not compete with the key conversions: for an E4M3
+// byte b = s eeee mmm, (b + (b & 0x80)) << 7 is the fp16 s 0eeee mmm0000000, exactly the
+// byte's value times 2^-8 (E4M3 subnormals become fp16 subnormals); two bytes are done at
+// once in the 16-bit halves of a word. The factor 2^8 is folded into the output. (An E4M3
+// NaN in a value column becomes a finite number here; the same byte is a key column too,
+// whose exact conversion makes that key's score, and so the row's output, NaN.) Rows at or
+// past `valid` are written as zeros.
+template <int G>
+__device__ __forceinline__ void convert_value_pair(const uint8_t* src, uint8_t* dst, int valid, int gi) {
+  constexpr int kPer = 1024 / G;                 // 16-byte units per thread
+  constexpr int kRound = kPer > 8 ? 8 : kPer;
+#pragma unroll 1
+  for (int r0 = 0; r0 < kPer; r0 += kRound) {
+    uint4 v[kRound];
+#pragma unroll
+    for (int jj = 0; jj < kRound; ++jj) {
+      const int idx = gi + (r0 + jj) * G, row = (idx & 511) >> 2;   // chunk idx / 512, column idx % 4
+      v[jj] = make_uint4(0, 0, 0, 0);
+      if (row < valid)
+        v[jj] = *reinterpret_cast<const uint4*>(src + (row >> 6) * (kVStageBytes / 2) + ((row >> 3) & 7) * 1024 +
+                                                (idx >> 9) * 512 + (row & 7) * 64 + (idx & 3) * 16);
+    }
+#pragma unroll
+    for (int jj = 0; jj < kRound; ++jj) {
+      const int idx = gi + (r0 + jj) * G, row = (idx & 511) >> 2, q4 = idx & 3;
+      const uint32_t b4[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
+      uint32_t hh[8];
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        const uint32_t t0 = __byte_perm(b4[k2], 0u, 0x4140u), t1 = __byte_perm(b4[k2], 0u, 0x4342u);
+        hh[2 * k2] = ((t0 & 0x00800080u) + t0) << 7;
+        hh[2 * k2 + 1] = ((t1 & 0x00800080u) + t1) << 7;
+      }
+      uint8_t* drow = dst + (idx >> 9) * kChunkBytes + (row >> 3) * 1024 + (row & 7) * 128;
+      *reinterpret_cast<uint4*>(drow + (((2 * q4) ^ (row & 7)) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+      *reinterpret_cast<uint4*>(drow + (((2 * q4 + 1) ^ (row & 7)) << 4)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
+    }
+  }
+}
+
 template <int RC, bool FP8>
 __global__ void __launch_bounds__(Cfg<RC, FP8>::kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeArgs a) {
@@ -273,7 +318,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       mbar_init(b_vempty + 8 * i, 1);
     }
     mbar_init(b_qfull, 1);
-    mbar_init(b_qready, 64);
+    mbar_init(b_qready, 4);
     for (int i = 0; i < NKS; ++i) mbar_init(b_kstage + 8 * i, 1);
     for (int i = 0; i < NVS; ++i) mbar_init(b_vstage + 8 * i, 1);
     mbar_init(b_qempty, 1);
@@ -511,6 +556,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     const uint32_t lane_addr = (uint32_t)(w4 * 32) << 16;
     const float kvs = FP8 ? __ldg(a.kv_scale) : 1.0f;
     const float c_log2 = a.softmax_scale * kvs * kLog2e;
+    const float kvo = FP8 ? kvs * kValueDqScale : 1.0f;   // value scale (exact power-of-2 fold)
     uint32_t gn = 0;
     bool ok = true;
     float lsum[RC];
@@ -648,7 +694,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       if (t < RC) {
         const float tot = (wmax_s[t] + wmax_s[RC + t]) + (wmax_s[2 * RC + t] + wmax_s[3 * RC + t]);
         tot_s[t] = tot;
-        alpha_s[t] = tot > 0.f ? kvs / tot : 0.f;     // the row's output factor
+        alpha_s[t] = tot > 0.f ? kvo / tot : 0.f;     // the row's output factor
       }
       named_bar_sync(kSoftmaxBar, 128);
       const bool direct = U.slot < 0;
@@ -711,49 +757,23 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       named_bar_sync(kSoftmaxBar, 128);
       gn += T;
     }
-  } else if (FP8 && (warp == 2 || warp == 3)) {
-    // ============================================================ Q bf16 -> fp16 (FP8)
-    const int gi = threadIdx.x - 64;                    // 0..63
-    uint32_t ucount = 0;
-    for (int u = u0; u < u1; ++u, ++ucount) {
-      if (!wait_warp(b_qfull, ucount & 1)) break;
-      bool q_bad = false;
-      for (int i = gi; i < C::kQBytes / 16; i += 64) {
-        uint4* q = reinterpret_cast<uint4*>(gQ + 16 * i);
-        uint4 v = *q;
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
-          q_bad |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
-          __half2 h = __floats2half2_rn(lo, hi);
-          w[k] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        *q = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      if (q_bad) atomicOr(err, MLA_DEVERR_Q_RANGE);
-      fence_proxy_async_smem();
-      mbar_arrive(b_qready);
-    }
   } else if (FP8 && warp >= 8) {
-    // ============================================================ FP8 load + dequant
+    // ============================================================ FP8 keys (+ Q)
     // Warps 8-11, one thread per key row of the tile (thread gi = tensor-memory lane gi).
-    // Per tile n: the key positions of tile n (KC chunks each) are converted from the raw
-    // staging ring into a tensor-memory key slot (the QK^T MMAs read A from there), then
-    // the value chunk pairs of tile n-1 are converted into the fp16 value ring in shared
-    // memory. Raw rows are fetched by thread 0 with TMA boxes (one per 64-row page half)
-    // as far ahead as the staging rings allow; E4M3 -> fp16 is exact. Value rows past the
-    // sequence end are written as zeros; key rows past it are masked by the softmax.
+    // Every key position (KC chunks) is converted from its raw staging slot into a
+    // tensor-memory key slot, which the QK^T MMAs read as their A operand (E4M3 -> fp16 is
+    // exact; key rows past the sequence end are masked by the softmax). At the start of
+    // each unit the group converts that unit's Q from bf16 to fp16 in place.
+    // Thread 0 does the waits (the group barrier passes them on), then refills the raw
+    // staging slots the group has just finished reading, with TMA boxes (one per 64-row
+    // page half).
     const int gi = threadIdx.x - 256;                   // 0..127 = key row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp & 3) << 21);   // (32 * (warp % 4)) << 16
-    TileIter kc, vc, ki, vi;                            // key/value consume and issue cursors
+    TileIter kc, ki;                                    // consume / issue cursors
     bool kmore = iter_begin(kc, a, u0, u1, err, false);
-    bool vmore = iter_begin(vc, a, u0, u1, err, false);
     bool kimore = gi == 0 && iter_begin(ki, a, u0, u1, err, false);
-    bool vimore = gi == 0 && iter_begin(vi, a, u0, u1, err, false);
-    int kic = 0, vic = 0;
-    uint32_t kip = 0, vip = 0, kcp = 0, vcp = 0;        // positions issued / consumed
-    // thread 0 keeps both staging rings full: a slot is free once its position is consumed
+    int kic = 0;
+    uint32_t kip = 0, kcp = 0, uq = 0;
     auto top_up = [&]() {
       while (kimore && kip < kcp + NKS) {
         const uint32_t sl = kip % NKS, bar = b_kstage + 8 * sl, dst = sKS + sl * C::kKStageBytes;
@@ -765,6 +785,96 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         if (++kic == C::kSlotsPerTile) { kic = 0; kimore = iter_next(ki, a, u1, err, false); }
         ++kip;
       }
+    };
+    if (gi == 0) top_up();
+    // staging row gi of a key position: half gi/64, group (gi/8)%8, row gi%8; its four
+    // 16-byte units are 64-byte swizzled by row (TMA swizzle mode of the key map)
+    const int kr7 = gi & 7;
+    const uint32_t krow_off = (uint32_t)(gi >> 6) * (C::kKStageBytes / 2) + ((gi >> 3) & 7) * (C::KC * 512) + kr7 * 64;
+    bool ok = true;
+    while (kmore && ok) {
+      if (kc.tile == kc.U.tb) {
+        // ---- Q of the unit, bf16 -> fp16 in place, once the QK^T issuer has loaded it
+        const bool mine = gi != 0 || wait(b_qfull, uq & 1);
+        ok = !named_bar_or(kKeyDqBar, kKeyDqThreads, !mine);
+        if (!ok) break;
+        bool q_bad = false;
+        for (int i = gi; i < C::kQBytes / 16; i += kKeyDqThreads) {
+          uint4* qp = reinterpret_cast<uint4*>(gQ + 16 * i);
+          const uint4 v = *qp;
+          uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
+            q_bad |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+            __half2 h = __floats2half2_rn(lo, hi);
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+          }
+          *qp = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (q_bad) atomicOr(err, MLA_DEVERR_Q_RANGE);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_qready);
+        ++uq;
+      }
+      for (int sl = 0; sl < C::kSlotsPerTile && ok; ++sl) {
+        const uint32_t st = kcp % NKS, ks = kcp % NK;
+        const bool mine =
+            gi != 0 || (wait(b_kstage + 8 * st, (kcp / NKS) & 1) && wait(b_kempty + 8 * ks, ((kcp / NK) & 1) ^ 1));
+        ok = !named_bar_or(kKeyDqBar, kKeyDqThreads, !mine);   // everyone is done with the last slot
+        if (!ok) break;
+        if (gi == 0) top_up();
+        tc_fence_after();
+        const uint8_t* src = gKS + st * C::kKStageBytes + krow_off;
+        const uint32_t tbase = lane_base + C::kKTmemBase + ks * C::kKTmemSlotCols;
+        uint4 raw[C::KC][4];
+#pragma unroll
+        for (int cc = 0; cc < C::KC; ++cc)
+#pragma unroll
+          for (int u16 = 0; u16 < 4; ++u16)
+            raw[cc][u16] = *reinterpret_cast<const uint4*>(src + cc * 512 + ((u16 ^ ((kr7 >> 1) & 3)) << 4));
+#pragma unroll
+        for (int cc = 0; cc < C::KC; ++cc) {
+          uint32_t w[32];
+#pragma unroll
+          for (int u16 = 0; u16 < 4; ++u16) {
+            const uint32_t b4[4] = {raw[cc][u16].x, raw[cc][u16].y, raw[cc][u16].z, raw[cc][u16].w};
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+              __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b4[k2] & 0xFFFFu), __NV_E4M3);
+              __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b4[k2] >> 16), __NV_E4M3);
+              w[8 * u16 + 2 * k2] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+              w[8 * u16 + 2 * k2 + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+            }
+          }
+          tmem_st16u(tbase + cc * 32, w);
+          tmem_st16u(tbase + cc * 32 + 16, w + 16);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_kfull + 8 * ks);
+        ++kcp;
+      }
+      if (ok) kmore = iter_next(kc, a, u1, err, false);
+    }
+    if (gi == 0) {
+      volatile uint32_t no_abort = 0;
+      for (uint32_t q = kcp; q < kip; ++q)
+        mbar_wait(b_kstage + 8 * (q % NKS), (q / NKS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
+    }
+  } else if (FP8 && (warp == 2 || warp == 3)) {
+    // ============================================================ FP8 values
+    // Warps 2-3: every value chunk pair, from the raw staging ring into the fp16 value
+    // ring (convert_value_pair). Thread 0 does the waits and the TMA refills.
+    const int gi = threadIdx.x - 64;                    // 0..63
+    TileIter vc, vi;
+    bool vmore = iter_begin(vc, a, u0, u1, err, false);
+    bool vimore = gi == 0 && iter_begin(vi, a, u0, u1, err, false);
+    int vic = 0;
+    uint32_t vip = 0, vcp = 0, vtile = 0;
+    auto top_up = [&]() {
       while (vimore && vip < vcp + NVS) {
         const uint32_t sl = vip % NVS, bar = b_vstage + 8 * sl, dst = sVS + sl * kVStageBytes;
         const uint32_t nbox = (vi.rb0 >= 0 ? 1u : 0u) + (vi.rb1 >= 0 ? 1u : 0u);
@@ -775,110 +885,27 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         ++vip;
       }
     };
-    bool ok = true, first = true;
-    // staging row gi of a key position: half gi/64, group (gi/8)%8, row gi%8; its four
-    // 16-byte units are 64-byte swizzled by row (TMA swizzle mode of the key map)
-    const int kr7 = gi & 7;
-    const uint32_t krow_off = (uint32_t)(gi >> 6) * (C::kKStageBytes / 2) + ((gi >> 3) & 7) * (C::KC * 512) + kr7 * 64;
-    while (ok) {
-      const bool doK = kmore;
-      if (doK) {
-        for (int sl = 0; sl < C::kSlotsPerTile && ok; ++sl) {
-          if (gi == 0) top_up();
-          const uint32_t st = kcp % NKS, ks = kcp % NK;
-          ok = wait(b_kstage + 8 * st, (kcp / NKS) & 1);
-          ok = ok && wait(b_kempty + 8 * ks, ((kcp / NK) & 1) ^ 1);
-          if (ok) {
-            tc_fence_after();
-            const uint8_t* src = gKS + st * C::kKStageBytes + krow_off;
-            const uint32_t tbase = lane_base + C::kKTmemBase + ks * C::kKTmemSlotCols;
-#pragma unroll
-            for (int cc = 0; cc < C::KC; ++cc) {
-              uint32_t w[32];
-#pragma unroll
-              for (int u16 = 0; u16 < 4; ++u16) {
-                const uint4 v = *reinterpret_cast<const uint4*>(src + cc * 512 + ((u16 ^ ((kr7 >> 1) & 3)) << 4));
-                const uint32_t b4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int k2 = 0; k2 < 4; ++k2) {
-                  __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b4[k2] & 0xFFFFu), __NV_E4M3);
-                  __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b4[k2] >> 16), __NV_E4M3);
-                  w[8 * u16 + 2 * k2] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-                  w[8 * u16 + 2 * k2 + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
-                }
-              }
-              tmem_st16u(tbase + cc * 32, w);
-              tmem_st16u(tbase + cc * 32 + 16, w + 16);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_kfull + 8 * ks);
-          }
-          ok = !named_bar_or(kDequantBar, kDequantThreads, !ok);   // staging slot released
-          ++kcp;
-        }
-        if (ok) kmore = iter_next(kc, a, u1, err, false);
+    if (gi == 0) top_up();
+    bool ok = true;
+    while (vmore && ok) {
+      const int valid = vc.U.L - vc.tile * kTileTokens;
+      for (int j = 0; j < kPairsPerTile && ok; ++j) {
+        const uint32_t vp = 4 * vtile + j, st = vcp % NVS, vs = vp % NV;
+        const bool mine =
+            gi != 0 || (wait(b_vstage + 8 * st, (vcp / NVS) & 1) && wait(b_vempty + 8 * vs, ((vp / NV) & 1) ^ 1));
+        ok = !named_bar_or(kValDqBar, kValDqThreads, !mine);   // everyone is done with the last slot
+        if (!ok) break;
+        if (gi == 0) top_up();
+        convert_value_pair<kValDqThreads>(gVS + st * kVStageBytes, gV + vs * kVSlotBytes, valid, gi);
+        fence_proxy_async_smem();
+        named_bar_sync(kValDqBar, kValDqThreads);
+        if (gi == 0) mbar_arrive(b_vfull + 8 * vs);
+        ++vcp;
       }
-      const bool doV = ok && vmore && (!first || !doK);   // values lag the keys by one tile
-      if (doV) {
-        const int valid = vc.U.L - vc.tile * kTileTokens;
-        for (int j = 0; j < kPairsPerTile && ok; ++j) {
-          if (gi == 0) top_up();
-          const uint32_t st = vcp % NVS, vs = vcp % NV;
-          ok = wait(b_vstage + 8 * st, (vcp / NVS) & 1);
-          ok = ok && wait(b_vempty + 8 * vs, ((vcp / NV) & 1) ^ 1);
-          if (ok) {
-            // unit idx: chunk idx / 512, row (idx % 512) / 4, 16-byte column idx % 4;
-            // staging row r of chunk c at half r / 64, group (r / 8) % 8, row r % 8
-            const uint8_t* src = gVS + st * kVStageBytes;
-            uint8_t* dst = gV + vs * kVSlotBytes;
-#pragma unroll 1
-            for (int base = gi; base < 1024; base += 4 * kDequantThreads) {
-              uint4 v[4];
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                const int idx = base + jj * kDequantThreads, row = (idx & 511) >> 2;
-                v[jj] = make_uint4(0, 0, 0, 0);
-                if (row < valid)
-                  v[jj] = *reinterpret_cast<const uint4*>(src + (row >> 6) * (kVStageBytes / 2) +
-                                                          ((row >> 3) & 7) * 1024 + (idx >> 9) * 512 +
-                                                          (row & 7) * 64 + (idx & 3) * 16);
-              }
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                const int idx = base + jj * kDequantThreads, row = (idx & 511) >> 2, q4 = idx & 3;
-                const uint32_t b4[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
-                uint32_t hh[8];
-#pragma unroll
-                for (int k2 = 0; k2 < 4; ++k2) {
-                  __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b4[k2] & 0xFFFFu), __NV_E4M3);
-                  __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b4[k2] >> 16), __NV_E4M3);
-                  hh[2 * k2] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-                  hh[2 * k2 + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
-                }
-                uint8_t* drow = dst + (idx >> 9) * kChunkBytes + (row >> 3) * 1024 + (row & 7) * 128;
-                *reinterpret_cast<uint4*>(drow + (((2 * q4) ^ (row & 7)) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-                *reinterpret_cast<uint4*>(drow + (((2 * q4 + 1) ^ (row & 7)) << 4)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
-              }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_vfull + 8 * vs);
-          }
-          ok = !named_bar_or(kDequantBar, kDequantThreads, !ok);
-          ++vcp;
-        }
-        if (ok) vmore = iter_next(vc, a, u1, err, false);
-      }
-      first = false;
-      if (!doK && !doV) break;
+      if (ok) { vmore = iter_next(vc, a, u1, err, false); ++vtile; }
     }
-    // loads issued but not consumed (only after a failed wait) land before exit
     if (gi == 0) {
       volatile uint32_t no_abort = 0;
-      for (uint32_t q = kcp; q < kip; ++q)
-        mbar_wait(b_kstage + 8 * (q % NKS), (q / NKS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
       for (uint32_t q = vcp; q < vip; ++q)
         mbar_wait(b_vstage + 8 * (q % NVS), (q / NVS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
     }

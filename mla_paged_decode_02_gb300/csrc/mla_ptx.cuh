@@ -179,14 +179,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-// The same store for 16 raw 32-bit words.
+// The same store for 16 raw 32-bit words. It touches no generic memory, so (unlike the
+// fences and waits, which carry a memory clobber) shared-memory loads may move across it;
+// tcgen05.wait::st orders it.
 __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
                "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
                :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
                   "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]),
-                  "r"(v[13]), "r"(v[14]), "r"(v[15])
-               : "memory");
+                  "r"(v[13]), "r"(v[14]), "r"(v[15]));
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
