@@ -12,10 +12,12 @@
 // 2 KB rows). Persistent grid-stride loop over the list the scheduler wrote, so nothing
 // launches per sequence.
 #include "mla_internal.h"
+#include "mla_ptx.cuh"
 
 namespace mla {
 
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
+  griddep_wait();                      // launched early; the decode kernel's partials first
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -62,8 +64,16 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
 }
 
 cudaError_t launch_combine(const CombineArgs& a, int grid, cudaStream_t s) {
-  combine_kernel<<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, a);
 }
 
 }  // namespace mla

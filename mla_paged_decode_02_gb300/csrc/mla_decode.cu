@@ -345,6 +345,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  // the set-up above overlaps the scheduler (programmatic dependent launch); its output is
+  // read only after it has completed
+  griddep_wait();
 
   // this CTA's units: a contiguous range of the scheduler's list
   const int u0 = a.cta_first[blockIdx.x], u1 = a.cta_first[blockIdx.x + 1];
@@ -912,6 +915,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   }
 
   // ============================================================ teardown
+  griddep_launch_dependents();         // the combine kernel may start its launch
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -934,8 +938,17 @@ static cudaError_t prepare_one() {
 template <int RC, bool FP8>
 static cudaError_t launch_one(const DecodeArgs& a, int grid, cudaStream_t s) {
   using C = Cfg<RC, FP8>;
-  decode_kernel<RC, FP8><<<grid, C::kThreads, C::kDynBytes, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kDynBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap the scheduler
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<RC, FP8>, a);
 }
 
 int decode_key_chunks_per_slot(int rc, bool fp8) {

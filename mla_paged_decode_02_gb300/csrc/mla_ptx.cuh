@@ -82,6 +82,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// ------------------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while the previous
+// kernel on the stream is still running; it must execute griddep_wait() before it reads
+// anything that kernel writes (the wait returns once that grid has completed and its
+// writes are visible). griddep_launch_dependents() lets the next such kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -21,6 +21,7 @@
 // inside one CTA write the final output directly. Units are stored in position order,
 // so the units of CTA c are the contiguous range [cta_first[c], cta_first[c + 1]).
 #include "mla_internal.h"
+#include "mla_ptx.cuh"
 #include "../../include/mla.h"
 
 namespace mla {
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   static_assert(kSchedThreads == 1024, "the scan assumes 32 warps");
   __shared__ int64_t scan_tmp[32];
   const int tid = threadIdx.x;
+  griddep_launch_dependents();         // the decode grid may start its set-up now
   if (tid == 0) a.hdr[0] = 0u;
   __syncthreads();
 
