@@ -66,9 +66,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kSoftmaxBar = 1;          // named barrier of the 4 softmax warps
 constexpr uint32_t kKeyDqBar = 2;            // FP8 key dequantising warps 8-11
-constexpr uint32_t kValDqBar = 3;            // FP8 value dequantising warps 2-3
 constexpr int kKeyDqThreads = 128;
-constexpr int kValDqThreads = 64;
 constexpr float kValueDqScale = 256.f;       // FP8 values are converted as value * 2^-8
 constexpr int kSmemLimit = 232448;           // 227 KB per CTA
 constexpr int kStaticBudget = 3072;          // static shared memory (barriers, scratch)
@@ -267,7 +265,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ uint8_t dsmem_raw[];
   __shared__ __align__(8) uint64_t bar_kfull[NK], bar_kempty[NK], bar_vfull[NV], bar_vempty[NV];
   __shared__ __align__(8) uint64_t bar_qfull, bar_qready, bar_qempty;
-  __shared__ __align__(8) uint64_t bar_kstage[NKS], bar_vstage[NVS];
+  __shared__ __align__(8) uint64_t bar_kstage[NKS], bar_vstage[NVS], bar_vsempty[NVS];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_s_empty[2], bar_p_full[NP], bar_pv[NP];
   __shared__ __align__(8) uint64_t bar_o_empty, bar_drain[2], bar_vaux;
   __shared__ uint32_t tmem_base_s;
@@ -301,6 +299,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const uint32_t b_qfull = smem_u32(&bar_qfull), b_qready = smem_u32(&bar_qready);
   const uint32_t b_qempty = smem_u32(&bar_qempty);
   const uint32_t b_kstage = smem_u32(bar_kstage), b_vstage = smem_u32(bar_vstage);
+  const uint32_t b_vsempty = smem_u32(bar_vsempty);
   const uint32_t b_s_full = smem_u32(bar_s_full), b_s_empty = smem_u32(bar_s_empty);
   const uint32_t b_p_full = smem_u32(bar_p_full), b_pv = smem_u32(bar_pv);
   const uint32_t b_oempty = smem_u32(&bar_o_empty), b_drain = smem_u32(bar_drain);
@@ -320,7 +319,10 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     mbar_init(b_qfull, 1);
     mbar_init(b_qready, 4);
     for (int i = 0; i < NKS; ++i) mbar_init(b_kstage + 8 * i, 1);
-    for (int i = 0; i < NVS; ++i) mbar_init(b_vstage + 8 * i, 1);
+    for (int i = 0; i < NVS; ++i) {
+      mbar_init(b_vstage + 8 * i, 1);
+      mbar_init(b_vsempty + 8 * i, 1);
+    }
     mbar_init(b_qempty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_s_full + 8 * i, 1);
@@ -560,7 +562,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     const float kvs = FP8 ? __ldg(a.kv_scale) : 1.0f;
     const float c_log2 = a.softmax_scale * kvs * kLog2e;
     const float kvo = FP8 ? kvs * kValueDqScale : 1.0f;   // value scale (exact power-of-2 fold)
-    uint32_t gn = 0;
+    uint32_t gn = 0, vcp = 0;
     bool ok = true;
     float lsum[RC];
     for (int u = u0; u < u1 && ok; ++u) {
@@ -676,6 +678,26 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         }
         tc_fence_before();
         mbar_arrive(b_p_full + 8 * pb);
+        if (FP8) {
+          // ---- the values of this tile (FP8): raw E4M3 chunk pairs -> fp16 value ring,
+          // one pair at a time so that PV starts on each as soon as it is ready. Thread 0
+          // waits; the softmax barrier passes the outcome on.
+          const int valid = U.L - (U.tb + k) * kTileTokens;
+          for (int j = 0; j < kPairsPerTile && ok; ++j, ++vcp) {
+            const uint32_t st = vcp % NVS, vs = vcp % NV;
+            const bool mine =
+                t != 0 || (wait(b_vstage + 8 * st, (vcp / NVS) & 1) && wait(b_vempty + 8 * vs, ((vcp / NV) & 1) ^ 1));
+            ok = !named_bar_or(kSoftmaxBar, 128, !mine);
+            if (!ok) break;
+            convert_value_pair<128>(gVS + st * kVStageBytes, gV + vs * kVSlotBytes, valid, t);
+            fence_proxy_async_smem();
+            named_bar_sync(kSoftmaxBar, 128);
+            if (t == 0) {
+              mbar_arrive(b_vfull + 8 * vs);
+              mbar_arrive(b_vsempty + 8 * st);
+            }
+          }
+        }
       }
       if (!ok) break;
       // ---- epilogue: wait for the unit's last PV
@@ -867,49 +889,31 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       for (uint32_t q = kcp; q < kip; ++q)
         mbar_wait(b_kstage + 8 * (q % NKS), (q / NKS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
     }
-  } else if (FP8 && (warp == 2 || warp == 3)) {
-    // ============================================================ FP8 values
-    // Warps 2-3: every value chunk pair, from the raw staging ring into the fp16 value
-    // ring (convert_value_pair). Thread 0 does the waits and the TMA refills.
-    const int gi = threadIdx.x - 64;                    // 0..63
-    TileIter vc, vi;
-    bool vmore = iter_begin(vc, a, u0, u1, err, false);
-    bool vimore = gi == 0 && iter_begin(vi, a, u0, u1, err, false);
-    int vic = 0;
-    uint32_t vip = 0, vcp = 0, vtile = 0;
-    auto top_up = [&]() {
-      while (vimore && vip < vcp + NVS) {
-        const uint32_t sl = vip % NVS, bar = b_vstage + 8 * sl, dst = sVS + sl * kVStageBytes;
-        const uint32_t nbox = (vi.rb0 >= 0 ? 1u : 0u) + (vi.rb1 >= 0 ? 1u : 0u);
-        mbar_arrive_expect_tx(bar, nbox * (kVStageBytes / 2));
-        if (vi.rb0 >= 0) tma_load_4d(dst, &a.tm_v, bar, 0, 0, 2 * vic, (int32_t)(vi.rb0 >> 3));
-        if (vi.rb1 >= 0) tma_load_4d(dst + kVStageBytes / 2, &a.tm_v, bar, 0, 0, 2 * vic, (int32_t)(vi.rb1 >> 3));
-        if (++vic == kPairsPerTile) { vic = 0; vimore = iter_next(vi, a, u1, err, false); }
-        ++vip;
+  } else if (FP8 && warp == 2) {
+    // ============================================================ FP8 raw value producer
+    // One thread: every value chunk pair of every tile as two TMA boxes (one per 64-row
+    // page half) into the raw staging ring; the softmax warps convert them (after writing
+    // the tile's P^T) and release the staging slot.
+    if (lane == 0) {
+      TileIter it;
+      bool more = iter_begin(it, a, u0, u1, err, false);
+      bool ok = true;
+      uint32_t p = 0;
+      while (more && ok) {
+        const uint32_t nbox = (it.rb0 >= 0 ? 1u : 0u) + (it.rb1 >= 0 ? 1u : 0u);
+        for (int j = 0; j < kPairsPerTile; ++j, ++p) {
+          const uint32_t sl = p % NVS;
+          ok = wait(b_vsempty + 8 * sl, ((p / NVS) & 1) ^ 1);
+          if (!ok) break;
+          const uint32_t bar = b_vstage + 8 * sl, dst = sVS + sl * kVStageBytes;
+          mbar_arrive_expect_tx(bar, nbox * (kVStageBytes / 2));
+          if (it.rb0 >= 0) tma_load_4d(dst, &a.tm_v, bar, 0, 0, 2 * j, (int32_t)(it.rb0 >> 3));
+          if (it.rb1 >= 0) tma_load_4d(dst + kVStageBytes / 2, &a.tm_v, bar, 0, 0, 2 * j, (int32_t)(it.rb1 >> 3));
+        }
+        if (ok) more = iter_next(it, a, u1, err, false);
       }
-    };
-    if (gi == 0) top_up();
-    bool ok = true;
-    while (vmore && ok) {
-      const int valid = vc.U.L - vc.tile * kTileTokens;
-      for (int j = 0; j < kPairsPerTile && ok; ++j) {
-        const uint32_t vp = 4 * vtile + j, st = vcp % NVS, vs = vp % NV;
-        const bool mine =
-            gi != 0 || (wait(b_vstage + 8 * st, (vcp / NVS) & 1) && wait(b_vempty + 8 * vs, ((vp / NV) & 1) ^ 1));
-        ok = !named_bar_or(kValDqBar, kValDqThreads, !mine);   // everyone is done with the last slot
-        if (!ok) break;
-        if (gi == 0) top_up();
-        convert_value_pair<kValDqThreads>(gVS + st * kVStageBytes, gV + vs * kVSlotBytes, valid, gi);
-        fence_proxy_async_smem();
-        named_bar_sync(kValDqBar, kValDqThreads);
-        if (gi == 0) mbar_arrive(b_vfull + 8 * vs);
-        ++vcp;
-      }
-      if (ok) { vmore = iter_next(vc, a, u1, err, false); ++vtile; }
-    }
-    if (gi == 0) {
       volatile uint32_t no_abort = 0;
-      for (uint32_t q = vcp; q < vip; ++q)
+      for (uint32_t q = p > (uint32_t)NVS ? p - NVS : 0; q < p; ++q)
         mbar_wait(b_vstage + 8 * (q % NVS), (q / NVS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
     }
   }

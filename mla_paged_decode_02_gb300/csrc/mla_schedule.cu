@@ -11,11 +11,12 @@
 // key tiles and G groups of query rows; each (g, b) is a stream of n_b tiles, and the
 // streams are laid end to end, group-major:
 //   pos(g, b) = g * N + sum_{b' < b} n_b',    N = sum_b n_b,    W = G * N,
-// so that the G streams that read the same keys run at the same time on CTAs about
-// grid / G apart, and the second reader finds the keys in L2.
 // The persistent decode grid has one CTA per SM; CTA c takes the positions
 // [c q, (c + 1) q) with q = ceil(W / grid), so no CTA has more than one tile more work
-// than another whatever the length mix. A stream that a CTA boundary cuts becomes one
+// than another whatever the length mix. When G divides the grid, each row group instead
+// gets exactly grid / G CTAs and the same partition of its N tiles (q = ceil(N G / grid)):
+// CTA c + k grid / G then reads the same key tiles as CTA c, in the same order and at about
+// the same time, so of the G reads of every key tile only the first comes from DRAM. A stream that a CTA boundary cuts becomes one
 // unit per CTA it touches; each such piece writes a partial output (normalised, with
 // its log-sum-exp) to its own slot, and the combine kernel merges the pieces. Streams
 // inside one CTA write the final output directly. Units are stored in position order,
@@ -81,14 +82,19 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   int64_t n_tiles;
   const int64_t tile_off = block_exclusive_scan(my_tiles, scan_tmp, &n_tiles);
   const int64_t W = (int64_t)G * n_tiles;
-  const int64_t q = (W + a.grid - 1) / a.grid;   // >= 1: every sequence has a tile
+  const bool aligned = G > 1 && a.grid % G == 0;   // one CTA block per row group
+  const int cpg = aligned ? a.grid / G : a.grid;    // CTAs per row group
+  const int64_t q = aligned ? (n_tiles + cpg - 1) / cpg : (W + a.grid - 1) / a.grid;   // >= 1
 
   // 2. per group g (in position order): units, cut streams and partial slots of this
   //    thread's sequences, and their offsets; then the units themselves
   int64_t unit_base = 0, split_base = 0, slot_base = 0;
   for (int g = 0; g < G; ++g) {
+    // positions of group g: g N + p (one partition of all W) or p (aligned, CTAs g cpg ...)
+    const int64_t goff = aligned ? 0 : (int64_t)g * n_tiles;
+    const int cbase = aligned ? g * cpg : 0;
     int64_t my_units = 0, my_split = 0, my_slots = 0;
-    int64_t pre = (int64_t)g * n_tiles + tile_off;
+    int64_t pre = goff + tile_off;
     for (int b = b0; b < b1; ++b) {
       const int n = (clamped_len(a, b, false) + kTileTokens - 1) / kTileTokens;
       const int64_t ns = (pre + n - 1) / q - pre / q + 1;
@@ -115,8 +121,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
       for (int c = tid; c <= a.grid; c += kSchedThreads) a.cta_first[c] = -1;
       __syncthreads();
     }
-    // units in position order; the unit starting at c q is the first of CTA c
-    pre = (int64_t)g * n_tiles + tile_off;
+    // units in position order; the unit starting at c q is the first of CTA cbase + c
+    pre = goff + tile_off;
     for (int b = b0; b < b1; ++b) {
       const int Lc = clamped_len(a, b, false);
       const int n = (Lc + kTileTokens - 1) / kTileTokens;
@@ -131,11 +137,18 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
         const int64_t s1 = pre + n < (c + 1) * q ? pre + n : (c + 1) * q;
         const int tb = (int)(s0 - pre), te = (int)(s1 - pre);
         a.units[unit_off] = make_int4(b, g, tb | (te << 16), ns >= 2 ? slot0 + k : -1);
-        if (s0 == c * q) a.cta_first[c] = (int32_t)unit_off;
+        if (s0 == c * q) a.cta_first[cbase + c] = (int32_t)unit_off;
         ++unit_off;
       }
       if (ns >= 2) slot_off += ns;
       pre += n;
+    }
+    if (aligned) {
+      // a CTA of this group's block without work starts (and ends) at the group's end, so
+      // that the ranges [cta_first[c], cta_first[c + 1]) stay within their group
+      __syncthreads();
+      for (int c = cbase + tid; c < cbase + cpg; c += kSchedThreads)
+        if (a.cta_first[c] < 0) a.cta_first[c] = (int32_t)unit_base;
     }
   }
   __syncthreads();

@@ -1,10 +1,12 @@
 """The split scheduler's partition, read back from the workspace after a decode.
 
-The scheduler lays the (sequence, row group) streams of key tiles end to end and gives
-CTA c the positions [c q, (c + 1) q), q = ceil(W / grid). Checked here on the device's
-own output: every tile of every stream is covered exactly once, every CTA's units are a
-contiguous range holding exactly its share of tiles, and only streams cut by a CTA
-boundary get partial slots (consecutive ones). The workspace offsets below restate the
+The scheduler lays the (row group, sequence) streams of key tiles end to end and gives
+CTA c the positions [c q, (c + 1) q), q = ceil(W / grid); when the G row groups divide the
+grid, each group gets grid / G CTAs and the same partition of its N tiles instead
+(q = ceil(N / (grid / G))). Checked here on the device's own output: every tile of every
+stream is covered exactly once, every CTA's units are a contiguous range holding exactly
+its share of tiles, and only streams cut by a CTA boundary get partial slots (consecutive
+ones). The workspace offsets below restate the
 layout the library documents for its workspace (header, batch info, per-CTA first unit,
 cut streams, units), 256-byte aligned.
 """
@@ -67,16 +69,22 @@ def test_partition_is_exact_and_balanced(B, s_q, H, P, lens):
     splits = ws[split_off:split_off + 16 * n_split].view(np.int32).reshape(n_split, 4)
 
     n_b = (case.seq_lens.astype(np.int64) + 127) // 128
-    W = G * int(n_b.sum())
-    assert q == -(-W // grid)
+    N = int(n_b.sum())
+    W = G * N
+    aligned = G > 1 and grid % G == 0
+    cpg = grid // G if aligned else grid
+    assert q == (-(-N // cpg) if aligned else -(-W // grid))
     assert cta_first[grid] == n_units and np.all(np.diff(cta_first) >= 0)
     tb = units[:, 2] & 0xFFFF
     te = units[:, 2] >> 16
     assert np.all(te > tb)
     for c in range(grid):
-        share = max(0, min((c + 1) * q, W) - c * q)
+        cc, total = (c % cpg, N) if aligned else (c, W)
+        share = max(0, min((cc + 1) * q, total) - cc * q)
         sl = slice(cta_first[c], cta_first[c + 1])
         assert int((te[sl] - tb[sl]).sum()) == share, c
+        if aligned:
+            assert np.all(units[sl, 1] == c // cpg), c          # one row group per CTA block
     cover = {}
     for (b, gg, _, slot), s0, s1 in zip(units, tb, te):
         cover.setdefault((int(b), int(gg)), []).append((int(s0), int(s1), int(slot)))
