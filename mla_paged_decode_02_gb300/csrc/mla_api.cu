@@ -235,7 +235,10 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   ca.lse = lse;
   ca.R = R;
   ca.RC = rc;
-  if (launch_combine(ca, nsm, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // up to 2 * #SM cut streams x RC rows: 8 * #SM blocks of 8 warps give every (stream, row)
+  // task its own warp for RC <= 32 and at most two rounds for RC = 64 (the combine is a few
+  // dependent global loads per task: latency, not bandwidth)
+  if (launch_combine(ca, 8 * nsm, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
