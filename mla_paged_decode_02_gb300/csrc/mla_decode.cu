@@ -685,8 +685,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           const int valid = U.L - (U.tb + k) * kTileTokens;
           for (int j = 0; j < kPairsPerTile && ok; ++j, ++vcp) {
             const uint32_t st = vcp % NVS, vs = vcp % NV;
-            const bool mine =
-                t != 0 || (wait(b_vstage + 8 * st, (vcp / NVS) & 1) && wait(b_vempty + 8 * vs, ((vcp / NV) & 1) ^ 1));
+            // the raw rows have landed, and (the producer waited for it) the fp16 slot is free
+            const bool mine = t != 0 || wait(b_vstage + 8 * st, (vcp / NVS) & 1);
             ok = !named_bar_or(kSoftmaxBar, 128, !mine);
             if (!ok) break;
             convert_value_pair<128>(gVS + st * kVStageBytes, gV + vs * kVSlotBytes, valid, t);
@@ -893,7 +893,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     // ============================================================ FP8 raw value producer
     // One thread: every value chunk pair of every tile as two TMA boxes (one per 64-row
     // page half) into the raw staging ring; the softmax warps convert them (after writing
-    // the tile's P^T) and release the staging slot.
+    // the tile's P^T) and release the staging slot. The thread issues pair p only once the
+    // fp16 value slot it will be converted into is free as well, so that the landed raw
+    // rows are all the softmax warps need to wait for.
     if (lane == 0) {
       TileIter it;
       bool more = iter_begin(it, a, u0, u1, err, false);
@@ -903,7 +905,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         const uint32_t nbox = (it.rb0 >= 0 ? 1u : 0u) + (it.rb1 >= 0 ? 1u : 0u);
         for (int j = 0; j < kPairsPerTile; ++j, ++p) {
           const uint32_t sl = p % NVS;
-          ok = wait(b_vsempty + 8 * sl, ((p / NVS) & 1) ^ 1);
+          ok = wait(b_vsempty + 8 * sl, ((p / NVS) & 1) ^ 1) && wait(b_vempty + 8 * (p % NV), ((p / NV) & 1) ^ 1);
           if (!ok) break;
           const uint32_t bar = b_vstage + 8 * sl, dst = sVS + sl * kVStageBytes;
           mbar_arrive_expect_tx(bar, nbox * (kVStageBytes / 2));
