@@ -17,7 +17,6 @@
 namespace mla {
 
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
-  griddep_wait();                      // launched early; the decode kernel's partials first
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -63,17 +62,11 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   }
 }
 
+// Plain stream order after the decode kernel: an early (programmatic) launch, whose
+// blocks wait resident for the decode grid to finish, measured slower on long contexts.
 cudaError_t launch_combine(const CombineArgs& a, int grid, cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(256);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, a);
+  combine_kernel<<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace mla

@@ -15,33 +15,33 @@
 // 128-byte swizzle): as the K-major A operand of QK^T, and as the MN-major A operand
 // of PV. S^T double-buffers in TMEM (2*RC columns) next to O^T (4*RC columns).
 //
-// Pipeline (one CTA per SM, persistent over the work units the scheduler sorted):
-//   loaders     the key chunks (128 rows x 64 columns) of every tile into the K ring
-//               (16 KB slots) and the value chunk pairs (128 x 128) into the V ring (32 KB
-//               slots), by cp.async straight into the swizzled MMA layout: every thread
-//               computes the page address of its own 16-byte pieces from the block table.
-//               (Small TMA boxes — one 64-row page strip of 128 bytes — move only ~40 GB/s
-//               per SM even from L2, below the per-SM share of HBM bandwidth, while
-//               cp.async moves ~110 GB/s per SM from L2 and saturates HBM.) Values are
-//               read a second time for PV — they are L2-resident by then — so that no
-//               slot lives from QK^T through the softmax to PV. Key and value streams have
-//               their own warps, so key prefetch never waits for the softmax.
-//               bf16 cache: warps 0 and 2 load keys, warp 3 values. FP8 cache: warps 8-9
-//               (keys) and 10-11 (values) prefetch the E4M3 rows into small staging rings
-//               and dequantise them to fp16 (exact: every E4M3 value is an fp16 value);
-//               warps 2-3 convert Q from bf16 to fp16. The FP8 path multiplies in fp16
-//               with fp32 accumulation; kv_scale is folded into the score scale and the
-//               output.
-//   warp 1      MMA issuer (one thread) with two independent cursors, one over the QK^T
-//               chunks and one over the PV chunk pairs. It polls both sides and issues
-//               whichever has its inputs ready; QK^T may run up to two tiles ahead (the
-//               S^T double buffer). It also loads Q of each unit (TMA).
+// Pipeline (one CTA per SM, persistent over the contiguous range of work units the
+// scheduler gave it). Every mbarrier ring slot has exactly one producer.
+//   bf16 cache (256 threads):
+//   warp 0      key producer (one thread): every key slot (KC chunks of a tile) is two 4D
+//               TMA boxes, one per 64-row page half, landing directly in the swizzled
+//               MMA layout.
+//   warp 2      value producer: every value chunk pair as two TMA boxes, re-read from L2
+//               so that no slot lives from QK^T through the softmax to PV; zeroes the rows
+//               between the sequence end and the end of the last 16-key MMA step.
+//   warp 1      QK^T issuer (one thread): Q of each unit (TMA), then per tile the S^T
+//               buffer and every key slot in program order.
+//   warp 3      PV issuer (one thread): per tile P^T, then the four value chunk pairs.
+//   FP8 cache (384 threads):
+//   warps 8-11  one thread per key row: each unit's Q to fp16 in place; every raw E4M3
+//               key position (TMA-staged) to fp16 in a tensor-memory key slot, read by
+//               the QK^T MMAs as their A operand.
+//   warp 2      raw value producer (one thread): value chunk pairs into a raw staging
+//               ring.
+//   warps 0, 1  PV and QK^T issuers.
+//   both:
 //   warps 4-7   softmax (one thread per key of the tile = one TMEM lane): scale, causal
 //               mask, online softmax with a lazily-rescaled running max (the reference
 //               max moves only when a score exceeds it by more than 2^8, so O^T is
 //               rescaled rarely; the final normalisation uses the same reference, so the
-//               result is exact), P^T to shared memory, epilogue (O^T / l -> output or
-//               split partial plus LSE).
+//               result is exact), P^T to shared memory; FP8: then the tile's four value
+//               pairs from the raw ring into the fp16 value ring (integer conversion);
+//               epilogue (O^T / l -> output or split partial plus LSE).
 //
 // Every wait is bounded (mla_ptx.cuh): a stall sets the device error word and the CTA
 // waits for its in-flight copies and MMAs, frees its tensor memory and exits. Value rows
@@ -685,8 +685,10 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           const int valid = U.L - (U.tb + k) * kTileTokens;
           for (int j = 0; j < kPairsPerTile && ok; ++j, ++vcp) {
             const uint32_t st = vcp % NVS, vs = vcp % NV;
-            // the raw rows have landed, and (the producer waited for it) the fp16 slot is free
-            const bool mine = t != 0 || wait(b_vstage + 8 * st, (vcp / NVS) & 1);
+            // the raw rows have landed and the fp16 slot is free (with three or more value
+            // slots the producer waited for the slot before loading the rows)
+            const bool mine = t != 0 || (wait(b_vstage + 8 * st, (vcp / NVS) & 1) &&
+                                         (NV >= 3 || wait(b_vempty + 8 * vs, ((vcp / NV) & 1) ^ 1)));
             ok = !named_bar_or(kSoftmaxBar, 128, !mine);
             if (!ok) break;
             convert_value_pair<128>(gVS + st * kVStageBytes, gV + vs * kVSlotBytes, valid, t);
@@ -893,9 +895,10 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     // ============================================================ FP8 raw value producer
     // One thread: every value chunk pair of every tile as two TMA boxes (one per 64-row
     // page half) into the raw staging ring; the softmax warps convert them (after writing
-    // the tile's P^T) and release the staging slot. The thread issues pair p only once the
-    // fp16 value slot it will be converted into is free as well, so that the landed raw
-    // rows are all the softmax warps need to wait for.
+    // the tile's P^T) and release the staging slot. With three or more value slots the
+    // thread issues pair p only once the fp16 slot it will be converted into is free as
+    // well, so that the landed raw rows are all the softmax warps need to wait for (with
+    // two slots that would put the raw load's latency behind the slot's release).
     if (lane == 0) {
       TileIter it;
       bool more = iter_begin(it, a, u0, u1, err, false);
@@ -905,7 +908,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         const uint32_t nbox = (it.rb0 >= 0 ? 1u : 0u) + (it.rb1 >= 0 ? 1u : 0u);
         for (int j = 0; j < kPairsPerTile; ++j, ++p) {
           const uint32_t sl = p % NVS;
-          ok = wait(b_vsempty + 8 * sl, ((p / NVS) & 1) ^ 1) && wait(b_vempty + 8 * (p % NV), ((p / NV) & 1) ^ 1);
+          ok = wait(b_vsempty + 8 * sl, ((p / NVS) & 1) ^ 1) &&
+               (NV < 3 || wait(b_vempty + 8 * (p % NV), ((p / NV) & 1) ^ 1));
           if (!ok) break;
           const uint32_t bar = b_vstage + 8 * sl, dst = sVS + sl * kVStageBytes;
           mbar_arrive_expect_tx(bar, nbox * (kVStageBytes / 2));
@@ -921,7 +925,6 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   }
 
   // ============================================================ teardown
-  griddep_launch_dependents();         // the combine kernel may start its launch
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
