@@ -157,6 +157,22 @@ mla_status mla_decode_noalloc(const mla_decode_params* p, const void* q, const v
                               float softmax_scale, const float* kv_scale, void* out, float* lse,
                               mla_stream_t stream);
 
+/* Decode-kernel timing, for benchmarks and tests. After mla_profile_begin(n), each of the
+ * next n mla_decode / mla_decode_noalloc calls in this process records a CUDA event on
+ * its stream immediately before and immediately after its decode-kernel launch. The
+ * events belong to the library and are created on the device current at
+ * mla_profile_begin; the timed calls must run on that device. The event between the
+ * scheduler and the decode kernel also makes the decode kernel wait until the scheduler
+ * has finished (no overlap of its set-up), so each interval is the decode kernel alone.
+ * mla_profile_end waits for the recorded events, stores the summed decode-kernel time
+ * in milliseconds in *total_ms and the number of timed launches in *launches, and stops
+ * recording (with no mla_profile_begin before it: 0 and 0). Not thread safe: one
+ * profiling window per process at a time.
+ * Errors: MLA_ERR_INVALID_ARG for max_launches outside [1, 4096] or a NULL output;
+ * MLA_ERR_CUDA when an event cannot be created, recorded or read. */
+mla_status mla_profile_begin(int32_t max_launches);
+mla_status mla_profile_end(double* total_ms, int32_t* launches);
+
 /* Static text for a status code. */
 const char* mla_status_string(int32_t status);
 

@@ -21,7 +21,8 @@ STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED",
           -3: "MLA_ERR_WORKSPACE_TOO_SMALL", -4: "MLA_ERR_CUDA", -5: "MLA_ERR_TIMEOUT",
           -6: "MLA_ERR_DEVICE_INDEX"}
 EXPORTS = ("mla_abi_version", "mla_status_string", "mla_decode_workspace_size", "mla_decode",
-           "mla_decode_check", "mla_cache_write", "mla_decode_noalloc")
+           "mla_decode_check", "mla_cache_write", "mla_decode_noalloc", "mla_profile_begin",
+           "mla_profile_end")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla.so")
@@ -65,6 +66,10 @@ def lib() -> ctypes.CDLL:
                                          vp, vp, vp, vp]
         L.mla_cache_write.restype = i32
         L.mla_cache_write.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, vp, vp, vp]
+        L.mla_profile_begin.restype = i32
+        L.mla_profile_begin.argtypes = [i32]
+        L.mla_profile_end.restype = i32
+        L.mla_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i32)]
         _lib = L
     return _lib
 
@@ -174,6 +179,23 @@ def decode_check(workspace: torch.Tensor, stream=None):
     bits = ctypes.c_uint32(0)
     st = lib().mla_decode_check(_ptr(workspace), _stream(stream), ctypes.byref(bits))
     return int(st), int(bits.value)
+
+
+def profile_begin(max_launches: int) -> None:
+    """Time the decode kernel of each of the next `max_launches` decode calls (CUDA events
+    around its launch, recorded by the library on the call's stream)."""
+    st = lib().mla_profile_begin(int(max_launches))
+    if st != 0:
+        raise MLAError(st, "mla_profile_begin")
+
+
+def profile_end():
+    """Stop timing; returns (summed decode-kernel milliseconds, number of timed launches)."""
+    ms, n = ctypes.c_double(0.0), ctypes.c_int32(0)
+    st = lib().mla_profile_end(ctypes.byref(ms), ctypes.byref(n))
+    if st != 0:
+        raise MLAError(st, "mla_profile_end")
+    return float(ms.value), int(n.value)
 
 
 def cache_write(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch.Tensor,

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <vector>
 #include <cudaTypedefs.h>
 #include "mla_internal.h"
 #include "../../include/mla.h"
@@ -18,6 +19,15 @@ std::atomic<int> g_num_sms[kMaxDevices];
 std::atomic<uint32_t> g_prepared[kMaxDevices];   // bit per decode variant
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// decode-kernel timing window (mla_profile_begin / mla_profile_end)
+struct ProfileWindow {
+  std::vector<cudaEvent_t> ev;   // 2 per launch: before, after
+  int cap = 0, next = 0;
+  bool on = false;
+};
+ProfileWindow g_prof;
+constexpr int kMaxProfiledLaunches = 4096;
 
 int variant_bit(int rc, bool fp8) {
   return (rc == 16 ? 0 : rc == 32 ? 2 : 4) + (fp8 ? 1 : 0);
@@ -224,7 +234,13 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   da.num_pages = p->num_pages;
   da.causal = p->causal;
   da.softmax_scale = softmax_scale;
+  const bool timed = g_prof.on && g_prof.next < g_prof.cap;
+  if (timed && cudaEventRecord(g_prof.ev[2 * g_prof.next], s) != cudaSuccess) return MLA_ERR_CUDA;
   if (launch_decode(da, rc, fp8, nsm, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (timed) {
+    if (cudaEventRecord(g_prof.ev[2 * g_prof.next + 1], s) != cudaSuccess) return MLA_ERR_CUDA;
+    ++g_prof.next;
+  }
 
   CombineArgs ca{};
   ca.hdr = hdr;
@@ -239,6 +255,38 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   // task its own warp for RC <= 32 and at most two rounds for RC = 64 (the combine is a few
   // dependent global loads per task: latency, not bandwidth)
   if (launch_combine(ca, 8 * nsm, s) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+MLA_EXPORT mla_status mla_profile_begin(int32_t max_launches) {
+  using mla::g_prof;
+  if (max_launches < 1 || max_launches > mla::kMaxProfiledLaunches) return MLA_ERR_INVALID_ARG;
+  while ((int)g_prof.ev.size() < 2 * max_launches) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return MLA_ERR_CUDA;
+    g_prof.ev.push_back(e);
+  }
+  g_prof.cap = max_launches;
+  g_prof.next = 0;
+  g_prof.on = true;
+  return MLA_OK;
+}
+
+MLA_EXPORT mla_status mla_profile_end(double* total_ms, int32_t* launches) {
+  using mla::g_prof;
+  if (total_ms == nullptr || launches == nullptr) return MLA_ERR_INVALID_ARG;
+  const int n = g_prof.on ? g_prof.next : 0;
+  g_prof.on = false;
+  double sum = 0.0;
+  for (int i = 0; i < n; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    sum += ms;
+  }
+  *total_ms = sum;
+  *launches = n;
   return MLA_OK;
 }
 

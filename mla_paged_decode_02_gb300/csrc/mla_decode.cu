@@ -103,8 +103,11 @@ struct Cfg {
   static constexpr int NV = RC == 16 ? 3 : 2;
   static constexpr int kKStageBytes = KC * 8192;        // raw FP8 key position: 2 halves x KC x 4 KB
   static constexpr int NKS = FP8 ? (RC == 64 ? 3 : 2) : 0;   // raw staging depths
-  static constexpr int NVS = FP8 ? 2 : 0;
+  static constexpr int NVS = FP8 ? (RC == 64 ? 2 : 3) : 0;
   static constexpr int kKLoaders = FP8 ? 4 : 1;         // arrivals that fill a K slot
+  // FP8 values: 16-byte units a thread converts per unrolled round (code size against
+  // latency hiding; measured: 8 for 16 rows, 4 for 32 and 64)
+  static constexpr int kValueRound = RC == 16 ? 8 : 4;
   static constexpr int kVLoaders = 1;
   static_assert(!FP8 || kKTmemBase + NK * kKTmemSlotCols <= 512, "tensor memory budget");
   static_assert(kSlotsPerTile * KC == 9, "a tile is 9 chunks");
@@ -221,10 +224,10 @@ __device__ __forceinline__ bool iter_next(TileIter& it, const DecodeArgs& a, int
 // NaN in a value column becomes a finite number here; the same byte is a key column too,
 // whose exact conversion makes that key's score, and so the row's output, NaN.) Rows at or
 // past `valid` are written as zeros.
-template <int G>
+template <int G, int kRound>
 __device__ __forceinline__ void convert_value_pair(const uint8_t* src, uint8_t* dst, int valid, int gi) {
   constexpr int kPer = 1024 / G;                 // 16-byte units per thread
-  constexpr int kRound = kPer > 8 ? 8 : kPer;
+  static_assert(kPer % kRound == 0, "whole rounds");
 #pragma unroll 1
   for (int r0 = 0; r0 < kPer; r0 += kRound) {
     uint4 v[kRound];
@@ -592,24 +595,31 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         mbar_arrive(b_s_empty + 8 * sb);
 
         const int j = (U.tb + k) * kTileTokens + t;
-        float mr[RC];
-#pragma unroll
-        for (int r = 0; r < RC; r += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(mref_s + r);
-          mr[r] = v.x; mr[r + 1] = v.y; mr[r + 2] = v.z; mr[r + 3] = v.w;
-        }
+        // the reference maxima are read from shared memory (a broadcast) where they are
+        // used, rather than held in RC registers
+        auto mref4 = [&](int r) { return *reinterpret_cast<const float4*>(mref_s + r); };
         bool need = false;
         if ((U.tb + k + 1) * kTileTokens <= mask_from) {
 #pragma unroll
-          for (int r = 0; r < RC; ++r) {
-            s[r] *= c_log2;
-            need |= s[r] > mr[r] + kRescaleLog2;
+          for (int r = 0; r < RC; r += 4) {
+            const float4 m4 = mref4(r);
+            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              s[r + i] *= c_log2;
+              need |= s[r + i] > mm[i] + kRescaleLog2;
+            }
           }
         } else {
 #pragma unroll
-          for (int r = 0; r < RC; ++r) {
-            s[r] = j < nvis_s[r] ? s[r] * c_log2 : -INFINITY;
-            need |= s[r] > mr[r] + kRescaleLog2;
+          for (int r = 0; r < RC; r += 4) {
+            const float4 m4 = mref4(r);
+            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              s[r + i] = j < nvis_s[r + i] ? s[r + i] * c_log2 : -INFINITY;
+              need |= s[r + i] > mm[i] + kRescaleLog2;
+            }
           }
         }
         bool rescale = false;
@@ -629,21 +639,23 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           }
           named_bar_sync(kSoftmaxBar, 128);
 #pragma unroll
-          for (int r = 0; r < RC; ++r) {
-            lsum[r] *= alpha_s[r];
-            mr[r] = mref_s[r];
-          }
+          for (int r = 0; r < RC; ++r) lsum[r] *= alpha_s[r];
           rescale = k > 0;
         }
         // P^T row of this key, in registers until its buffer is free
         uint32_t pw[RC / 2];
 #pragma unroll
-        for (int r = 0; r < RC; r += 2) {
-          const float p0 = s[r] == -INFINITY ? 0.f : ex2_approx(s[r] - mr[r]);
-          const float p1 = s[r + 1] == -INFINITY ? 0.f : ex2_approx(s[r + 1] - mr[r + 1]);
-          pw[r / 2] = pack2<FP8>(p0, p1);
-          lsum[r] += p0;          // the normaliser sums the unrounded probabilities
-          lsum[r + 1] += p1;
+        for (int r = 0; r < RC; r += 4) {
+          const float4 m4 = mref4(r);
+          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+          for (int i = 0; i < 4; i += 2) {
+            const float p0 = s[r + i] == -INFINITY ? 0.f : ex2_approx(s[r + i] - mm[i]);
+            const float p1 = s[r + i + 1] == -INFINITY ? 0.f : ex2_approx(s[r + i + 1] - mm[i + 1]);
+            pw[(r + i) / 2] = pack2<FP8>(p0, p1);
+            lsum[r + i] += p0;      // the normaliser sums the unrounded probabilities
+            lsum[r + i + 1] += p1;
+          }
         }
         // the buffer's previous user, PV(n - NP), must have completed
         if (n >= (uint32_t)NP) {
@@ -691,7 +703,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
                                          (NV >= 3 || wait(b_vempty + 8 * vs, ((vcp / NV) & 1) ^ 1)));
             ok = !named_bar_or(kSoftmaxBar, 128, !mine);
             if (!ok) break;
-            convert_value_pair<128>(gVS + st * kVStageBytes, gV + vs * kVSlotBytes, valid, t);
+            convert_value_pair<128, C::kValueRound>(gVS + st * kVStageBytes, gV + vs * kVSlotBytes, valid, t);
             fence_proxy_async_smem();
             named_bar_sync(kSoftmaxBar, 128);
             if (t == 0) {
@@ -855,18 +867,19 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         tc_fence_after();
         const uint8_t* src = gKS + st * C::kKStageBytes + krow_off;
         const uint32_t tbase = lane_base + C::kKTmemBase + ks * C::kKTmemSlotCols;
-        uint4 raw[C::KC][4];
-#pragma unroll
-        for (int cc = 0; cc < C::KC; ++cc)
+        // one chunk per iteration: the five roles of a CTA share the SM's instruction
+        // caches, and the fully unrolled position (KC chunks) lost more to instruction
+        // fetch stalls than the loop costs (measured 10% slower with 16 query rows)
+#pragma unroll 1
+        for (int cc = 0; cc < C::KC; ++cc) {
+          uint4 raw[4];
 #pragma unroll
           for (int u16 = 0; u16 < 4; ++u16)
-            raw[cc][u16] = *reinterpret_cast<const uint4*>(src + cc * 512 + ((u16 ^ ((kr7 >> 1) & 3)) << 4));
-#pragma unroll
-        for (int cc = 0; cc < C::KC; ++cc) {
+            raw[u16] = *reinterpret_cast<const uint4*>(src + cc * 512 + ((u16 ^ ((kr7 >> 1) & 3)) << 4));
           uint32_t w[32];
 #pragma unroll
           for (int u16 = 0; u16 < 4; ++u16) {
-            const uint32_t b4[4] = {raw[cc][u16].x, raw[cc][u16].y, raw[cc][u16].z, raw[cc][u16].w};
+            const uint32_t b4[4] = {raw[u16].x, raw[u16].y, raw[u16].z, raw[u16].w};
 #pragma unroll
             for (int k2 = 0; k2 < 4; ++k2) {
               __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(b4[k2] & 0xFFFFu), __NV_E4M3);

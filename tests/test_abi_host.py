@@ -74,6 +74,16 @@ def test_decode_rejects_null_and_misaligned_pointers_without_a_gpu(lib):
     assert lib.mla_decode(ctypes.byref(unsup), *args) == -2
 
 
+def test_profile_window_arguments_without_a_gpu(lib):
+    assert lib.mla_profile_begin(0) == -1
+    assert lib.mla_profile_begin(4097) == -1
+    ms, n = ctypes.c_double(7.0), ctypes.c_int32(7)
+    assert lib.mla_profile_end(None, ctypes.byref(n)) == -1
+    assert lib.mla_profile_end(ctypes.byref(ms), None) == -1
+    assert lib.mla_profile_end(ctypes.byref(ms), ctypes.byref(n)) == 0     # no window open
+    assert ms.value == 0.0 and n.value == 0
+
+
 def test_cache_write_rejects_bad_arguments_without_a_gpu(lib):
     vp = ctypes.c_void_p
     good = vp(1 << 20)

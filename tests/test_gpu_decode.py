@@ -156,6 +156,21 @@ def test_repeated_calls_are_deterministic():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+def test_profile_window_times_the_decode_kernels_and_changes_nothing():
+    """Events around the decode launch (a timing window of two calls) leave the results
+    bit-identical; each window counts its launches and stops after max_launches."""
+    case = synth.make_case(B=4, s_q=1, H=16, page_size=64, seq_lens=[3000, 10, 700, 2500], seed=46)
+    g = GpuCase(case)
+    out0, lse0 = [t.clone() for t in g.decode()]
+    api.profile_begin(2)
+    for _ in range(3):
+        out1, lse1 = g.decode()
+    ms, n = api.profile_end()
+    assert n == 2 and 0.0 < ms < 1000.0
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+    assert api.profile_end() == (0.0, 0)          # the window is closed
+
+
 def test_out_of_range_block_table_entry_is_reported_not_faulted():
     case = synth.make_case(B=2, s_q=1, H=16, page_size=64, seq_lens=[100, 200], seed=45)
     g = GpuCase(case)
