@@ -82,6 +82,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// --------------------------------------------------------------------- E4M3 -> fp16
+// Two E4M3 bytes (the low 16 bits of v16; the low byte goes to the low half) to an fp16
+// pair in one hardware convert. Exact: every E4M3 value, subnormals and NaN included, is
+// an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 x;\n\t"
+      "cvt.u16.u32 x, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, x;\n\t}"
+      : "=r"(r) : "r"(v16));
+  return r;
+}
+
 // ------------------------------------------------------------ programmatic dependent launch
 // A kernel launched with programmatic stream serialisation may start while the previous
 // kernel on the stream is still running; it must execute griddep_wait() before it reads
