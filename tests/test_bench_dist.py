@@ -49,3 +49,16 @@ def test_two_gloo_ranks_agree_on_max_and_sum(tmp_path):
     assert [d["world"] for d in res] == [2, 2]
     assert all(d["max"] == 11.0 for d in res)
     assert all(d["sum"] == 3.0 for d in res)
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    """The DRAM-traffic table is keyed by a hash of the kernel code without its comments:
+    an edit of a comment keeps the key, any change of code (or a string) changes it."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+    src = 'int a = 1; // one\n/* block\n comment */ const char* s = "x // y";\n'
+    same = 'int a = 1;   // the value one\nconst char* s = "x // y"; /* other */\n'
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(src.replace("a = 1", "a = 2"))
+    assert bench._code_only(src) != bench._code_only(src.replace('"x // y"', '"x /* y"'))
+    assert len(bench.kernel_source_hash()) == 16
