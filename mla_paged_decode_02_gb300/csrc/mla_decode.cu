@@ -1,6 +1,7 @@
 // mla_decode.cu — split-KV paged MLA decode core for sm_103a (TMA + tcgen05 + TMEM).
 //
-// The operation ("[WIP][Attention] FlashAttn MLA": decode MQA in MLA; shapes from the
+// The operation ("[WIP][Attention] FlashAttn MLA", opening post: MLA decode runs as
+// multi-query attention over the latent cache; shapes from the
 // kernel-test log in "[Attention] Blackwell FP8 MLA support with CUTLASS_MLA backend"):
 // all query rows of a sequence (s_q new tokens x H heads, 576 wide) attend over one
 // shared latent row per token; scores use all 576 columns, values the first 512.
