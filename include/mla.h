@@ -4,8 +4,8 @@
  * What the library computes
  * -------------------------
  * "[WIP][Attention] FlashAttn MLA" (opening post) runs the decode step of MLA as
- * "decode MQA": after weight absorption, every query head attends over ONE shared
- * latent key/value head. The kernel-test log quoted in "[Attention] Blackwell FP8 MLA
+ * multi-query attention: after weight absorption, every query head attends over ONE
+ * shared latent key/value head. The kernel-test log quoted in "[Attention] Blackwell FP8 MLA
  * support with CUTLASS_MLA backend" (comment by elvischenv) fixes the shapes:
  * h_kv = 1, d = 576 (512 latent + 64 rope) for the scores, dv = 512 for the output,
  * s_q new tokens per sequence, causal, a paged cache, and an FP8 (float8_e4m3fn)
