@@ -1,4 +1,5 @@
-"""Compile the test-only tcgen05 layout probe into tests/native/libumma_probe.so."""
+"""Compile the test-only tcgen05 layout probes into tests/native/libumma_probe.so and
+tests/native/libumma_pair_probe.so."""
 import os
 import shutil
 import subprocess
@@ -7,17 +8,23 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-def build() -> str:
+def build_one(name: str) -> str:
     nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
-    out = os.path.join(HERE, "libumma_probe.so")
+    out = os.path.join(HERE, f"lib{name}.so")
     cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-std=c++17", "-lineinfo",
            "-Xcompiler", "-fPIC,-fvisibility=hidden", "-shared", "-o", out,
-           os.path.join(HERE, "umma_probe.cu")]
+           os.path.join(HERE, f"{name}.cu")]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("probe build failed")
+        raise RuntimeError(f"probe build failed: {name}")
     return out
+
+
+def build() -> list:
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=2) as ex:
+        return list(ex.map(build_one, ["umma_probe", "umma_pair_probe"]))
 
 
 if __name__ == "__main__":
