@@ -30,7 +30,7 @@ ProfileWindow g_prof;
 constexpr int kMaxProfiledLaunches = 4096;
 
 int variant_bit(int rc, bool fp8) {
-  return (rc == 16 ? 0 : rc == 32 ? 2 : 4) + (fp8 ? 1 : 0);
+  return (rc == 16 ? 0 : rc == 32 ? 2 : rc == 64 ? 4 : 6) + (fp8 ? 1 : 0);
 }
 
 cudaError_t current_device(int* dev) {
@@ -140,8 +140,8 @@ MLA_EXPORT size_t mla_decode_workspace_size(const mla_decode_params* p, int32_t 
     num_sms = sm_count(dev);
     if (num_sms <= 0) return 0;
   }
-  const int R = p->s_q * p->num_heads;
-  return ws_layout(p->batch, R, num_sms).total;
+  const Plan plan = make_plan(p->s_q * p->num_heads, p->kv_dtype == MLA_KV_FP8_E4M3);
+  return ws_layout(p->batch, plan, plan_workers(plan, num_sms)).total;
 }
 
 MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, const void* kv_cache,
@@ -165,15 +165,17 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   const int nsm = sm_count(dev);
   if (nsm <= 0) return MLA_ERR_CUDA;
   const int B = p->batch, R = p->s_q * p->num_heads;
-  const int rc = rows_per_group(R);
-  const int G = (R + rc - 1) / rc;
-  const WsLayout w = ws_layout(B, R, nsm);
+  const Plan plan = make_plan(R, fp8);
+  const int rc = plan.rc, G = plan.G;
+  const int grid = plan_workers(plan, nsm);
+  if (grid < 1) return MLA_ERR_UNSUPPORTED;
+  const WsLayout w = ws_layout(B, plan, grid);
   if (workspace_bytes < w.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
   if (!get_encoder()) return MLA_ERR_CUDA;
 
   const uint32_t bit = 1u << variant_bit(rc, fp8);
   if (!(g_prepared[dev].load() & bit)) {
-    if (decode_prepare(rc, fp8) != cudaSuccess) return MLA_ERR_CUDA;
+    if ((plan.pair ? decode_pair_prepare(fp8) : decode_prepare(rc, fp8)) != cudaSuccess) return MLA_ERR_CUDA;
     g_prepared[dev].fetch_or(bit);
   }
 
@@ -199,7 +201,8 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   sa.G = G;
   const int64_t cap = (int64_t)p->max_blocks_per_seq * p->page_size;
   sa.max_len = (int)(cap < p->max_seq_len ? cap : p->max_seq_len);
-  sa.grid = nsm;
+  sa.grid = grid;
+  sa.tile = plan.tile;
   sa.max_units = w.max_units;
   sa.max_split = w.max_split;
   sa.max_slots = w.max_slots;
@@ -207,11 +210,15 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
 
   DecodeArgs da;
   std::memset(&da, 0, sizeof(da));
-  if (!encode_q_map(&da.tm_q, q, B, R, rc)) return MLA_ERR_INVALID_ARG;
+  // a CTA of a pair holds 64 of its unit's 128 rows and loads keys one chunk at a time
+  if (!encode_q_map(&da.tm_q, q, B, R, plan.pair ? 64 : rc)) return MLA_ERR_INVALID_ARG;
   {
     const int64_t rows = (int64_t)p->num_pages * p->page_size;
-    if (!encode_kv_map(&da.tm_k, kv_cache, rows, (uint32_t)decode_key_chunks_per_slot(rc, fp8), fp8, true) ||
-        !encode_kv_map(&da.tm_v, kv_cache, rows, 2, fp8, false))
+    // chunks per key / value box: a pair loads 2 / 4 adjacent chunks of each row
+    const uint32_t kc = plan.pair ? 2u : (uint32_t)decode_key_chunks_per_slot(rc, fp8);
+    const uint32_t vc = plan.pair ? 4u : 2u;
+    if (!encode_kv_map(&da.tm_k, kv_cache, rows, kc, fp8, true) ||
+        !encode_kv_map(&da.tm_v, kv_cache, rows, vc, fp8, false))
       return MLA_ERR_INVALID_ARG;
   }
   da.kv_cache = kv_cache;
@@ -236,7 +243,8 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   da.softmax_scale = softmax_scale;
   const bool timed = g_prof.on && g_prof.next < g_prof.cap;
   if (timed && cudaEventRecord(g_prof.ev[2 * g_prof.next], s) != cudaSuccess) return MLA_ERR_CUDA;
-  if (launch_decode(da, rc, fp8, nsm, s) != cudaSuccess) return MLA_ERR_CUDA;
+  const cudaError_t le = plan.pair ? launch_decode_pair(da, fp8, grid, s) : launch_decode(da, rc, fp8, grid, s);
+  if (le != cudaSuccess) return MLA_ERR_CUDA;
   if (timed) {
     if (cudaEventRecord(g_prof.ev[2 * g_prof.next + 1], s) != cudaSuccess) return MLA_ERR_CUDA;
     ++g_prof.next;
@@ -251,9 +259,9 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   ca.lse = lse;
   ca.R = R;
   ca.RC = rc;
-  // up to 2 * #SM cut streams x RC rows: 8 * #SM blocks of 8 warps give every (stream, row)
-  // task its own warp for RC <= 32 and at most two rounds for RC = 64 (the combine is a few
-  // dependent global loads per task: latency, not bandwidth)
+  // up to 2 * workers cut streams x RC rows: 8 * #SM blocks of 8 warps give every (stream,
+  // row) task its own warp for RC <= 32 and at most two rounds for RC = 64 or 128 (the
+  // combine is a few dependent global loads per task: latency, not bandwidth)
   if (launch_combine(ca, 8 * nsm, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }

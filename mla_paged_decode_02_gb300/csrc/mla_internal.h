@@ -16,9 +16,25 @@ constexpr int kMaxSeqLen = 1 << 20;
 constexpr int kMaxRows = 4096;     // s_q * H
 constexpr int kMaxBatch = 1 << 16;
 
-// Query rows (s_q * H of them per sequence) are processed in groups of RC rows; RC is
-// the N of every MMA. 16/32/64 are instantiated.
-inline int rows_per_group(int rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 : 64; }
+// Execution plan for the s_q * H query rows of a sequence. Rows are processed in groups
+// of RC rows (the N of every MMA). Up to 64 rows: one CTA per SM, RC = 16/32/64, 128-key
+// tiles. More than 64 rows with a bf16 cache: CTA pairs (a cluster of two CTAs on two
+// SMs) with RC = 128 and 256-key tiles, each CTA holding 128 of the keys and 64 of the
+// rows, so that every key tile is read once for 128 rows. The schedule's workers are
+// SMs or CTA pairs.
+struct Plan {
+  int rc, G, tile;
+  bool pair;
+};
+inline Plan make_plan(int rows, bool fp8) {
+  Plan p;
+  p.pair = rows > 64 && !fp8;
+  p.rc = p.pair ? 128 : rows <= 16 ? 16 : rows <= 32 ? 32 : 64;
+  p.G = (rows + p.rc - 1) / p.rc;
+  p.tile = p.pair ? 2 * kTileTokens : kTileTokens;
+  return p;
+}
+inline int plan_workers(const Plan& p, int num_sms) { return p.pair ? num_sms / 2 : num_sms; }
 
 // Workspace: [header 256 B][batch_info int4 x B][cta_first int32 x (grid + 1)]
 //            [split_list int4 x max_split][units int4 x max_units]
@@ -34,10 +50,10 @@ struct WsLayout {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout ws_layout(int B, int R, int grid) {
+inline WsLayout ws_layout(int B, const Plan& p, int grid) {
   WsLayout w{};
-  const int rc = rows_per_group(R);
-  const int64_t G = (R + rc - 1) / rc;
+  const int rc = p.rc;
+  const int64_t G = p.G;
   w.max_units = (int64_t)B * G + grid;
   w.max_split = grid;
   w.max_slots = 2 * (int64_t)grid;
@@ -60,6 +76,7 @@ struct SchedArgs {
   int4* split_list;      // (b, g, pieces, first partial slot) of every cut stream
   int4* units;           // (b, g, tile_begin | tile_end << 16, partial slot or -1)
   int32_t B, s_q, G, max_len, grid;
+  int32_t tile;          // keys per tile (128, or 256 for CTA pairs)
   int64_t max_units, max_split, max_slots;
 };
 
@@ -97,6 +114,9 @@ struct CombineArgs {
 
 // Launchers (return the launch error).
 cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t s);
+// CTA-pair decode (rc = 128): grid = 2 * pairs CTAs in clusters of two.
+cudaError_t launch_decode_pair(const DecodeArgs& a, bool fp8, int pairs, cudaStream_t s);
+cudaError_t decode_pair_prepare(bool fp8);
 cudaError_t launch_decode(const DecodeArgs& a, int rc, bool fp8, int grid, cudaStream_t s);
 cudaError_t decode_prepare(int rc, bool fp8);   // per-device kernel attributes
 int decode_key_chunks_per_slot(int rc, bool fp8);  // chunks in one key TMA box

@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
 
   // 1. key tiles per sequence (lengths clamped into the valid range; bad ones flagged)
   int64_t my_tiles = 0;
-  for (int b = b0; b < b1; ++b) my_tiles += (clamped_len(a, b, true) + kTileTokens - 1) / kTileTokens;
+  for (int b = b0; b < b1; ++b) my_tiles += (clamped_len(a, b, true) + a.tile - 1) / a.tile;
   int64_t n_tiles;
   const int64_t tile_off = block_exclusive_scan(my_tiles, scan_tmp, &n_tiles);
   const int64_t W = (int64_t)G * n_tiles;
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
     int64_t my_units = 0, my_split = 0, my_slots = 0;
     int64_t pre = goff + tile_off;
     for (int b = b0; b < b1; ++b) {
-      const int n = (clamped_len(a, b, false) + kTileTokens - 1) / kTileTokens;
+      const int n = (clamped_len(a, b, false) + a.tile - 1) / a.tile;
       const int64_t ns = (pre + n - 1) / q - pre / q + 1;
       my_units += ns;
       if (ns >= 2) { my_split += 1; my_slots += ns; }
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
     pre = goff + tile_off;
     for (int b = b0; b < b1; ++b) {
       const int Lc = clamped_len(a, b, false);
-      const int n = (Lc + kTileTokens - 1) / kTileTokens;
+      const int n = (Lc + a.tile - 1) / a.tile;
       if (g == 0) a.batch_info[b] = make_int4(n, 0, Lc, 0);
       const int64_t c_lo = pre / q;
       const int ns = (int)((pre + n - 1) / q - c_lo + 1);

@@ -87,6 +87,19 @@ SMALL = [
     (3, 1, 128, 128, [1500, 130, 2000], F8, True),
     (2, 1, 64, 64, [4096, 3000], F8, True),
     (2, 3, 16, 64, [3, 129], F8, True),
+    # more than 64 rows, bf16 cache: CTA pairs, 128-row groups, 256-key super-tiles
+    (2, 1, 128, 64, [1, 255], BF, True),             # a single key; one short of a super-tile
+    (3, 1, 128, 64, [256, 257, 513], BF, True),      # super-tile edges
+    (3, 1, 128, 128, [64, 65, 190], BF, True),       # 64-key block edges, ragged 16-key steps
+    (2, 1, 128, 128, [77, 4000], BF, True),          # split across many pairs, 128-row combine
+    (2, 2, 128, 64, [300, 70], BF, True),            # two row groups, causal
+    (2, 1, 96, 64, [500, 129], BF, True),            # a partly filled row group
+    (2, 2, 64, 64, [1000, 65], BF, True),            # 128 rows from s_q = 2
+    (1, 4, 128, 64, [5000], BF, False),              # four row groups, non-causal, splits
+    (2, 1, 8, 64, [700, 1300], BF, True),            # H = 8 (TP = 16 of 128 heads)
+    (2, 1, 64, 64, [900, 2100], BF, True),           # H = 64 (TP = 2)
+    (2, 1, 16, 256, [300, 1100], BF, True),          # page size 256
+    (2, 1, 128, 256, [300, 1100], BF, True),
 ]
 
 

@@ -3,7 +3,8 @@
 The scheduler lays the (row group, sequence) streams of key tiles end to end and gives
 CTA c the positions [c q, (c + 1) q), q = ceil(W / grid); when the G row groups divide the
 grid, each group gets grid / G CTAs and the same partition of its N tiles instead
-(q = ceil(N / (grid / G))). Checked here on the device's own output: every tile of every
+(q = ceil(N / (grid / G))). With more than 64 rows and a bf16 cache the workers are CTA
+pairs (grid = #SM / 2), a row group is 128 rows and a tile 256 keys. Checked here on the device's own output: every tile of every
 stream is covered exactly once, every CTA's units are a contiguous range holding exactly
 its share of tiles, and only streams cut by a CTA boundary get partial slots (consecutive
 ones). The workspace offsets below restate the
@@ -26,8 +27,15 @@ def _cuda():
         pytest.skip("no CUDA device")
 
 
+def _plan(R, nsm):
+    """(rows per group, keys per tile, schedule workers) for R rows and a bf16 cache."""
+    if R > 64:
+        return 128, 256, nsm // 2
+    return (16 if R <= 16 else 32 if R <= 32 else 64), 128, nsm
+
+
 def _offsets(B, R, grid):
-    rc = 16 if R <= 16 else 32 if R <= 32 else 64
+    rc = _plan(R, 2 * grid)[0]
     G = -(-R // rc)
     al = lambda x: (x + 255) // 256 * 256
     off = 256
@@ -46,6 +54,8 @@ CASES = [
     (4, 1, 16, 64, [5000, 17, 640, 2049]),
     (3, 4, 128, 64, [1000, 67, 3000]),
     (2, 1, 128, 128, [300, 1000]),
+    (2, 2, 128, 64, [4000, 70]),
+    (3, 1, 96, 64, [500, 129, 20000]),
     (1, 1, 16, 64, [131072]),
     (300, 1, 16, 64, (1, 700)),
 ]
@@ -57,8 +67,8 @@ def test_partition_is_exact_and_balanced(B, s_q, H, P, lens):
     g = GpuCase(case)
     g.decode()
     torch.cuda.synchronize()
-    grid = torch.cuda.get_device_properties(0).multi_processor_count
     R = s_q * H
+    _, tile, grid = _plan(R, torch.cuda.get_device_properties(0).multi_processor_count)
     rc, G, cta_off, split_off, units_off = _offsets(B, R, grid)
     ws = g.workspace.cpu().numpy().view(np.uint8)
     hdr = ws[:16].view(np.uint32)
@@ -68,7 +78,7 @@ def test_partition_is_exact_and_balanced(B, s_q, H, P, lens):
     units = ws[units_off:units_off + 16 * n_units].view(np.int32).reshape(n_units, 4)
     splits = ws[split_off:split_off + 16 * n_split].view(np.int32).reshape(n_split, 4)
 
-    n_b = (case.seq_lens.astype(np.int64) + 127) // 128
+    n_b = (case.seq_lens.astype(np.int64) + tile - 1) // tile
     N = int(n_b.sum())
     W = G * N
     aligned = G > 1 and grid % G == 0
