@@ -2,8 +2,12 @@
 
 A step is one pass of the hot path over one batch: the cache write of the step's new
 tokens (B * s_q rows) followed by mla_decode (split scheduler, split-KV decode, LSE
-combine). The default workload is the ragged-batch configuration (B=128, s_q=1, H=16,
-page 64, seq_lens ~ U[2048, 6144], bf16 cache); --config picks another.
+combine). The default workload is the DeepSeek-V3-shaped batch (B=512, s_q=1, H=128,
+page 128, seq_lens ~ U[1000, 2000], bf16 cache); --config / --kv / --s_q pick another.
+
+per_config  (N=1) the decode kernel and call timed on each of the other workloads: the
+           16-head ragged batch (bf16 and FP8), the 128-head batch with the FP8 cache and
+           the long-context FP8 batch at s_q = 1 and 4, each with its roofline
 
 value      decode TFLOP/s of the whole job (algorithmic flops 2*(576+512) per visible
            (row, head, key), summed over ranks) with inputs resident in HBM
@@ -46,11 +50,12 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--kv", default=None, choices=[None, "bf16", "fp8"])
     ap.add_argument("--s_q", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true")
     return ap.parse_args()
 
 
@@ -217,6 +222,85 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def roofline(case, kern_ms, flops, kv_bytes, q_bytes):
+    """The decode kernel's roofline: the slower of the flops at the bf16 tensor peak and the
+    KV + Q bytes at the HBM copy bandwidth (both measured on this GPU model)."""
+    peaks, peak_kind = load_peaks()
+    t = kern_ms * 1e-3
+    hbm_t = (kv_bytes + q_bytes) / (peaks["hbm_gbs"] * 1e9)
+    tc_t = flops / (peaks["bf16_tflops"] * 1e12)
+    if hbm_t >= tc_t:
+        roof = {"bound": "hbm", "achieved": (kv_bytes + q_bytes) / t / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = ncu_traffic(case.name)
+    roof["peak_source"] = f"{peak_kind} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops'})"
+    roof["t_roof_us"] = max(hbm_t, tc_t) * 1e6
+    roof["decode_kernel_us"] = kern_ms * 1e3
+    return roof, max(hbm_t, tc_t)
+
+
+PER_CONFIG = [(2, None, None), (3, None, None), (4, "bf16", None), (4, "fp8", None), (5, None, 1), (5, None, 4)]
+
+
+def measure_config(cfg, kv, s_q, steps, warmup, device):
+    """Decode kernel and decode call of one workload (inputs resident, L2 flushed between
+    calls when the cache is smaller than three times L2): CUDA events on the stream."""
+    import torch
+    from mla_paged_decode_02_gb300 import api, synth
+    from mla_paged_decode_02_gb300.workload import DeviceWorkload
+    kvd = None if kv is None else (synth.KV_BF16 if kv == "bf16" else synth.KV_FP8_E4M3)
+    case = synth.make_config(cfg, kv_dtype=kvd, s_q=s_q)
+    g = DeviceWorkload(case, device=device)
+    flops, kv_bytes, q_bytes, _ = algorithmic(case)
+    stream = torch.cuda.current_stream()
+    out = torch.empty((case.B, case.s_q, case.H, 512), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((case.B, case.s_q, case.H), dtype=torch.float32, device=device)
+    flush = torch.empty(int(512e6), dtype=torch.uint8, device=device) if kv_bytes < 3 * 129e6 else None
+
+    def call():
+        g.decode(out=out, lse=lse)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    st, bits = api.decode_check(g.workspace)
+    if st != 0:
+        raise RuntimeError(f"{case.name}: device error word {bits:#x}")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for k in range(steps):
+        if flush is not None:
+            flush.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        call()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    call_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    for k in range(steps):
+        if flush is not None:
+            flush.fill_(k & 0xFF)
+        if k == 0:
+            api.profile_begin(steps)
+        call()
+    kern_total, n = api.profile_end()
+    kern_ms = kern_total / n
+    roof, t_roof = roofline(case, kern_ms, flops, kv_bytes, q_bytes)
+    roof["decode_call_us"] = call_ms * 1e3
+    roof["call_frac"] = t_roof / (call_ms * 1e-3)
+    res = {"workload": case.name, "B": case.B, "s_q": case.s_q, "H": case.H, "page_size": case.page_size,
+           "kv": "fp8_e4m3" if case.kv_dtype else "bf16", "tokens": int(case.seq_lens.sum()),
+           "decode_tflops": round(flops / (kern_ms * 1e-3) / 1e12, 3),
+           "kv_gbs": round(kv_bytes / (kern_ms * 1e-3) / 1e9, 1),
+           "l2": "flushed between calls" if flush is not None else "inputs larger than L2",
+           "roofline": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in roof.items()}}
+    del g, flush, out, lse
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank, local_rank, world):
     import torch
     from mla_paged_decode_02_gb300 import api
@@ -361,25 +445,11 @@ def run_ours(args, rank, local_rank, world):
     e2e_value = total_flops / (e2e_ms * 1e-3) / 1e12
 
     # ---- roofline of the decode kernel
-    peaks, peak_kind = load_peaks()
-    t = kern_ms * 1e-3
-    hbm_t = (kv_bytes + q_bytes) / (peaks["hbm_gbs"] * 1e9)
-    tc_t = flops / (peaks["bf16_tflops"] * 1e12)
-    if hbm_t >= tc_t:
-        roof = {"bound": "hbm", "achieved": (kv_bytes + q_bytes) / t / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    else:
-        roof = {"bound": "tensor", "achieved": flops / t / 1e12, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = ncu_traffic(case.name)
-    roof["peak_source"] = f"{peak_kind} ({'hbm_gbs' if roof['bound'] == 'hbm' else 'bf16_tflops'})"
-    roof["t_roof_us"] = max(hbm_t, tc_t) * 1e6
-    roof["decode_kernel_us"] = kern_ms * 1e3
+    roof, t_roof = roofline(case, kern_ms, flops, kv_bytes, q_bytes)
     roof["kernel_timed"] = ("decode_kernel: CUDA events recorded by the library around its launch "
                             "(mla_profile_begin/end), a second pass of the same K steps")
     roof["decode_call_us"] = dec_ms * 1e3
-    roof["call_frac"] = max(hbm_t, tc_t) / (dec_ms * 1e-3)
+    roof["call_frac"] = t_roof / (dec_ms * 1e-3)
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
@@ -398,6 +468,14 @@ def run_ours(args, rank, local_rank, world):
         "gpu_launches": 4 * args.steps,      # cache write, scheduler, decode, combine per step
         "clocks": clk,
     }
+    if world == 1 and not args.no_per_config:
+        del g
+        torch.cuda.empty_cache()
+        from mla_paged_decode_02_gb300 import synth
+        kvd = lambda kv: None if kv is None else (synth.KV_BF16 if kv == "bf16" else synth.KV_FP8_E4M3)
+        line["per_config"] = [measure_config(c, kv, sq, max(args.steps, 10), max(args.warmup, 3), device)
+                              for c, kv, sq in PER_CONFIG
+                              if synth.config_name(c, kvd(kv), sq) != case.name]
     return line, case
 
 

@@ -31,9 +31,9 @@
  *   allocates device memory, never frees, and never synchronises the stream.
  * - Layouts are dense row-major as written next to each argument.
  * - Neither outputs nor the workspace need to be zeroed beforehand: every value a
- *   kernel reads from them it wrote earlier in the same call ("does this need to be
- *   torch.zeros? or does torch.empty work" — review thread of "[NVIDIA] Add Cutlass
- *   MLA backend": empty works).
+ *   kernel reads from them it wrote earlier in the same call. (The review thread of
+ *   "[NVIDIA] Add Cutlass MLA backend" asks whether the prior kernel's output must be
+ *   zero-filled by the caller; here uninitialised buffers are fine.)
  * - Host-detectable errors return a negative mla_status and launch nothing.
  *   Errors only the device can see (a block-table entry outside [0, num_pages), a
  *   sequence length outside [s_q, min(max_seq_len, max_blocks_per_seq*page_size)],
@@ -65,7 +65,8 @@ typedef enum {
   MLA_ERR_CUDA = -4,                 /* a CUDA runtime call failed (e.g. no device) */
   MLA_ERR_TIMEOUT = -5,              /* device error word: a pipeline wait gave up */
   MLA_ERR_DEVICE_INDEX = -6          /* device error word: a block-table entry, sequence
-                                        length or slot was out of range */
+                                        length, slot or (FP8 cache) query value was out of
+                                        range */
 } mla_status;
 
 typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
@@ -146,6 +147,8 @@ mla_status mla_cache_write(const void* latent, const void* rope, const int64_t* 
  * cudaFree or other allocating call is made.
  * - Returns MLA_ERR_WORKSPACE_TOO_SMALL, launching nothing, when the parameters need
  *   more scratch than that (mla_decode_workspace_size(p, 0) > MLA_NOALLOC_SCRATCH_BYTES).
+ *   On a 152-SM GB300 that admits up to 32 query rows per sequence (s_q * H <= 32, e.g.
+ *   16 or 32 heads at s_q = 1); 64 or more rows need more split scratch and are refused.
  * - The first call on a device looks up the array's device address (with that device
  *   current) and caches it; make that first call before any stream capture.
  * - All calls share the one array, which keeps the last call's contents (nothing in it
@@ -156,6 +159,11 @@ mla_status mla_decode_noalloc(const mla_decode_params* p, const void* q, const v
                               const int32_t* block_table, const int32_t* seq_lens,
                               float softmax_scale, const float* kv_scale, void* out, float* lse,
                               mla_stream_t stream);
+
+/* mla_decode_check for mla_decode_noalloc: synchronises `stream` and reads the device error
+ * word that the last no-allocation call left in the library's static scratch array (same
+ * results and `bits` as mla_decode_check). Allocates nothing. */
+mla_status mla_decode_noalloc_check(mla_stream_t stream, uint32_t* bits);
 
 /* Decode-kernel timing, for benchmarks and tests. After mla_profile_begin(n), each of the
  * next n mla_decode / mla_decode_noalloc calls in this process records a CUDA event on

@@ -21,8 +21,8 @@ STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED",
           -3: "MLA_ERR_WORKSPACE_TOO_SMALL", -4: "MLA_ERR_CUDA", -5: "MLA_ERR_TIMEOUT",
           -6: "MLA_ERR_DEVICE_INDEX"}
 EXPORTS = ("mla_abi_version", "mla_status_string", "mla_decode_workspace_size", "mla_decode",
-           "mla_decode_check", "mla_cache_write", "mla_decode_noalloc", "mla_profile_begin",
-           "mla_profile_end")
+           "mla_decode_check", "mla_cache_write", "mla_decode_noalloc", "mla_decode_noalloc_check",
+           "mla_profile_begin", "mla_profile_end")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla.so")
@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
         L.mla_decode_noalloc.restype = i32
         L.mla_decode_noalloc.argtypes = [ctypes.POINTER(DecodeParams), vp, vp, vp, vp, ctypes.c_float,
                                          vp, vp, vp, vp]
+        L.mla_decode_noalloc_check.restype = i32
+        L.mla_decode_noalloc_check.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         L.mla_cache_write.restype = i32
         L.mla_cache_write.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, vp, vp, vp]
         L.mla_profile_begin.restype = i32
@@ -113,14 +115,9 @@ def _kv_dtype_of(kv_cache: torch.Tensor) -> int:
     raise TypeError(f"kv_cache dtype {kv_cache.dtype}: expected bfloat16, uint8 or float8_e4m3fn")
 
 
-def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
-           seq_lens: torch.Tensor, softmax_scale: float, kv_scale: torch.Tensor | None = None,
-           *, max_seq_len: int, causal: bool = True, out: torch.Tensor | None = None,
-           lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-           stream=None):
-    """Paged MLA decode. q [B, s_q, H, 576] bf16; kv_cache [Np, P, 576] (bf16, or uint8 /
-    float8_e4m3fn bytes); block_table [B, MB] int32; seq_lens [B] int32; kv_scale a
-    1-element float32 device tensor for the FP8 cache. Returns (out, lse)."""
+def _decode_inputs(q, kv_cache, block_table, seq_lens, kv_scale, max_seq_len, causal, out, lse):
+    """Check the decode inputs (the library reads them asynchronously, so they are used as
+    given: no temporary copies), allocate missing outputs, and build the parameters."""
     B, s_q, H, d = q.shape
     if d != D_QK or q.dtype != torch.bfloat16 or not q.is_contiguous():
         raise ValueError("q must be a contiguous bf16 [B, s_q, H, 576] tensor")
@@ -129,7 +126,10 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
         raise ValueError("kv_cache must be a contiguous [Np, P, 576] tensor")
     if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise ValueError("block_table and seq_lens must be int32")
-    block_table = block_table.contiguous()
+    if not block_table.is_contiguous() or not seq_lens.is_contiguous():
+        raise ValueError("block_table and seq_lens must be contiguous")
+    if block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("block_table must be [B, MB] and seq_lens [B]")
     kvd = _kv_dtype_of(kv_cache)
     if kvd == KV_FP8_E4M3 and (kv_scale is None or kv_scale.dtype != torch.float32):
         raise ValueError("the FP8 cache needs kv_scale as a float32 device tensor")
@@ -138,6 +138,19 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
         out = torch.empty((B, s_q, H, D_V), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, s_q, H), dtype=torch.float32, device=q.device)
+    return params, kvd, out, lse
+
+
+def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+           seq_lens: torch.Tensor, softmax_scale: float, kv_scale: torch.Tensor | None = None,
+           *, max_seq_len: int, causal: bool = True, out: torch.Tensor | None = None,
+           lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+           stream=None):
+    """Paged MLA decode. q [B, s_q, H, 576] bf16; kv_cache [Np, P, 576] (bf16, or uint8 /
+    float8_e4m3fn bytes); block_table [B, MB] int32; seq_lens [B] int32; kv_scale a
+    1-element float32 device tensor for the FP8 cache. Returns (out, lse)."""
+    params, kvd, out, lse = _decode_inputs(q, kv_cache, block_table, seq_lens, kv_scale, max_seq_len,
+                                           causal, out, lse)
     if workspace is None:
         workspace = alloc_workspace(params, q.device)
     st = lib().mla_decode(ctypes.byref(params), _ptr(q), _ptr(kv_cache), _ptr(block_table),
@@ -155,23 +168,23 @@ def decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.T
                    lse: torch.Tensor | None = None, stream=None):
     """decode() without a workspace, for callers that cannot allocate device memory: the
     library's own static scratch array (NOALLOC_SCRATCH_BYTES) is used instead. Calls
-    must not overlap on the GPU."""
-    B, s_q, H, _ = q.shape
-    Np, P, _ = kv_cache.shape
-    kvd = _kv_dtype_of(kv_cache)
-    params = make_params(B, s_q, H, P, Np, block_table.shape[1], max_seq_len, kvd, causal)
-    if out is None:
-        out = torch.empty((B, s_q, H, D_V), dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty((B, s_q, H), dtype=torch.float32, device=q.device)
-    st = lib().mla_decode_noalloc(ctypes.byref(params), _ptr(q), _ptr(kv_cache),
-                                  _ptr(block_table.contiguous()), _ptr(seq_lens),
-                                  ctypes.c_float(softmax_scale),
+    must not overlap on the GPU; pass out and lse to allocate nothing here either."""
+    params, kvd, out, lse = _decode_inputs(q, kv_cache, block_table, seq_lens, kv_scale, max_seq_len,
+                                           causal, out, lse)
+    st = lib().mla_decode_noalloc(ctypes.byref(params), _ptr(q), _ptr(kv_cache), _ptr(block_table),
+                                  _ptr(seq_lens), ctypes.c_float(softmax_scale),
                                   _ptr(kv_scale) if kvd == KV_FP8_E4M3 else None, _ptr(out),
                                   _ptr(lse), _stream(stream))
     if st != MLA_OK:
         raise MLAError(st, "mla_decode_noalloc")
     return out, lse
+
+
+def decode_noalloc_check(stream=None):
+    """Synchronise and read the device error word of the last decode_noalloc: (status, bits)."""
+    bits = ctypes.c_uint32(0)
+    st = lib().mla_decode_noalloc_check(_stream(stream), ctypes.byref(bits))
+    return int(st), int(bits.value)
 
 
 def decode_check(workspace: torch.Tensor, stream=None):
@@ -206,11 +219,11 @@ def cache_write(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch.Te
     if latent.shape != (n, 512) or rope.shape != (n, 64) or latent.dtype != torch.bfloat16 \
             or rope.dtype != torch.bfloat16 or not latent.is_contiguous() or not rope.is_contiguous():
         raise ValueError("latent [N,512] and rope [N,64] must be contiguous bf16")
-    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != n:
-        raise ValueError("slot_mapping must be int64 [N]")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != n or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous int64 [N] tensor")
     Np, P, _ = kv_cache.shape
     kvd = _kv_dtype_of(kv_cache)
-    st = lib().mla_cache_write(_ptr(latent), _ptr(rope), _ptr(slot_mapping.contiguous()), n,
+    st = lib().mla_cache_write(_ptr(latent), _ptr(rope), _ptr(slot_mapping), n,
                                _ptr(kv_cache), Np, P, kvd,
                                _ptr(kv_scale) if kvd == KV_FP8_E4M3 else None,
                                _ptr(device_error), _stream(stream))

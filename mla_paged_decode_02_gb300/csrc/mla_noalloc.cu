@@ -13,7 +13,8 @@
 // that device, with that device current) and cached. Every call shares the one array:
 // two calls that overlap on the GPU (on different streams, or from different threads)
 // race on it. Nothing needs clearing between calls: the scheduler kernel writes every
-// scratch word the later kernels read, in the same call.
+// scratch word the later kernels read, in the same call. mla_decode_noalloc_check reads
+// the device error word the last call left at the start of the array.
 #include <atomic>
 #include <cuda_runtime.h>
 #include "mla_internal.h"
@@ -60,4 +61,11 @@ extern "C" __attribute__((visibility("default"))) mla_status mla_decode_noalloc(
   if (mla::scratch_address(&scratch) != cudaSuccess) return MLA_ERR_CUDA;
   return mla_decode(p, q, kv_cache, block_table, seq_lens, softmax_scale, kv_scale, out, lse,
                     scratch, mla::kNoAllocScratchBytes, stream);
+}
+
+extern "C" __attribute__((visibility("default"))) mla_status mla_decode_noalloc_check(mla_stream_t stream,
+                                                                                  uint32_t* bits) {
+  void* scratch = nullptr;
+  if (mla::scratch_address(&scratch) != cudaSuccess) return MLA_ERR_CUDA;
+  return mla_decode_check(scratch, stream, bits);
 }

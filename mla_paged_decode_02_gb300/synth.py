@@ -179,15 +179,24 @@ CONFIGS = {
 SEED_OF = {1: 1001, 2: 1002, 3: 1002, 4: 1004, 5: 1005}
 
 
+def config_name(config_id: int, kv_dtype: int | None = None, s_q: int | None = None) -> str:
+    """Name of a workload (no data is drawn)."""
+    kw = CONFIGS[config_id]
+    kv = kw["kv_dtype"] if kv_dtype is None else kv_dtype
+    sq = kw["s_q"] if s_q is None else s_q
+    name = kw["name"]
+    if kv == KV_FP8_E4M3 and not name.endswith("fp8"):
+        name += "_fp8"
+    if sq != 1:
+        name += f"_sq{sq}"
+    return name
+
+
 def make_config(config_id: int, kv_dtype: int | None = None, s_q: int | None = None) -> DecodeCase:
     kw = dict(CONFIGS[config_id])
     if kv_dtype is not None:
         kw["kv_dtype"] = kv_dtype
     if s_q is not None:
         kw["s_q"] = s_q
-    name = kw.pop("name")
-    if kw["kv_dtype"] == KV_FP8_E4M3 and not name.endswith("fp8"):
-        name += "_fp8"
-    if kw["s_q"] != 1:
-        name += f"_sq{kw['s_q']}"
-    return make_case(seed=SEED_OF[config_id], name=name, **kw)
+    kw.pop("name")
+    return make_case(seed=SEED_OF[config_id], name=config_name(config_id, kv_dtype, s_q), **kw)

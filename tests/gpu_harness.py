@@ -54,11 +54,3 @@ def compare(case, out_gpu: torch.Tensor, lse_gpu: torch.Tensor, out_ref: np.ndar
         assert stats["cos_diff"] < FP8_COS_DIFF, stats
     assert lse_err <= LSE_ABS, stats
     return stats
-
-
-def sample_rows(case, n_batches=12, n_heads=6, seed=0):
-    """A deterministic sample of (b, i, h): first, last and random batches; all s_q rows."""
-    rng = np.random.default_rng(seed)
-    bs = sorted(set([0, case.B - 1] + list(rng.choice(case.B, size=min(case.B, n_batches), replace=False))))
-    hs = sorted(set([0, case.H - 1] + list(rng.choice(case.H, size=min(case.H, n_heads), replace=False))))
-    return [(b, i, h) for b in bs for i in range(case.s_q) for h in hs]

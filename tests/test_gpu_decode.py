@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_harness import GpuCase, compare, oracle_decode, sample_rows, torch_bf16_to_bits
+from gpu_harness import GpuCase, compare, oracle_decode, torch_bf16_to_bits
 from mla_paged_decode_02_gb300 import api, synth
 from oracle import fp8_e4m3
 from oracle import mla_oracle as O
@@ -194,6 +194,24 @@ def test_out_of_range_block_table_entry_is_reported_not_faulted():
     assert bits & 0x1
 
 
+def test_fp8_query_beyond_the_float16_range_is_reported():
+    """With an FP8 cache the MMAs run in fp16, so q is converted bf16 -> fp16; a query value
+    above the fp16 range is flagged in the device error word (MLA_DEVERR_Q_RANGE) rather
+    than silently saturated, and a clean call afterwards reports nothing."""
+    case = synth.make_case(B=2, s_q=1, H=16, page_size=64, seq_lens=[100, 200], seed=47, kv_dtype=F8)
+    g = GpuCase(case)
+    q0 = g.q.clone()
+    g.q[1, 0, 5, 17] = 1.0e5                       # a bf16 value, above 65504
+    g.decode()
+    st, bits = api.decode_check(g.workspace)
+    assert st == -6 and bits & 0x4
+    g.q = q0
+    out, lse = g.decode()
+    assert api.decode_check(g.workspace) == (0, 0)
+    ro, rl = oracle_decode(case, g.cache_numpy())
+    compare(case, out, lse, ro, rl)
+
+
 def test_bad_arguments_launch_nothing():
     case = synth.make_case(B=1, s_q=1, H=16, page_size=64, seq_lens=[10], seed=46)
     g = GpuCase(case)
@@ -208,19 +226,19 @@ FULL = [(2, None, None), (3, None, None), (4, BF, None), (4, F8, None), (5, None
 
 
 @pytest.mark.parametrize("cfg,kv,s_q", FULL)
-def test_full_size_configs_sampled_rows(cfg, kv, s_q):
+def test_full_size_configs_every_row(cfg, kv, s_q):
+    """Each full-size workload, every output element and LSE against the float64 oracle (the
+    oracle walks each sequence's pages once; seconds per workload on the host cores)."""
     case = synth.make_config(cfg, kv_dtype=kv, s_q=s_q)
     g = GpuCase(case)
     out, lse = g.decode()
     torch.cuda.synchronize()
     st, bits = api.decode_check(g.workspace)
     assert st == 0 and bits == 0
-    # properties over every row
-    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
-    rows = sample_rows(case, n_batches=4 if cfg == 5 else 10, n_heads=4)
+    cache = g.cache_numpy()
     if cfg == 3:
         ref_cache = O.cache_write(case.empty_cache(), case.latent_bits, case.rope_bits,
                                   case.slot_mapping, case.page_size, case.kv_dtype, case.kv_scale)
-        assert np.array_equal(g.cache_numpy(), ref_cache)        # bit-exact FP8 write at full size
-    ro, rl = oracle_decode(case, g.cache_numpy(), rows=rows)
-    compare(case, out, lse, ro, rl, rows=rows)
+        assert np.array_equal(cache, ref_cache)        # bit-exact FP8 write at full size
+    ro, rl = oracle_decode(case, cache)
+    compare(case, out, lse, ro, rl)

@@ -25,11 +25,17 @@ def _cuda():
     api.lib()
 
 
-def call_noalloc(g):
-    """One call through the C ABI entry point itself."""
-    c = g.case
+def outputs(c):
     out = torch.full((c.B, c.s_q, c.H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((c.B, c.s_q, c.H), float("nan"), dtype=torch.float32, device="cuda")
+    return out, lse
+
+
+def call_noalloc(g, out=None, lse=None):
+    """One call through the C ABI entry point itself (into out, lse when given)."""
+    c = g.case
+    if out is None:
+        out, lse = outputs(c)
     st = api.lib().mla_decode_noalloc(
         ctypes.byref(g.params), ctypes.c_void_p(g.q.data_ptr()), ctypes.c_void_p(g.cache.data_ptr()),
         ctypes.c_void_p(g.block_table.data_ptr()), ctypes.c_void_p(g.seq_lens.data_ptr()),
@@ -68,6 +74,31 @@ def test_noalloc_matches_mla_decode_on_two_calls_in_a_row():
     o, l = call_noalloc(gs[0])
     torch.cuda.synchronize()
     close(o, l, refs[0][0], refs[0][1])
+    assert api.decode_noalloc_check() == (0, 0)          # no device-side error
+
+
+def test_a_warm_call_allocates_no_device_memory():
+    g = GpuCase(synth.make_case(B=4, s_q=1, H=16, page_size=64, seq_lens=(100, 3000), seed=73))
+    out, lse = outputs(g.case)
+    call_noalloc(g, out, lse)                             # first call on the device: set-up
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    call_noalloc(g, out, lse)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == alloc0
+    assert api.decode_noalloc_check() == (0, 0)
+
+
+def test_noalloc_reports_a_block_table_entry_outside_the_pool():
+    g = GpuCase(synth.make_case(B=2, s_q=1, H=16, page_size=64, seq_lens=[100, 200], seed=74))
+    g.block_table[1, 2] = g.case.num_pages + 5
+    call_noalloc(g)
+    st, bits = api.decode_noalloc_check()
+    assert st == -6 and bits & 0x1
+    g.block_table[1, 2] = int(g.case.block_table[1, 2])   # a valid table: the word is clean again
+    call_noalloc(g)
+    assert api.decode_noalloc_check() == (0, 0)
 
 
 def test_noalloc_refuses_work_beyond_its_scratch():
