@@ -384,6 +384,27 @@ def run_ours(args, rank, local_rank, world):
     if kern_n != args.steps:
         raise RuntimeError(f"timed {kern_n} decode kernels, expected {args.steps}")
     kern_ms = kern_ms_total / kern_n
+    # ---- the same step through the fused entry point (the scheduler kernel writes the new
+    # rows): one launch fewer per step
+    def fused_step():
+        api.decode_with_cache_write(lat_d, rope_d, slots_d, g.q, g.cache, g.block_table, g.seq_lens,
+                                    case.softmax_scale, g.kv_scale, max_seq_len=case.max_seq_len,
+                                    causal=case.causal, out=out, lse=lse, workspace=g.workspace)
+
+    for _ in range(args.warmup):
+        fused_step()
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for k in range(args.steps):
+        if flush_buf is not None:
+            flush_buf.fill_(k & 0xFF)
+        fev[k][0].record(stream)
+        fused_step()
+        fev[k][1].record(stream)
+    torch.cuda.synchronize()
+    st, bits = api.decode_check(g.workspace)
+    if st != 0:
+        raise RuntimeError(f"device error word after the fused steps: status {st} bits {bits:#x}")
+    fused_ms = sum(a.elapsed_time(b) for a, b in fev) / args.steps
     step_ms = sum(a.elapsed_time(b) for a, b in ev)
     dec_ms = sum(a.elapsed_time(b) for a, b in dec) / args.steps
     step_ms_max = max_over_ranks(step_ms, world, device)
@@ -466,6 +487,9 @@ def run_ours(args, rank, local_rank, world):
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 5)},
         "roofline": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in roof.items()},
         "gpu_launches": 4 * args.steps,      # cache write, scheduler, decode, combine per step
+        "fused_step": {"ms_per_step": round(fused_ms, 5), "launches_per_step": 3,
+                       "two_call_ms_per_step": round(ms_per_step, 5), "two_call_launches_per_step": 4,
+                       "how": "mla_decode_with_cache_write: extra CTAs of the scheduler's launch write the step's new rows"},
         "clocks": clk,
     }
     if world == 1 and not args.no_per_config:

@@ -80,8 +80,8 @@ typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
 
 typedef struct mla_decode_params {
   int32_t batch;               /* B >= 1 */
-  int32_t s_q;                 /* new query tokens per sequence, 1..64 */
-  int32_t num_heads;           /* H >= 1; s_q * H <= 4096 */
+  int32_t s_q;                 /* new query tokens per sequence, 1..512 */
+  int32_t num_heads;           /* H >= 1; s_q * H <= 65536 */
   int32_t page_size;           /* P: a multiple of 64, at most 1024 */
   int32_t num_pages;           /* Np: pages in the pool */
   int32_t max_blocks_per_seq;  /* MB: row stride of block_table */
@@ -114,6 +114,24 @@ mla_status mla_decode(const mla_decode_params* p, const void* q, const void* kv_
                       const int32_t* block_table, const int32_t* seq_lens,
                       float softmax_scale, const float* kv_scale, void* out, float* lse,
                       void* workspace, size_t workspace_bytes, mla_stream_t stream);
+
+/* mla_cache_write of a decode step's new tokens followed by mla_decode, in one launch
+ * chain ("[Attention] Blackwell FP8 MLA support with CUTLASS_MLA backend", Purpose: the
+ * FP8 cache the decode reads; the step appends each sequence's s_q new latent rows and
+ * attends over them). Arguments as mla_cache_write (latent, rope, slot_mapping,
+ * num_tokens; the cache geometry and kv_dtype come from `p`) and as mla_decode. The new
+ * rows are written by extra CTAs of the split scheduler's launch while its first CTA
+ * computes the schedule, one launch fewer than the two calls (beyond 2^17 tokens the
+ * cache-write kernel runs ahead of the scheduler instead); the decode reads the cache
+ * only after that launch has completed. seq_lens counts the new tokens, whose slots lie
+ * in the sequences' pages. A slot outside the pool is skipped and reported as
+ * MLA_DEVERR_SLOT through mla_decode_check. */
+mla_status mla_decode_with_cache_write(const mla_decode_params* p, const void* latent, const void* rope,
+                                       const int64_t* slot_mapping, int32_t num_tokens, const void* q,
+                                       void* kv_cache, const int32_t* block_table,
+                                       const int32_t* seq_lens, float softmax_scale,
+                                       const float* kv_scale, void* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, mla_stream_t stream);
 
 /* Synchronises `stream`, then reads the device error word left in `workspace` by the
  * last mla_decode on it: MLA_OK, MLA_ERR_DEVICE_INDEX, MLA_ERR_TIMEOUT, or
@@ -180,6 +198,15 @@ mla_status mla_decode_noalloc_check(mla_stream_t stream, uint32_t* bits);
  * MLA_ERR_CUDA when an event cannot be created, recorded or read. */
 mla_status mla_profile_begin(int32_t max_launches);
 mla_status mla_profile_end(double* total_ms, int32_t* launches);
+
+/* Test support (not for production use; not thread safe). Every pipeline wait inside the
+ * decode kernels is bounded: after `wait_limit_ns` (0 restores the default, 2 s) it gives
+ * up, sets MLA_DEVERR_TIMEOUT in the device error word, and the kernel drains its copies
+ * and MMAs and exits, leaving the CUDA context usable. With stall = 1 the first softmax
+ * wait of every CTA waits on a barrier nothing arrives on, so that the bound is reached
+ * without any fault; stall = 0 restores normal operation. Applies to the decode calls
+ * launched after it. Errors: MLA_ERR_INVALID_ARG for a stall value other than 0 or 1. */
+mla_status mla_test_set_hooks(uint64_t wait_limit_ns, int32_t stall);
 
 /* Static text for a status code. */
 const char* mla_status_string(int32_t status);

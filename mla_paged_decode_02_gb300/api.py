@@ -22,7 +22,7 @@ STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED",
           -6: "MLA_ERR_DEVICE_INDEX"}
 EXPORTS = ("mla_abi_version", "mla_status_string", "mla_decode_workspace_size", "mla_decode",
            "mla_decode_check", "mla_cache_write", "mla_decode_noalloc", "mla_decode_noalloc_check",
-           "mla_profile_begin", "mla_profile_end")
+           "mla_profile_begin", "mla_profile_end", "mla_test_set_hooks", "mla_decode_with_cache_write")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla.so")
@@ -68,6 +68,11 @@ def lib() -> ctypes.CDLL:
         L.mla_decode_noalloc_check.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         L.mla_cache_write.restype = i32
         L.mla_cache_write.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, vp, vp, vp]
+        L.mla_decode_with_cache_write.restype = i32
+        L.mla_decode_with_cache_write.argtypes = [ctypes.POINTER(DecodeParams), vp, vp, vp, i32, vp, vp, vp, vp,
+                                                  ctypes.c_float, vp, vp, vp, vp, sz, vp]
+        L.mla_test_set_hooks.restype = i32
+        L.mla_test_set_hooks.argtypes = [ctypes.c_uint64, i32]
         L.mla_profile_begin.restype = i32
         L.mla_profile_begin.argtypes = [i32]
         L.mla_profile_end.restype = i32
@@ -162,6 +167,35 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
     return out, lse
 
 
+def decode_with_cache_write(latent: torch.Tensor, rope: torch.Tensor, slot_mapping: torch.Tensor,
+                            q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                            seq_lens: torch.Tensor, softmax_scale: float,
+                            kv_scale: torch.Tensor | None = None, *, max_seq_len: int,
+                            causal: bool = True, out: torch.Tensor | None = None,
+                            lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                            stream=None):
+    """cache_write() of a step's new tokens followed by decode(), in one launch chain (the
+    scheduler kernel writes the new rows). Returns (out, lse)."""
+    n = latent.shape[0]
+    if latent.shape != (n, 512) or rope.shape != (n, 64) or latent.dtype != torch.bfloat16 \
+            or rope.dtype != torch.bfloat16 or not latent.is_contiguous() or not rope.is_contiguous():
+        raise ValueError("latent [N,512] and rope [N,64] must be contiguous bf16")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != n or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous int64 [N] tensor")
+    params, kvd, out, lse = _decode_inputs(q, kv_cache, block_table, seq_lens, kv_scale, max_seq_len,
+                                           causal, out, lse)
+    if workspace is None:
+        workspace = alloc_workspace(params, q.device)
+    st = lib().mla_decode_with_cache_write(ctypes.byref(params), _ptr(latent), _ptr(rope), _ptr(slot_mapping), n,
+                                           _ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
+                                           ctypes.c_float(softmax_scale),
+                                           _ptr(kv_scale) if kvd == KV_FP8_E4M3 else None, _ptr(out), _ptr(lse),
+                                           _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != MLA_OK:
+        raise MLAError(st, "mla_decode_with_cache_write")
+    return out, lse
+
+
 def decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
                    seq_lens: torch.Tensor, softmax_scale: float, kv_scale: torch.Tensor | None = None,
                    *, max_seq_len: int, causal: bool = True, out: torch.Tensor | None = None,
@@ -192,6 +226,14 @@ def decode_check(workspace: torch.Tensor, stream=None):
     bits = ctypes.c_uint32(0)
     st = lib().mla_decode_check(_ptr(workspace), _stream(stream), ctypes.byref(bits))
     return int(st), int(bits.value)
+
+
+def test_set_hooks(wait_limit_ns: int = 0, stall: bool = False) -> None:
+    """Tests only: bound of the kernels' pipeline waits (0 = the default 2 s) and the stall
+    that makes the first softmax wait run out."""
+    st = lib().mla_test_set_hooks(int(wait_limit_ns), int(bool(stall)))
+    if st != 0:
+        raise MLAError(st, "mla_test_set_hooks")
 
 
 def profile_begin(max_launches: int) -> None:

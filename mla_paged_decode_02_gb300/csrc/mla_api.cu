@@ -6,6 +6,7 @@
 #include <vector>
 #include <cudaTypedefs.h>
 #include "mla_internal.h"
+#include "mla_ptx.cuh"
 #include "../../include/mla.h"
 
 #define MLA_EXPORT extern "C" __attribute__((visibility("default")))
@@ -28,6 +29,10 @@ struct ProfileWindow {
 };
 ProfileWindow g_prof;
 constexpr int kMaxProfiledLaunches = 4096;
+
+// test hooks (mla_test_set_hooks): the wait bound passed to the kernels and the stall flag
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
+std::atomic<int32_t> g_test_stall{0};
 
 int variant_bit(int rc, bool fp8) {
   return (rc == 16 ? 0 : rc == 32 ? 2 : rc == 64 ? 4 : 6) + (fp8 ? 1 : 0);
@@ -74,7 +79,7 @@ mla_status check_params(const mla_decode_params* p) {
   if (p->causal != 0 && p->causal != 1) return MLA_ERR_INVALID_ARG;
   if (p->max_seq_len < p->s_q) return MLA_ERR_INVALID_ARG;
   if (p->page_size % 64 != 0 || p->page_size > 1024) return MLA_ERR_UNSUPPORTED;
-  if (p->s_q > 64 || (int64_t)p->s_q * p->num_heads > kMaxRows) return MLA_ERR_UNSUPPORTED;
+  if (p->s_q > kMaxSq || (int64_t)p->s_q * p->num_heads > kMaxRows) return MLA_ERR_UNSUPPORTED;
   if (p->batch > kMaxBatch || p->max_seq_len > kMaxSeqLen) return MLA_ERR_UNSUPPORTED;
   if ((int64_t)p->num_pages * p->page_size >= (int64_t)1 << 31) return MLA_ERR_UNSUPPORTED;
   if ((int64_t)p->max_blocks_per_seq * p->page_size < p->s_q) return MLA_ERR_INVALID_ARG;
@@ -144,10 +149,22 @@ MLA_EXPORT size_t mla_decode_workspace_size(const mla_decode_params* p, int32_t 
   return ws_layout(p->batch, plan, plan_workers(plan, num_sms)).total;
 }
 
-MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, const void* kv_cache,
-                                 const int32_t* block_table, const int32_t* seq_lens,
-                                 float softmax_scale, const float* kv_scale, void* out, float* lse,
-                                 void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+namespace mla {
+namespace {
+// The step's new tokens for the fused cache write (num == 0: none).
+struct FusedWrite {
+  const void* latent;
+  const void* rope;
+  const int64_t* slots;
+  int32_t num;
+};
+}  // namespace
+}  // namespace mla
+
+static mla_status decode_impl(const mla_decode_params* p, const void* q, const void* kv_cache,
+                              const int32_t* block_table, const int32_t* seq_lens, float softmax_scale,
+                              const float* kv_scale, void* out, float* lse, void* workspace,
+                              size_t workspace_bytes, mla_stream_t stream, const FusedWrite& fw) {
   mla_status st = check_params(p);
   if (st != MLA_OK) return st;
   const bool fp8 = p->kv_dtype == MLA_KV_FP8_E4M3;
@@ -206,6 +223,25 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   sa.max_units = w.max_units;
   sa.max_split = w.max_split;
   sa.max_slots = w.max_slots;
+  if (fw.num > 0) {
+    // the new tokens' rows go into the cache ahead of the decode: CTAs of the scheduler's
+    // launch write them next to the schedule computation (for very large writes, the
+    // cache-write kernel runs ahead of the scheduler instead)
+    const int64_t total_slots = (int64_t)p->num_pages * p->page_size;
+    if (fw.num <= kMaxFusedWriteTokens) {
+      sa.w_latent = static_cast<const uint4*>(fw.latent);
+      sa.w_rope = static_cast<const uint4*>(fw.rope);
+      sa.w_slots = fw.slots;
+      sa.w_cache = static_cast<uint8_t*>(const_cast<void*>(kv_cache));
+      sa.w_kv_scale = kv_scale;
+      sa.w_total_slots = total_slots;
+      sa.w_n = fw.num;
+      sa.w_fp8 = fp8 ? 1 : 0;
+    } else if (launch_cache_write(fw.latent, fw.rope, fw.slots, fw.num, const_cast<void*>(kv_cache), total_slots, fp8,
+                                  kv_scale, nullptr, s) != cudaSuccess) {
+      return MLA_ERR_CUDA;
+    }
+  }
   if (launch_schedule(sa, s) != cudaSuccess) return MLA_ERR_CUDA;
 
   DecodeArgs da;
@@ -241,6 +277,8 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   da.num_pages = p->num_pages;
   da.causal = p->causal;
   da.softmax_scale = softmax_scale;
+  da.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  da.test_stall = g_test_stall.load(std::memory_order_relaxed);
   const bool timed = g_prof.on && g_prof.next < g_prof.cap;
   if (timed && cudaEventRecord(g_prof.ev[2 * g_prof.next], s) != cudaSuccess) return MLA_ERR_CUDA;
   const cudaError_t le = plan.pair ? launch_decode_pair(da, fp8, grid, s) : launch_decode(da, rc, fp8, grid, s);
@@ -252,6 +290,10 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
 
   CombineArgs ca{};
   ca.hdr = hdr;
+  ca.err = hdr;
+  ca.w_slots = fw.num > 0 ? fw.slots : nullptr;
+  ca.w_n = fw.num;
+  ca.w_total_slots = (int64_t)p->num_pages * p->page_size;
   ca.split_list = split_list;
   ca.part_o = po;
   ca.part_lse = plse;
@@ -264,6 +306,36 @@ MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, cons
   // combine is a few dependent global loads per task: latency, not bandwidth)
   if (launch_combine(ca, 8 * nsm, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
+}
+
+MLA_EXPORT mla_status mla_test_set_hooks(uint64_t wait_limit_ns, int32_t stall) {
+  if (stall != 0 && stall != 1) return MLA_ERR_INVALID_ARG;
+  mla::g_wait_limit_ns.store(wait_limit_ns == 0 ? mla::kWaitLimitNs : wait_limit_ns);
+  mla::g_test_stall.store(stall);
+  return MLA_OK;
+}
+
+MLA_EXPORT mla_status mla_decode(const mla_decode_params* p, const void* q, const void* kv_cache,
+                                 const int32_t* block_table, const int32_t* seq_lens,
+                                 float softmax_scale, const float* kv_scale, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, mla_stream_t stream) {
+  return decode_impl(p, q, kv_cache, block_table, seq_lens, softmax_scale, kv_scale, out, lse, workspace,
+                     workspace_bytes, stream, FusedWrite{nullptr, nullptr, nullptr, 0});
+}
+
+MLA_EXPORT mla_status mla_decode_with_cache_write(const mla_decode_params* p, const void* latent,
+                                                  const void* rope, const int64_t* slot_mapping,
+                                                  int32_t num_tokens, const void* q, void* kv_cache,
+                                                  const int32_t* block_table, const int32_t* seq_lens,
+                                                  float softmax_scale, const float* kv_scale, void* out,
+                                                  float* lse, void* workspace, size_t workspace_bytes,
+                                                  mla_stream_t stream) {
+  if (num_tokens < 0) return MLA_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!latent || !rope || !slot_mapping)) return MLA_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!aligned(latent, 16) || !aligned(rope, 16) || !aligned(slot_mapping, 8)))
+    return MLA_ERR_INVALID_ARG;
+  return decode_impl(p, q, kv_cache, block_table, seq_lens, softmax_scale, kv_scale, out, lse, workspace,
+                     workspace_bytes, stream, FusedWrite{latent, rope, slot_mapping, num_tokens});
 }
 
 MLA_EXPORT mla_status mla_profile_begin(int32_t max_launches) {

@@ -13,11 +13,16 @@
 // launches per sequence.
 #include "mla_internal.h"
 #include "mla_ptx.cuh"
+#include "../../include/mla.h"
 
 namespace mla {
 
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   const int lane = threadIdx.x & 31;
+  // a fused cache write skipped slots outside the pool: report them (the error word was
+  // cleared by the scheduler, which ran before this kernel)
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < a.w_n; i += (int64_t)gridDim.x * blockDim.x)
+    if (a.w_slots[i] >= a.w_total_slots) atomicOr(a.err, MLA_DEVERR_SLOT);
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t tasks = (int64_t)a.hdr[2] * a.RC;

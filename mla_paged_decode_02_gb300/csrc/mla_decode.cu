@@ -265,7 +265,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   __shared__ __align__(8) uint64_t bar_qfull, bar_qready, bar_qempty;
   __shared__ __align__(8) uint64_t bar_kstage[NKS], bar_vstage[NVS], bar_vsempty[NVS];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_s_empty[2], bar_p_full[NP], bar_pv[NP];
-  __shared__ __align__(8) uint64_t bar_o_empty, bar_drain[2], bar_vaux;
+  __shared__ __align__(8) uint64_t bar_o_empty, bar_drain[2], bar_vaux, bar_never;
   __shared__ uint32_t tmem_base_s;
   __shared__ uint32_t abort_s;
   __shared__ __align__(16) float mref_s[RC];
@@ -302,6 +302,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const uint32_t b_p_full = smem_u32(bar_p_full), b_pv = smem_u32(bar_pv);
   const uint32_t b_oempty = smem_u32(&bar_o_empty), b_drain = smem_u32(bar_drain);
   const uint32_t b_vaux = smem_u32(&bar_vaux);
+  const uint32_t b_never = smem_u32(&bar_never);   // tests: a barrier nothing arrives on
   volatile uint32_t* abort_flag = &abort_s;
   uint32_t* err = a.err;
 
@@ -334,6 +335,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     mbar_init(b_drain, 1);
     mbar_init(b_drain + 8, 1);
     mbar_init(b_vaux, 1);
+    mbar_init(b_never, 1);
     abort_s = 0u;
     fence_mbarrier_init();
     tma_prefetch_desc(&a.tm_q);
@@ -354,7 +356,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const int R = a.R;
 
   auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
-    return mbar_wait(bar, parity, abort_flag, err, MLA_DEVERR_TIMEOUT);
+    return mbar_wait(bar, parity, abort_flag, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
   };
   // A wait whose outcome the whole warp agrees on (any lane giving up -> all give up),
   // so warp-collective instructions after it never see a diverged warp.
@@ -392,7 +394,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       // the last loads issued have landed before the CTA may exit
       volatile uint32_t no_abort = 0;
       for (uint32_t q = p > (uint32_t)NK ? p - NK : 0; q < p; ++q)
-        mbar_wait(b_kfull + 8 * (q % NK), (q / NK) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
+        mbar_wait(b_kfull + 8 * (q % NK), (q / NK) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
     }
   } else if (!FP8 && warp == 2) {
     // ============================================================ value producer (bf16)
@@ -440,7 +442,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     if (lane == 0) {
       volatile uint32_t no_abort = 0;
       for (uint32_t q = p > (uint32_t)NV ? p - NV : 0; q < p; ++q)
-        mbar_wait(b_vfull + 8 * (q % NV), (q / NV) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
+        mbar_wait(b_vfull + 8 * (q % NV), (q / NV) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
     }
   } else if (warp == 1) {
     // ============================================================ QK^T issuer
@@ -504,7 +506,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       // drain: every MMA issued has completed before tensor memory is released
       umma_commit(b_drain);
       volatile uint32_t no_abort = 0;
-      mbar_wait(b_drain, 0, &no_abort, err, MLA_DEVERR_TIMEOUT);
+      mbar_wait(b_drain, 0, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
     }
   } else if (warp == C::kPvWarp) {
     // ============================================================ PV issuer
@@ -550,7 +552,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       }
       umma_commit(b_drain + 8);
       volatile uint32_t no_abort = 0;
-      mbar_wait(b_drain + 8, 0, &no_abort, err, MLA_DEVERR_TIMEOUT);
+      mbar_wait(b_drain + 8, 0, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
     }
   } else if (warp >= 4 && warp < 8) {
     // ============================================================ softmax / epilogue
@@ -579,6 +581,10 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       named_bar_sync(kSoftmaxBar, 128);
       for (int k = 0; k < T && ok; ++k) {
         const uint32_t n = gn + k, sb = n & 1, pb = n % NP;
+        if (a.test_stall && n == 0) {
+          ok = wait_softmax(b_never, 0);            // tests: this wait runs out
+          if (!ok) break;
+        }
         ok = wait_softmax(b_s_full + 8 * sb, (n >> 1) & 1);
         if (!ok) break;
         tc_fence_after();
@@ -895,7 +901,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     if (gi == 0) {
       volatile uint32_t no_abort = 0;
       for (uint32_t q = kcp; q < kip; ++q)
-        mbar_wait(b_kstage + 8 * (q % NKS), (q / NKS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
+        mbar_wait(b_kstage + 8 * (q % NKS), (q / NKS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
     }
   } else if (FP8 && warp == 2) {
     // ============================================================ FP8 raw value producer
@@ -926,7 +932,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       }
       volatile uint32_t no_abort = 0;
       for (uint32_t q = p > (uint32_t)NVS ? p - NVS : 0; q < p; ++q)
-        mbar_wait(b_vstage + 8 * (q % NVS), (q / NVS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
+        mbar_wait(b_vstage + 8 * (q % NVS), (q / NVS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
     }
   }
 

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
   __shared__ __align__(8) uint64_t bar_qfull, bar_qempty;
   __shared__ __align__(8) uint64_t bar_sfull[2], bar_sempty[2], bar_pfull, bar_pin, bar_pvdone, bar_oempty;
   __shared__ __align__(8) uint64_t bar_x[2][2];
-  __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ __align__(8) uint64_t bar_drain, bar_never;
   __shared__ uint32_t tmem_base_s, abort_s;
   __shared__ __align__(16) float xbuf[2][2][68];     // [warpgroup][parity]: word 0 flag, words 4..67 values
   __shared__ __align__(16) float mref_s[2][64];
@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
   const uint32_t b_pfull = smem_u32(&bar_pfull), b_pin = smem_u32(&bar_pin), b_pvdone = smem_u32(&bar_pvdone);
   const uint32_t b_oempty = smem_u32(&bar_oempty), b_drain = smem_u32(&bar_drain);
   const uint32_t b_x = smem_u32(bar_x);
+  const uint32_t b_never = smem_u32(&bar_never);   // tests: a barrier nothing arrives on
   volatile uint32_t* abort_flag = &abort_s;
   uint32_t* err = a.err;
 
@@ -181,6 +182,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
     mbar_init(b_oempty, 2);               // the even CTA's two warpgroups, as b_sempty
     for (int i = 0; i < 4; ++i) mbar_init(b_x + 8 * i, 1);   // own arrival + the peer's bytes
     mbar_init(b_drain, 1);
+    mbar_init(b_never, 1);
     abort_s = 0u;
     fence_mbarrier_init();
     tma_prefetch_desc(&a.tm_q);
@@ -206,7 +208,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
   // A failed wait also raises the peer's abort flag, so that its waits end too.
   auto fail_peer = [&]() { st_cluster_u32(map_to_rank(smem_u32(&abort_s), peer), 1u); };
   auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
-    const bool ok = mbar_wait(bar, parity, abort_flag, err, MLA_DEVERR_TIMEOUT);
+    const bool ok = mbar_wait(bar, parity, abort_flag, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
     if (!ok) fail_peer();
     return ok;
   };
@@ -310,13 +312,21 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       }
     }
     if (ok && ptile >= 0) ok = load_values(pu, ptile, prb);
+    // after an abort the odd CTA cannot observe its own loads (they count on the even CTA's
+    // barrier, whose phase may never complete): both producers wait 50 us, far longer than
+    // a load takes, before leaving
+    if (*abort_flag) {
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 50000ull) {
+      }
+    }
     // the even CTA waits until the last loads of both CTAs have landed (normally the MMA
     // issuer already has); a CTA must not leave with copies into its memory in flight
     if (leader && lane == 0) {
       volatile uint32_t no_abort = 0;
       for (uint32_t q = r > (uint32_t)kRing ? r - kRing : 0; q < r; ++q)
-        mbar_wait(b_full + 8 * (q % kRing), (q / kRing) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
-      if (uq > 0) mbar_wait(b_qfull, (uq - 1) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT);
+        mbar_wait(b_full + 8 * (q % kRing), (q / kRing) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
+      if (uq > 0) mbar_wait(b_qfull, (uq - 1) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
     }
   } else if (warp == 1 && leader) {
     // ================================================================ MMA issuer (even CTA)
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       // every MMA issued has completed before tensor memory is released
       umma_pair_commit(b_drain);
       volatile uint32_t no_abort = 0;
-      mbar_wait(b_drain, 0, &no_abort, err, MLA_DEVERR_TIMEOUT);
+      mbar_wait(b_drain, 0, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
     }
   } else if (warp >= 4) {
     // ================================================================ softmax / epilogue
@@ -421,7 +431,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
         const uint4 v = t == 0 ? make_uint4(flag, 0, 0, 0) : *reinterpret_cast<const uint4*>(vals + 4 * (t - 1));
         st_async_v4(dst, v, map_to_rank(xb, peer));
       }
-      const bool w = mbar_wait_cluster(xb, (xc >> 1) & 1, abort_flag, err, MLA_DEVERR_TIMEOUT);
+      const bool w = mbar_wait_cluster(xb, (xc >> 1) & 1, abort_flag, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
       ++xc;
       if (named_bar_or(bar, 128, !w)) {
         if (t == 0) fail_peer();
@@ -460,6 +470,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       for (int k = 0; k < T && ok; ++k) {
         const uint32_t n = gn + k;
         const int tile = U.tb + k;
+        if (a.test_stall && n == 0) {
+          ok = wait_wg(b_never, 0);                  // tests: this wait runs out
+          if (!ok) break;
+        }
         ok = wait_wg(b_sfull + 8 * (n & 1), (n >> 1) & 1);
         if (!ok) break;
         tc_fence_after();
@@ -587,7 +601,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
             mbar_arrive_expect_tx(b_pfull, kStageBytes);   // own rows; the odd CTA's copy to come
           } else {
             mbar_arrive_expect_tx(b_pin, kStageBytes);
-            ok = mbar_wait(b_pin, n & 1, abort_flag, err, MLA_DEVERR_TIMEOUT);   // the even CTA's copy
+            ok = mbar_wait(b_pin, n & 1, abort_flag, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);   // the even CTA's copy
             if (ok) mbar_arrive_cluster(lead(b_pfull));
             else fail_peer();
           }

@@ -13,8 +13,11 @@ constexpr int kDQK = 576;          // 512 latent + 64 rope
 constexpr int kDV = 512;
 constexpr int kTileTokens = 128;   // keys per tile: the M of the QK^T MMA (tokens on M)
 constexpr int kMaxSeqLen = 1 << 20;
-constexpr int kMaxRows = 4096;     // s_q * H
+constexpr int kMaxRows = 65536;    // s_q * H
+constexpr int kMaxSq = 512;        // new query tokens per sequence (the decode threshold the
+                                   // "[WIP][Attention] FlashAttn MLA" page tunes up to)
 constexpr int kMaxBatch = 1 << 16;
+constexpr int kMaxFusedWriteTokens = 1 << 17;   // new tokens the scheduler's launch writes itself
 
 // Execution plan for the s_q * H query rows of a sequence. Rows are processed in groups
 // of RC rows (the N of every MMA). Up to 64 rows: one CTA per SM, RC = 16/32/64, 128-key
@@ -77,6 +80,14 @@ struct SchedArgs {
   int4* units;           // (b, g, tile_begin | tile_end << 16, partial slot or -1)
   int32_t B, s_q, G, max_len, grid;
   int32_t tile;          // keys per tile (128, or 256 for CTA pairs)
+  // fused cache write of the step's new tokens (w_n > 0): done before the schedule
+  const uint4* w_latent;
+  const uint4* w_rope;
+  const int64_t* w_slots;
+  uint8_t* w_cache;
+  const float* w_kv_scale;
+  int64_t w_total_slots;
+  int32_t w_n, w_fp8;
   int64_t max_units, max_split, max_slots;
 };
 
@@ -100,10 +111,16 @@ struct DecodeArgs {
   const float* kv_scale;
   int32_t s_q, H, R, P, MB, num_pages, causal;
   float softmax_scale;
+  uint64_t wait_limit_ns;  // bound of every pipeline wait (2 s; tests may shorten it)
+  int32_t test_stall;      // tests only: 1 = the first softmax wait never completes
 };
 
 struct CombineArgs {
   const uint32_t* hdr;
+  uint32_t* err;           // the device error word (hdr[0])
+  const int64_t* w_slots;  // fused cache write: its slots are checked here (w_n > 0)
+  int64_t w_total_slots;
+  int32_t w_n;
   const int4* split_list;
   const float* part_o;
   const float* part_lse;

@@ -59,22 +59,23 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Wait for the phase of `bar` with the given parity to complete. The waiting thread
 // sleeps in the barrier (woken when the phase completes) rather than spinning, so that
-// waiting warps take no issue slots from working ones. Bounded: after `kWaitLimitNs` of
-// wall time the wait gives up, ORs `timeout_bit` into the global error word, raises the
-// CTA-wide abort flag and returns false. A raised abort flag also ends every other wait
-// (within one sleep period), so a stalled pipeline never hangs the GPU.
+// waiting warps take no issue slots from working ones. Bounded: after `limit_ns` of wall
+// time (2 s unless a test shortens it) the wait gives up, ORs `timeout_bit` into the global
+// error word, raises the CTA-wide abort flag and returns false. A raised abort flag also
+// ends every other wait (within one sleep period), so a stalled pipeline never hangs the GPU.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr uint32_t kSleepHintNs = 200000u;         // longest single sleep: 0.2 ms
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile uint32_t* abort_flag,
-                                          uint32_t* err_word, uint32_t timeout_bit) {
+                                          uint32_t* err_word, uint32_t timeout_bit,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1u;
       atomicOr(err_word, timeout_bit);
       return false;
@@ -316,13 +317,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                                  uint32_t* err_word, uint32_t timeout_bit) {
+                                                  uint32_t* err_word, uint32_t timeout_bit,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait_cluster(bar, parity, 0)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait_cluster(bar, parity, kSleepHintNs)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1u;
       atomicOr(err_word, timeout_bit);
       return false;

@@ -21,6 +21,7 @@
 // its log-sum-exp) to its own slot, and the combine kernel merges the pieces. Streams
 // inside one CTA write the final output directly. Units are stored in position order,
 // so the units of CTA c are the contiguous range [cta_first[c], cta_first[c + 1]).
+#include "mla_cache_write.cuh"
 #include "mla_internal.h"
 #include "mla_ptx.cuh"
 #include "../../include/mla.h"
@@ -28,6 +29,7 @@
 namespace mla {
 
 constexpr int kSchedThreads = 1024;
+constexpr int kMaxWriteCtas = 128;
 
 // Exclusive prefix sum over the block's threads (warp shuffles, then the 32 warp totals).
 __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* tmp, int64_t* total) {
@@ -68,6 +70,22 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   __shared__ int64_t scan_tmp[32];
   const int tid = threadIdx.x;
   griddep_launch_dependents();         // the decode grid may start its set-up now
+  if (blockIdx.x > 0) {
+    // fused call: CTAs 1.. write the step's new tokens into the cache while CTA 0 computes
+    // the schedule (the decode grid reads the cache only after this grid has completed).
+    // Slots outside the pool are skipped here and reported by the combine kernel, which
+    // runs after CTA 0 has cleared the error word.
+    const int64_t total = (int64_t)a.w_n * kWriteGroupsPerToken;
+    const int64_t stride = (int64_t)(gridDim.x - 1) * kSchedThreads;
+    const float scale = a.w_fp8 ? __ldg(a.w_kv_scale) : 1.0f;
+    for (int64_t i = (int64_t)(blockIdx.x - 1) * kSchedThreads + tid; i < total; i += stride) {
+      const int64_t t = i / kWriteGroupsPerToken;
+      const int c = (int)(i - t * kWriteGroupsPerToken);
+      if (a.w_fp8) write_group<true>(a.w_latent, a.w_rope, a.w_slots, t, c, a.w_cache, a.w_total_slots, scale, nullptr);
+      else write_group<false>(a.w_latent, a.w_rope, a.w_slots, t, c, a.w_cache, a.w_total_slots, scale, nullptr);
+    }
+    return;
+  }
   if (tid == 0) a.hdr[0] = 0u;
   __syncthreads();
 
@@ -163,7 +181,14 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
 }
 
 cudaError_t launch_schedule(const SchedArgs& a, cudaStream_t s) {
-  schedule_kernel<<<1, kSchedThreads, 0, s>>>(a);
+  // CTA 0 schedules; a fused cache write adds CTAs of 1024 threads, one 8-value group each
+  int extra = 0;
+  if (a.w_n > 0) {
+    const int64_t groups = (int64_t)a.w_n * kWriteGroupsPerToken;
+    extra = (int)((groups + kSchedThreads - 1) / kSchedThreads);
+    if (extra > kMaxWriteCtas) extra = kMaxWriteCtas;
+  }
+  schedule_kernel<<<1 + extra, kSchedThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

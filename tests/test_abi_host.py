@@ -70,8 +70,15 @@ def test_decode_rejects_null_and_misaligned_pointers_without_a_gpu(lib):
     assert lib.mla_decode(ctypes.byref(p), *a) == -1
     fp8 = api.make_params(2, 1, 16, 64, 10, 5, 300, api.KV_FP8_E4M3)
     assert lib.mla_decode(ctypes.byref(fp8), *args) == -1          # FP8 without kv_scale
-    unsup = api.make_params(2, 65, 16, 64, 10, 50, 3000, api.KV_BF16)
+    unsup = api.make_params(2, 513, 16, 64, 10, 50, 3000, api.KV_BF16)     # s_q above 512
     assert lib.mla_decode(ctypes.byref(unsup), *args) == -2
+    unsup = api.make_params(2, 512, 129, 64, 10, 50, 3000, api.KV_BF16)    # s_q * H above 65536
+    assert lib.mla_decode(ctypes.byref(unsup), *args) == -2
+
+
+def test_test_hooks_reject_a_bad_stall_value(lib):
+    assert lib.mla_test_set_hooks(0, 2) == -1
+    assert lib.mla_test_set_hooks(0, 0) == 0
 
 
 def test_profile_window_arguments_without_a_gpu(lib):

@@ -100,6 +100,13 @@ SMALL = [
     (2, 1, 64, 64, [900, 2100], BF, True),           # H = 64 (TP = 2)
     (2, 1, 16, 256, [300, 1100], BF, True),          # page size 256
     (2, 1, 128, 256, [300, 1100], BF, True),
+    # multi-token decode (causal within the new tokens) up to the 512-token decode threshold
+    (2, 8, 16, 64, [200, 700], BF, True),            # 128 rows
+    (2, 64, 16, 64, [64, 900], BF, True),            # 1024 rows, s_q = seq_len for one sequence
+    (1, 512, 16, 64, [1000], BF, True),              # 8192 rows, 64 row groups
+    (2, 16, 128, 64, [300, 2000], BF, True),         # 2048 rows
+    (2, 8, 16, 64, [200, 700], F8, True),            # FP8, two 64-row groups
+    (2, 32, 64, 128, [40, 600], F8, True),           # FP8, 2048 rows
 ]
 
 
@@ -206,6 +213,27 @@ def test_fp8_query_beyond_the_float16_range_is_reported():
     st, bits = api.decode_check(g.workspace)
     assert st == -6 and bits & 0x4
     g.q = q0
+    out, lse = g.decode()
+    assert api.decode_check(g.workspace) == (0, 0)
+    ro, rl = oracle_decode(case, g.cache_numpy())
+    compare(case, out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("H,kv", [(16, BF), (16, F8), (128, BF), (128, F8)])
+def test_a_stalled_pipeline_times_out_and_the_next_call_is_clean(H, kv):
+    """Failure detection: with the wait bound shortened to 20 ms and the first softmax wait
+    of every CTA made to wait on a barrier nothing arrives on, the call reports
+    MLA_ERR_TIMEOUT (no fault, no hang); the kernel drained its copies and MMAs, so the
+    next normal call on the same stream gives the oracle's result."""
+    case = synth.make_case(B=3, s_q=1, H=H, page_size=64, seq_lens=[300, 2000, 70], seed=48, kv_dtype=kv)
+    g = GpuCase(case)
+    try:
+        api.test_set_hooks(wait_limit_ns=20_000_000, stall=True)
+        g.decode()
+        st, bits = api.decode_check(g.workspace)
+    finally:
+        api.test_set_hooks(0, False)
+    assert st == -5 and bits & 0x8
     out, lse = g.decode()
     assert api.decode_check(g.workspace) == (0, 0)
     ro, rl = oracle_decode(case, g.cache_numpy())
