@@ -106,6 +106,20 @@ bool encode_kv_map(CUtensorMap* m, const void* cache, int64_t rows, uint32_t chu
   return r == CUDA_SUCCESS;
 }
 
+// q as [B][R/8 groups][9 chunks][8 rows][64 elements]: a box of 8 groups x 9 chunks is 64
+// whole 1152-byte rows (one contiguous piece each, the cheapest for TMA), landing as
+// [group][chunk][8 rows][64] with 128-byte swizzle. Needs R % 8 == 0.
+bool encode_q_rows_map(CUtensorMap* m, const void* q, int B, int R) {
+  cuuint64_t dims[5] = {64, 8, 9, (cuuint64_t)(R / 8), (cuuint64_t)B};
+  cuuint64_t strides[4] = {(cuuint64_t)kDQK * 2, 128, (cuuint64_t)kDQK * 2 * 8, (cuuint64_t)kDQK * 2 * R};
+  cuuint32_t box[5] = {64, 8, 9, 8, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(q), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool encode_q_map(CUtensorMap* m, const void* q, int B, int R, int rc) {
   cuuint64_t dims[3] = {(cuuint64_t)kDQK, (cuuint64_t)R, (cuuint64_t)B};
   cuuint64_t strides[2] = {(cuuint64_t)kDQK * 2, (cuuint64_t)kDQK * 2 * R};
@@ -246,13 +260,15 @@ static mla_status decode_impl(const mla_decode_params* p, const void* q, const v
 
   DecodeArgs da;
   std::memset(&da, 0, sizeof(da));
-  // a CTA of a pair holds 64 of its unit's 128 rows and loads keys one chunk at a time
-  if (!encode_q_map(&da.tm_q, q, B, R, plan.pair ? 64 : rc)) return MLA_ERR_INVALID_ARG;
+  // a CTA of a pair holds 64 of its unit's 128 rows (as whole rows when R % 8 == 0)
+  da.q_whole_rows = plan.pair && R % 8 == 0 ? 1 : 0;
+  if (da.q_whole_rows ? !encode_q_rows_map(&da.tm_q, q, B, R) : !encode_q_map(&da.tm_q, q, B, R, plan.pair ? 64 : rc))
+    return MLA_ERR_INVALID_ARG;
   {
     const int64_t rows = (int64_t)p->num_pages * p->page_size;
     // chunks per key / value box: a pair loads 2 / 4 adjacent chunks of each row
     const uint32_t kc = plan.pair ? 2u : (uint32_t)decode_key_chunks_per_slot(rc, fp8);
-    const uint32_t vc = plan.pair ? 4u : 2u;
+    const uint32_t vc = plan.pair ? 4u : (uint32_t)decode_value_chunks_per_box(rc, fp8);
     if (!encode_kv_map(&da.tm_k, kv_cache, rows, kc, fp8, true) ||
         !encode_kv_map(&da.tm_v, kv_cache, rows, vc, fp8, false))
       return MLA_ERR_INVALID_ARG;

@@ -59,7 +59,6 @@ namespace mla {
 
 constexpr int kChunkBytes = 16384;   // one 64-column chunk of a tile: 128 rows x 128 B
 constexpr int kVSlotBytes = 32768;   // two chunks: 128 value columns
-constexpr int kVStageBytes = 16384;  // raw FP8 pair: 2 halves x [8 groups][2 chunks][8 rows][64 B]
 constexpr int kPairsPerTile = 4;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -79,7 +78,7 @@ struct Cfg {
   static constexpr int kQBytes = RC * 1152;            // 9 chunks x RC rows x 128 B
   static constexpr int kPRow = RC * 2;                  // bytes of one P^T row (one key)
   static constexpr int kPBytes = 128 * kPRow;
-  static constexpr int kNumP = RC == 64 && FP8 ? 1 : 2;  // P^T buffers
+  static constexpr int kNumP = FP8 && (RC == 64 || RC == 16) ? 1 : 2;  // P^T buffers
   static constexpr uint32_t kPSwz = RC == 64 ? kSwizzle128 : RC == 32 ? kSwizzle64 : kSwizzle32;
   static constexpr int kTmemCols = FP8 || RC == 64 ? 512 : RC == 32 ? 256 : 128;
   static constexpr int kThreads = FP8 ? 384 : 256;
@@ -99,10 +98,21 @@ struct Cfg {
   static constexpr int kKTmemBase = 6 * RC;
   static constexpr int kKTmemSlotCols = KC * 32;
   static constexpr int NK = FP8 ? (RC == 32 ? 3 : 4) : (RC < 64 ? 2 : 3);
-  static constexpr int NV = RC == 16 ? 3 : 2;
-  static constexpr int kKStageBytes = KC * 8192;        // raw FP8 key position: 2 halves x KC x 4 KB
-  static constexpr int NKS = FP8 ? (RC == 64 ? 3 : 2) : 0;   // raw staging depths
-  static constexpr int NVS = FP8 ? (RC == 64 ? 2 : 3) : 0;
+  // FP8 raw staging. TMA cost grows with the number of contiguous row pieces a box has
+  // (about 6 ns per piece per SM), so with 16 rows the raw keys are whole 576-byte rows (one
+  // stage = the tile's two 64-row halves, 72 KB, feeding all of its TMEM positions) and the
+  // raw values 4-chunk boxes (256-byte pieces, 32 KB, feeding two value pairs). 32 and 64
+  // rows keep 1-3 chunk key stages and 2-chunk value stages: their Q and P^T leave no room.
+  static constexpr bool kRawRows = FP8 && RC == 16;
+  static constexpr int NV = kRawRows ? 2 : RC == 16 ? 3 : 2;
+  static constexpr int kKRawChunks = kRawRows ? 9 : KC;     // chunks of a row per raw key box
+  static constexpr int kKStageBytes = kKRawChunks * 8192;   // 2 halves x 64 rows x chunks x 64 B
+  static constexpr int kKPosPerStage = kRawRows ? kSlotsPerTile : 1;   // TMEM key positions per stage
+  static constexpr int kVRawChunks = kRawRows ? 4 : 2;      // chunks of a row per raw value box
+  static constexpr int kVStage = kVRawChunks * 8192;        // 2 halves x 64 rows x chunks x 64 B
+  static constexpr int kPairsPerVStage = kVRawChunks / 2;
+  static constexpr int NKS = FP8 ? (kRawRows ? 1 : RC == 64 ? 3 : 2) : 0;   // raw staging depths
+  static constexpr int NVS = FP8 ? (kRawRows ? 2 : RC == 64 ? 2 : 3) : 0;
   static constexpr int kKLoaders = FP8 ? 4 : 1;         // arrivals that fill a K slot
   // FP8 values: 16-byte units a thread converts per unrolled round (code size against
   // latency hiding; measured: 8 for 16 rows, 4 for 32 and 64)
@@ -111,7 +121,7 @@ struct Cfg {
   static_assert(!FP8 || kKTmemBase + NK * kKTmemSlotCols <= 512, "tensor memory budget");
   static_assert(kSlotsPerTile * KC == 9, "a tile is 9 chunks");
   static constexpr int kDynBytes = 1024 + kQBytes + kNumP * kPBytes + (FP8 ? 0 : NK * kKSlotBytes) +
-                                   NV * kVSlotBytes + NKS * kKStageBytes + NVS * kVStageBytes;
+                                   NV * kVSlotBytes + NKS * kKStageBytes + NVS * kVStage;
   static_assert(kDynBytes + kStaticBudget <= kSmemLimit, "shared memory budget");
 };
 
@@ -220,8 +230,10 @@ __device__ __forceinline__ bool iter_next(TileIter& it, const DecodeArgs& a, int
 // conversion, chosen so that values and keys would not compete for the convert unit, was
 // measured 15% slower on the 16-row workload.) Rows at or past `valid` are written as
 // zeros.
-template <int G, int kRound>
-__device__ __forceinline__ void convert_value_pair(const uint8_t* src, uint8_t* dst, int valid, int gi) {
+// The raw stage holds VC chunks of every row: [2 halves][8 groups][VC chunks][8 rows][64 B];
+// the pair is chunks cb, cb + 1 of it.
+template <int G, int kRound, int VC>
+__device__ __forceinline__ void convert_value_pair(const uint8_t* src, uint8_t* dst, int valid, int gi, int cb) {
   constexpr int kPer = 1024 / G;                 // 16-byte units per thread
   static_assert(kPer % kRound == 0, "whole rounds");
 #pragma unroll 1
@@ -232,8 +244,8 @@ __device__ __forceinline__ void convert_value_pair(const uint8_t* src, uint8_t* 
       const int idx = gi + (r0 + jj) * G, row = (idx & 511) >> 2;   // chunk idx / 512, column idx % 4
       v[jj] = make_uint4(0, 0, 0, 0);
       if (row < valid)
-        v[jj] = *reinterpret_cast<const uint4*>(src + (row >> 6) * (kVStageBytes / 2) + ((row >> 3) & 7) * 1024 +
-                                                (idx >> 9) * 512 + (row & 7) * 64 + (idx & 3) * 16);
+        v[jj] = *reinterpret_cast<const uint4*>(src + (row >> 6) * (VC * 4096) + ((row >> 3) & 7) * (VC * 512) +
+                                                (cb + (idx >> 9)) * 512 + (row & 7) * 64 + (idx & 3) * 16);
     }
 #pragma unroll
     for (int jj = 0; jj < kRound; ++jj) {
@@ -285,7 +297,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const uint32_t sK = sP + NP * C::kPBytes;
   const uint32_t sV = sK + (FP8 ? 0 : NK * C::kKSlotBytes);
   const uint32_t sKS = sV + NV * kVSlotBytes;
-  const uint32_t sVS = sKS + (FP8 ? NKS * C::kKStageBytes : 0);
+  const uint32_t sVS = sKS + (FP8 ? NKS * C::kKStageBytes : 0);   // raw value stages, C::kVStage each
   uint8_t* gQ = gbase;
   uint8_t* gP = gbase + (sP - sQ);
   uint8_t* gV = gbase + (sV - sQ);
@@ -697,19 +709,24 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           // waits; the softmax barrier passes the outcome on.
           const int valid = U.L - (U.tb + k) * kTileTokens;
           for (int j = 0; j < kPairsPerTile && ok; ++j, ++vcp) {
-            const uint32_t st = vcp % NVS, vs = vcp % NV;
+            // raw stage vst holds kPairsPerVStage pairs: waited for at its first pair and
+            // released after its last
+            const uint32_t vst = vcp / C::kPairsPerVStage, st = vst % NVS, vs = vcp % NV;
+            const int pin = (int)(vcp % C::kPairsPerVStage);
+            const bool first = pin == 0, last = pin == C::kPairsPerVStage - 1;
             // the raw rows have landed and the fp16 slot is free (with three or more value
             // slots the producer waited for the slot before loading the rows)
-            const bool mine = t != 0 || (wait(b_vstage + 8 * st, (vcp / NVS) & 1) &&
+            const bool mine = t != 0 || ((!first || wait(b_vstage + 8 * st, (vst / NVS) & 1)) &&
                                          (NV >= 3 || wait(b_vempty + 8 * vs, ((vcp / NV) & 1) ^ 1)));
             ok = !named_bar_or(kSoftmaxBar, 128, !mine);
             if (!ok) break;
-            convert_value_pair<128, C::kValueRound>(gVS + st * kVStageBytes, gV + vs * kVSlotBytes, valid, t);
+            convert_value_pair<128, C::kValueRound, C::kVRawChunks>(gVS + st * C::kVStage, gV + vs * kVSlotBytes,
+                                                                    valid, t, 2 * pin);
             fence_proxy_async_smem();
             named_bar_sync(kSoftmaxBar, 128);
             if (t == 0) {
               mbar_arrive(b_vfull + 8 * vs);
-              mbar_arrive(b_vsempty + 8 * st);
+              if (last) mbar_arrive(b_vsempty + 8 * st);
             }
           }
         }
@@ -812,25 +829,28 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     TileIter kc, ki;                                    // consume / issue cursors
     bool kmore = iter_begin(kc, a, u0, u1, err, false);
     bool kimore = gi == 0 && iter_begin(ki, a, u0, u1, err, false);
+    // raw stages: kip issued, kfreed read by every thread (free again), kwaited landed
     int kic = 0;
-    uint32_t kip = 0, kcp = 0, uq = 0;
+    uint32_t kip = 0, kcp = 0, uq = 0, kfreed = 0, kwaited = 0;
     auto top_up = [&]() {
-      while (kimore && kip < kcp + NKS) {
+      while (kimore && kip < kfreed + NKS) {
         const uint32_t sl = kip % NKS, bar = b_kstage + 8 * sl, dst = sKS + sl * C::kKStageBytes;
         const uint32_t nbox = (ki.rb0 >= 0 ? 1u : 0u) + (ki.rb1 >= 0 ? 1u : 0u);
+        // a whole-row stage (all 9 chunks) or the KC chunks of one position
+        const int32_t c0 = C::kRawRows ? 0 : kic * C::KC;
         mbar_arrive_expect_tx(bar, nbox * (C::kKStageBytes / 2));
-        if (ki.rb0 >= 0) tma_load_4d(dst, &a.tm_k, bar, 0, 0, kic * C::KC, (int32_t)(ki.rb0 >> 3));
-        if (ki.rb1 >= 0)
-          tma_load_4d(dst + C::kKStageBytes / 2, &a.tm_k, bar, 0, 0, kic * C::KC, (int32_t)(ki.rb1 >> 3));
-        if (++kic == C::kSlotsPerTile) { kic = 0; kimore = iter_next(ki, a, u1, err, false); }
+        if (ki.rb0 >= 0) tma_load_4d(dst, &a.tm_k, bar, 0, 0, c0, (int32_t)(ki.rb0 >> 3));
+        if (ki.rb1 >= 0) tma_load_4d(dst + C::kKStageBytes / 2, &a.tm_k, bar, 0, 0, c0, (int32_t)(ki.rb1 >> 3));
+        if (C::kRawRows || ++kic == C::kSlotsPerTile) { kic = 0; kimore = iter_next(ki, a, u1, err, false); }
         ++kip;
       }
     };
     if (gi == 0) top_up();
-    // staging row gi of a key position: half gi/64, group (gi/8)%8, row gi%8; its four
-    // 16-byte units are 64-byte swizzled by row (TMA swizzle mode of the key map)
+    // staging row gi of a key stage: half gi/64, group (gi/8)%8, row gi%8; each 64-byte
+    // chunk row's four 16-byte units are 64-byte swizzled by row (the key map's swizzle)
     const int kr7 = gi & 7;
-    const uint32_t krow_off = (uint32_t)(gi >> 6) * (C::kKStageBytes / 2) + ((gi >> 3) & 7) * (C::KC * 512) + kr7 * 64;
+    const uint32_t krow_off =
+        (uint32_t)(gi >> 6) * (C::kKStageBytes / 2) + ((gi >> 3) & 7) * (C::kKRawChunks * 512) + kr7 * 64;
     bool ok = true;
     while (kmore && ok) {
       if (kc.tile == kc.U.tb) {
@@ -859,14 +879,20 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         ++uq;
       }
       for (int sl = 0; sl < C::kSlotsPerTile && ok; ++sl) {
-        const uint32_t st = kcp % NKS, ks = kcp % NK;
-        const bool mine =
-            gi != 0 || (wait(b_kstage + 8 * st, (kcp / NKS) & 1) && wait(b_kempty + 8 * ks, ((kcp / NK) & 1) ^ 1));
-        ok = !named_bar_or(kKeyDqBar, kKeyDqThreads, !mine);   // everyone is done with the last slot
+        // position kcp reads raw stage rs (waited for at the stage's first position)
+        const uint32_t rs = kcp / C::kKPosPerStage, st = rs % NKS, ks = kcp % NK;
+        const int pin = (int)(kcp % C::kKPosPerStage);
+        const bool mine = gi != 0 || ((pin != 0 || wait(b_kstage + 8 * st, (rs / NKS) & 1)) &&
+                                      wait(b_kempty + 8 * ks, ((kcp / NK) & 1) ^ 1));
+        ok = !named_bar_or(kKeyDqBar, kKeyDqThreads, !mine);   // everyone is done with the last position
         if (!ok) break;
-        if (gi == 0) top_up();
+        if (pin == 0) kwaited = rs + 1;
+        if (C::kKPosPerStage == 1) {
+          kfreed = kcp;                                  // the previous position's stage
+          if (gi == 0) top_up();
+        }
         tc_fence_after();
-        const uint8_t* src = gKS + st * C::kKStageBytes + krow_off;
+        const uint8_t* src = gKS + st * C::kKStageBytes + krow_off + pin * (C::KC * 512);
         const uint32_t tbase = lane_base + C::kKTmemBase + ks * C::kKTmemSlotCols;
         // one chunk per iteration: the five roles of a CTA share the SM's instruction
         // caches, and the fully unrolled position (KC chunks) lost more to instruction
@@ -895,12 +921,18 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         __syncwarp();
         if (lane == 0) mbar_arrive(b_kfull + 8 * ks);
         ++kcp;
+        if (C::kKPosPerStage > 1 && pin == C::kKPosPerStage - 1) {
+          // every thread has read the stage's last position: refill it
+          named_bar_sync(kKeyDqBar, kKeyDqThreads);
+          kfreed = rs + 1;
+          if (gi == 0) top_up();
+        }
       }
       if (ok) kmore = iter_next(kc, a, u1, err, false);
     }
     if (gi == 0) {
       volatile uint32_t no_abort = 0;
-      for (uint32_t q = kcp; q < kip; ++q)
+      for (uint32_t q = kwaited; q < kip; ++q)
         mbar_wait(b_kstage + 8 * (q % NKS), (q / NKS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
     }
   } else if (FP8 && warp == 2) {
@@ -918,15 +950,16 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       uint32_t p = 0;
       while (more && ok) {
         const uint32_t nbox = (it.rb0 >= 0 ? 1u : 0u) + (it.rb1 >= 0 ? 1u : 0u);
-        for (int j = 0; j < kPairsPerTile; ++j, ++p) {
+        for (int j = 0; j < kPairsPerTile; j += C::kPairsPerVStage, ++p) {
+          // stage p: value chunks 2j .. 2j + kVRawChunks - 1 of the tile's rows
           const uint32_t sl = p % NVS;
           ok = wait(b_vsempty + 8 * sl, ((p / NVS) & 1) ^ 1) &&
                (NV < 3 || wait(b_vempty + 8 * (p % NV), ((p / NV) & 1) ^ 1));
           if (!ok) break;
-          const uint32_t bar = b_vstage + 8 * sl, dst = sVS + sl * kVStageBytes;
-          mbar_arrive_expect_tx(bar, nbox * (kVStageBytes / 2));
+          const uint32_t bar = b_vstage + 8 * sl, dst = sVS + sl * C::kVStage;
+          mbar_arrive_expect_tx(bar, nbox * (C::kVStage / 2));
           if (it.rb0 >= 0) tma_load_4d(dst, &a.tm_v, bar, 0, 0, 2 * j, (int32_t)(it.rb0 >> 3));
-          if (it.rb1 >= 0) tma_load_4d(dst + kVStageBytes / 2, &a.tm_v, bar, 0, 0, 2 * j, (int32_t)(it.rb1 >> 3));
+          if (it.rb1 >= 0) tma_load_4d(dst + C::kVStage / 2, &a.tm_v, bar, 0, 0, 2 * j, (int32_t)(it.rb1 >> 3));
         }
         if (ok) more = iter_next(it, a, u1, err, false);
       }
@@ -972,14 +1005,23 @@ static cudaError_t launch_one(const DecodeArgs& a, int grid, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, decode_kernel<RC, FP8>, a);
 }
 
+int decode_value_chunks_per_box(int rc, bool fp8) {
+  switch (rc * 2 + (fp8 ? 1 : 0)) {
+    case 33: return Cfg<16, true>::kVRawChunks;
+    case 65: return Cfg<32, true>::kVRawChunks;
+    case 129: return Cfg<64, true>::kVRawChunks;
+    default: return 2;
+  }
+}
+
 int decode_key_chunks_per_slot(int rc, bool fp8) {
   switch (rc * 2 + (fp8 ? 1 : 0)) {
     case 32: return Cfg<16, false>::KC;
-    case 33: return Cfg<16, true>::KC;
+    case 33: return Cfg<16, true>::kKRawChunks;
     case 64: return Cfg<32, false>::KC;
-    case 65: return Cfg<32, true>::KC;
+    case 65: return Cfg<32, true>::kKRawChunks;
     case 128: return Cfg<64, false>::KC;
-    case 129: return Cfg<64, true>::KC;
+    case 129: return Cfg<64, true>::kKRawChunks;
     default: return 0;
   }
 }

@@ -280,8 +280,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       if (lane == 0) {
         const uint32_t lb = lead(b_qfull);
         if (leader) mbar_arrive_expect_tx(b_qfull, 2 * kPairQBytes);
-        for (int c = 0; c < 9; ++c)
-          tma_load_3d_pair_hint(sQ + c * kQChunk, &a.tm_q, lb, 64 * c, 128 * U.g + 64 * (int)rank, U.b, pol_keep);
+        if (a.q_whole_rows)       // one box of 64 whole rows: [8 groups][9 chunks][8 rows][128 B]
+          tma_load_5d_pair_hint(sQ, &a.tm_q, lb, 0, 0, 0, (128 * U.g + 64 * (int)rank) / 8, U.b, pol_keep);
+        else                      // 9 boxes of one 64-column chunk: [9 chunks][64 rows][128 B]
+          for (int c = 0; c < 9; ++c)
+            tma_load_3d_pair_hint(sQ + c * kQChunk, &a.tm_q, lb, 64 * c, 128 * U.g + 64 * (int)rank, U.b, pol_keep);
       }
       for (int tile = U.tb; tile < U.te && ok; ++tile) {
         int64_t rb[4];
@@ -335,7 +338,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       const uint32_t idesc_pv = make_idesc(256, 128, 1, 1, 1);
       // key slot [2 halves][8 groups][2 chunks][8 rows][128 B]: K-major, 8-row groups 2 KB apart
       const uint64_t dK0 = make_sdesc(sR, 16, 2048, kSwizzle128);
-      const uint64_t dQ0 = make_sdesc(sQ, 16, 1024, kSwizzle128);
+      // Q chunk c: [64 rows][128 B] at sQ + 8 KB c, or chunk c of [8 groups][9 chunks][8 rows]
+      const uint64_t dQ0 = make_sdesc(sQ, 16, a.q_whole_rows ? 9 * 1024 : 1024, kSwizzle128);
+      const uint32_t q_chunk = a.q_whole_rows ? 1024 : kQChunk;
       // value slot [8 groups][4 chunks][8 rows][128 B]: MN-major, chunks 1 KB, groups 4 KB apart
       const uint64_t dV0 = make_sdesc(sR, 1024, 4096, kSwizzle128);
       const uint64_t dP0 = make_sdesc(sP, 1024, 1024, kSwizzle128);   // MN-major P^T
@@ -384,7 +389,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
             const uint64_t ad = dK0 + (uint64_t)(slot * (kSlotBytes >> 4));
             for (int cc = 0; cc < (ks == kKeySlots - 1 ? 1 : 2); ++cc) {
               const int c = 2 * ks + cc;
-              const uint64_t bd = dQ0 + (uint64_t)(c * (kQChunk >> 4));
+              const uint64_t bd = dQ0 + (uint64_t)(c * (q_chunk >> 4));
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 umma_pair_f16(d, ad + (uint64_t)(cc * (1024 >> 4) + 2 * kk), bd + 2 * kk, idesc_qk, (c | kk) != 0);

@@ -92,7 +92,9 @@ struct SchedArgs {
 };
 
 struct DecodeArgs {
-  CUtensorMap tm_q;      // q as [B][R][576], 64 x RC x 1 boxes, 128-byte swizzle
+  CUtensorMap tm_q;      // q as [B][R][576], 64 x RC x 1 boxes, 128-byte swizzle; CTA pairs with
+                         // R % 8 == 0: [B][R/8 groups][9 chunks][8 rows][64] (q_whole_rows),
+                         // one box of 64 whole rows
   // the cache viewed as [Np*P/8 row groups][9 chunks][8 rows][64 columns]: a box of KC
   // (keys) or 2 (values) chunks x 64 rows lands in shared memory as
   // [group][chunk][8 rows][64 columns] (bf16: 128-byte swizzle; E4M3: plain)
@@ -112,6 +114,7 @@ struct DecodeArgs {
   int32_t s_q, H, R, P, MB, num_pages, causal;
   float softmax_scale;
   uint64_t wait_limit_ns;  // bound of every pipeline wait (2 s; tests may shorten it)
+  int32_t q_whole_rows;    // tm_q loads 64 whole rows per box (see tm_q)
   int32_t test_stall;      // tests only: 1 = the first softmax wait never completes
 };
 
@@ -137,6 +140,7 @@ cudaError_t decode_pair_prepare(bool fp8);
 cudaError_t launch_decode(const DecodeArgs& a, int rc, bool fp8, int grid, cudaStream_t s);
 cudaError_t decode_prepare(int rc, bool fp8);   // per-device kernel attributes
 int decode_key_chunks_per_slot(int rc, bool fp8);  // chunks in one key TMA box
+int decode_value_chunks_per_box(int rc, bool fp8);  // chunks in one value TMA box
 cudaError_t launch_combine(const CombineArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_cache_write(const void* latent, const void* rope, const int64_t* slots,
                                int32_t n, void* cache, int64_t total_slots, bool fp8,

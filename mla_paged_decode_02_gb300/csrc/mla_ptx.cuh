@@ -475,3 +475,16 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const CUtens
       : "memory");
 }
 }  // namespace mla
+
+namespace mla {
+__device__ __forceinline__ void tma_load_5d_pair_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar_cluster,
+                                                      int32_t c0, int32_t c1, int32_t c2, int32_t c3, int32_t c4,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+         "l"(policy)
+      : "memory");
+}
+}  // namespace mla

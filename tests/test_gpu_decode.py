@@ -94,6 +94,7 @@ SMALL = [
     (2, 1, 128, 128, [77, 4000], BF, True),          # split across many pairs, 128-row combine
     (2, 2, 128, 64, [300, 70], BF, True),            # two row groups, causal
     (2, 1, 96, 64, [500, 129], BF, True),            # a partly filled row group
+    (2, 1, 100, 64, [500, 129], BF, True),           # rows not a multiple of 8: Q by chunks
     (2, 2, 64, 64, [1000, 65], BF, True),            # 128 rows from s_q = 2
     (1, 4, 128, 64, [5000], BF, False),              # four row groups, non-causal, splits
     (2, 1, 8, 64, [700, 1300], BF, True),            # H = 8 (TP = 16 of 128 heads)
