@@ -7,9 +7,9 @@
 // our own version of that step, computed on the device from seq_lens so that the whole
 // decode stays free of host synchronisation.
 //
-// Work is counted in (key tile, row group) pairs. Sequence b has n_b = ceil(L_b / 128)
-// key tiles and G groups of query rows; each (g, b) is a stream of n_b tiles, and the
-// streams are laid end to end, group-major:
+// Work is counted in (key tile, row group) pairs. Sequence b has n_b = ceil(L_b / T)
+// key tiles (T = 128, or 256 for CTA pairs) and G groups of query rows; each (g, b) is a
+// stream of n_b tiles, and the streams are laid end to end, group-major:
 //   pos(g, b) = g * N + sum_{b' < b} n_b',    N = sum_b n_b,    W = G * N,
 // The persistent decode grid has one CTA per SM; CTA c takes the positions
 // [c q, (c + 1) q) with q = ceil(W / grid), so no CTA has more than one tile more work
@@ -21,6 +21,9 @@
 // its log-sum-exp) to its own slot, and the combine kernel merges the pieces. Streams
 // inside one CTA write the final output directly. Units are stored in position order,
 // so the units of CTA c are the contiguous range [cta_first[c], cta_first[c + 1]).
+// The G x B streams are handled as one flattened, position-ordered index space (each
+// thread a contiguous range of it, one block-wide scan for the unit, split and slot
+// offsets), so the schedule's cost does not grow with the number of row groups.
 #include "mla_cache_write.cuh"
 #include "mla_internal.h"
 #include "mla_ptx.cuh"
@@ -30,6 +33,7 @@ namespace mla {
 
 constexpr int kSchedThreads = 1024;
 constexpr int kMaxWriteCtas = 128;
+constexpr int kMaxGroups = kMaxRows / 16;   // row groups of a sequence (16 rows or more each)
 
 // Exclusive prefix sum over the block's threads (warp shuffles, then the 32 warp totals).
 __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* tmp, int64_t* total) {
@@ -68,6 +72,8 @@ __device__ __forceinline__ int clamped_len(const SchedArgs& a, int b, bool repor
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   static_assert(kSchedThreads == 1024, "the scan assumes 32 warps");
   __shared__ int64_t scan_tmp[32];
+  __shared__ int64_t n_tiles_s;
+  __shared__ int32_t gend_s[kMaxGroups];   // end of each row group's units (aligned mode)
   const int tid = threadIdx.x;
   griddep_launch_dependents();         // the decode grid may start its set-up now
   if (blockIdx.x > 0) {
@@ -89,90 +95,96 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   if (tid == 0) a.hdr[0] = 0u;
   __syncthreads();
 
-  const int chunk = (a.B + kSchedThreads - 1) / kSchedThreads;
-  const int b0 = tid * chunk;
-  const int b1 = min(a.B, b0 + chunk);
-  const int G = a.G;
-
-  // 1. key tiles per sequence (lengths clamped into the valid range; bad ones flagged)
-  int64_t my_tiles = 0;
-  for (int b = b0; b < b1; ++b) my_tiles += (clamped_len(a, b, true) + a.tile - 1) / a.tile;
-  int64_t n_tiles;
-  const int64_t tile_off = block_exclusive_scan(my_tiles, scan_tmp, &n_tiles);
+  const int G = a.G, B = a.B;
+  // 1. key tiles per sequence (lengths clamped into the valid range; bad ones flagged) and
+  //    their exclusive prefix: batch_info[b] = (tiles, first tile of b, clamped length, 0)
+  {
+    const int chunk = (B + kSchedThreads - 1) / kSchedThreads;
+    const int b0 = tid * chunk, b1 = min(B, b0 + chunk);
+    int64_t my_tiles = 0;
+    for (int b = b0; b < b1; ++b) my_tiles += (clamped_len(a, b, true) + a.tile - 1) / a.tile;
+    int64_t n_tiles_all;
+    int64_t off = block_exclusive_scan(my_tiles, scan_tmp, &n_tiles_all);
+    for (int b = b0; b < b1; ++b) {
+      const int Lc = clamped_len(a, b, false);
+      const int n = (Lc + a.tile - 1) / a.tile;
+      a.batch_info[b] = make_int4(n, (int)off, Lc, 0);
+      off += n;
+    }
+    if (tid == 0) n_tiles_s = n_tiles_all;
+  }
+  __syncthreads();                     // batch_info (global, this block's writes) and n_tiles_s
+  const int64_t n_tiles = n_tiles_s;
   const int64_t W = (int64_t)G * n_tiles;
   const bool aligned = G > 1 && a.grid % G == 0;   // one CTA block per row group
   const int cpg = aligned ? a.grid / G : a.grid;    // CTAs per row group
   const int64_t q = aligned ? (n_tiles + cpg - 1) / cpg : (W + a.grid - 1) / a.grid;   // >= 1
 
-  // 2. per group g (in position order): units, cut streams and partial slots of this
-  //    thread's sequences, and their offsets; then the units themselves
-  int64_t unit_base = 0, split_base = 0, slot_base = 0;
-  for (int g = 0; g < G; ++g) {
-    // positions of group g: g N + p (one partition of all W) or p (aligned, CTAs g cpg ...)
-    const int64_t goff = aligned ? 0 : (int64_t)g * n_tiles;
-    const int cbase = aligned ? g * cpg : 0;
-    int64_t my_units = 0, my_split = 0, my_slots = 0;
-    int64_t pre = goff + tile_off;
-    for (int b = b0; b < b1; ++b) {
-      const int n = (clamped_len(a, b, false) + a.tile - 1) / a.tile;
-      const int64_t ns = (pre + n - 1) / q - pre / q + 1;
-      my_units += ns;
-      if (ns >= 2) { my_split += 1; my_slots += ns; }
-      pre += n;
-    }
-    int64_t g_units, g_split, g_slots;
-    int64_t unit_off = unit_base + block_exclusive_scan(my_units, scan_tmp, &g_units);
-    int64_t split_off = split_base + block_exclusive_scan(my_split, scan_tmp, &g_split);
-    int64_t slot_off = slot_base + block_exclusive_scan(my_slots, scan_tmp, &g_slots);
-    unit_base += g_units;
-    split_base += g_split;
-    slot_base += g_slots;
-    if (unit_base > a.max_units || split_base > a.max_split || slot_base > a.max_slots) {
-      // cannot happen for the sizes mla_decode_workspace_size returns; refuse to overflow
-      for (int c = tid; c <= a.grid; c += kSchedThreads) a.cta_first[c] = 0;
-      if (tid == 0) { atomicOr(a.hdr, MLA_DEVERR_SEQ_LEN); a.hdr[1] = 0; a.hdr[2] = 0; }
-      return;
-    }
-    if (g == 0) {
-      // the first unit of each CTA is set below; a CTA whose range starts at or past W
-      // has no work. The number of units is known only at the end: patched there.
-      for (int c = tid; c <= a.grid; c += kSchedThreads) a.cta_first[c] = -1;
-      __syncthreads();
-    }
-    // units in position order; the unit starting at c q is the first of CTA cbase + c
-    pre = goff + tile_off;
-    for (int b = b0; b < b1; ++b) {
-      const int Lc = clamped_len(a, b, false);
-      const int n = (Lc + a.tile - 1) / a.tile;
-      if (g == 0) a.batch_info[b] = make_int4(n, 0, Lc, 0);
-      const int64_t c_lo = pre / q;
-      const int ns = (int)((pre + n - 1) / q - c_lo + 1);
-      const int slot0 = ns >= 2 ? (int)slot_off : -1;
-      if (ns >= 2) a.split_list[split_off++] = make_int4(b, g, ns, slot0);
-      for (int k = 0; k < ns; ++k) {
-        const int64_t c = c_lo + k;
-        const int64_t s0 = pre > c * q ? pre : c * q;
-        const int64_t s1 = pre + n < (c + 1) * q ? pre + n : (c + 1) * q;
-        const int tb = (int)(s0 - pre), te = (int)(s1 - pre);
-        a.units[unit_off] = make_int4(b, g, tb | (te << 16), ns >= 2 ? slot0 + k : -1);
-        if (s0 == c * q) a.cta_first[cbase + c] = (int32_t)unit_off;
-        ++unit_off;
-      }
-      if (ns >= 2) slot_off += ns;
-      pre += n;
-    }
-    if (aligned) {
-      // a CTA of this group's block without work starts (and ends) at the group's end, so
-      // that the ranges [cta_first[c], cta_first[c + 1]) stay within their group
-      __syncthreads();
-      for (int c = cbase + tid; c < cbase + cpg; c += kSchedThreads)
-        if (a.cta_first[c] < 0) a.cta_first[c] = (int32_t)unit_base;
-    }
+  // 2. the (row group g, sequence b) streams in position order, flattened: item i = g B + b,
+  //    stream start pos = (aligned ? 0 : g N) + first tile of b. Every stream is cut at the
+  //    CTA boundaries it crosses (multiples of q): ns pieces, one unit each; a cut stream
+  //    (ns >= 2) gets ns consecutive partial slots and an entry in the split list.
+  const int64_t items = (int64_t)G * B;
+  const int64_t ichunk = (items + kSchedThreads - 1) / kSchedThreads;
+  const int64_t i0 = (int64_t)tid * ichunk, i1 = min(items, i0 + ichunk);
+  auto pieces = [&](int64_t i, int64_t* pre_out, int* n_out) -> int64_t {
+    const int g = (int)(i / B), b = (int)(i - (int64_t)g * B);
+    const int4 bi = a.batch_info[b];
+    const int64_t pre = (aligned ? 0 : (int64_t)g * n_tiles) + bi.y;
+    *pre_out = pre;
+    *n_out = bi.x;
+    return (pre + bi.x - 1) / q - pre / q + 1;
+  };
+  int64_t my_units = 0, my_split = 0, my_slots = 0;
+  for (int64_t i = i0; i < i1; ++i) {
+    int64_t pre;
+    int n;
+    const int64_t ns = pieces(i, &pre, &n);
+    my_units += ns;
+    if (ns >= 2) { my_split += 1; my_slots += ns; }
   }
+  int64_t n_units, n_split, n_slots;
+  int64_t unit_off = block_exclusive_scan(my_units, scan_tmp, &n_units);
+  int64_t split_off = block_exclusive_scan(my_split, scan_tmp, &n_split);
+  int64_t slot_off = block_exclusive_scan(my_slots, scan_tmp, &n_slots);
+  if (n_units > a.max_units || n_split > a.max_split || n_slots > a.max_slots) {
+    // cannot happen for the sizes mla_decode_workspace_size returns; refuse to overflow
+    for (int c = tid; c <= a.grid; c += kSchedThreads) a.cta_first[c] = 0;
+    if (tid == 0) { atomicOr(a.hdr, MLA_DEVERR_SEQ_LEN); a.hdr[1] = 0; a.hdr[2] = 0; }
+    return;
+  }
+  // the first unit of each CTA is set below; a CTA whose range starts at or past the end
+  // has no work (patched in step 3)
+  for (int c = tid; c <= a.grid; c += kSchedThreads) a.cta_first[c] = -1;
   __syncthreads();
+  for (int64_t i = i0; i < i1; ++i) {
+    int64_t pre;
+    int n;
+    const int ns = (int)pieces(i, &pre, &n);
+    const int g = (int)(i / B), b = (int)(i - (int64_t)g * B);
+    const int cbase = aligned ? g * cpg : 0;
+    if (b == 0 && g > 0) gend_s[g - 1] = (int32_t)unit_off;   // the units of groups < g end here
+    const int64_t c_lo = pre / q;
+    const int slot0 = ns >= 2 ? (int)slot_off : -1;
+    if (ns >= 2) a.split_list[split_off++] = make_int4(b, g, ns, slot0);
+    for (int k = 0; k < ns; ++k) {
+      const int64_t c = c_lo + k;
+      const int64_t s0 = pre > c * q ? pre : c * q;
+      const int64_t s1 = pre + n < (c + 1) * q ? pre + n : (c + 1) * q;
+      const int tb = (int)(s0 - pre), te = (int)(s1 - pre);
+      a.units[unit_off] = make_int4(b, g, tb | (te << 16), ns >= 2 ? slot0 + k : -1);
+      if (s0 == c * q) a.cta_first[cbase + c] = (int32_t)unit_off;
+      ++unit_off;
+    }
+    if (ns >= 2) slot_off += ns;
+  }
+  if (tid == 0) gend_s[G - 1] = (int32_t)n_units;
+  __syncthreads();
+  // 3. CTAs without work start (and end) at the end of their group's units (aligned: so
+  //    that the ranges [cta_first[c], cta_first[c + 1]) stay within the group), else at
+  //    the end of all units
   for (int c = tid; c <= a.grid; c += kSchedThreads)
-    if (a.cta_first[c] < 0) a.cta_first[c] = (int32_t)unit_base;
-  const int64_t n_units = unit_base, n_split = split_base;
+    if (a.cta_first[c] < 0) a.cta_first[c] = aligned && c < a.grid ? gend_s[c / cpg] : (int32_t)n_units;
   if (tid == 0) {
     a.hdr[1] = (uint32_t)n_units;
     a.hdr[2] = (uint32_t)n_split;
