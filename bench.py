@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="the workload's first B sequences only (smaller cases for profiling)")
     return ap.parse_args()
 
 
@@ -93,6 +95,19 @@ def barrier(world: int):
 def make_case(args, rank: int):
     from mla_paged_decode_02_gb300 import synth
     kv = None if args.kv is None else (synth.KV_BF16 if args.kv == "bf16" else synth.KV_FP8_E4M3)
+    if args.batch is not None:
+        # the same length distribution, seed and shape with a smaller batch
+        kw = dict(synth.CONFIGS[args.config])
+        name = synth.config_name(args.config, kv, args.s_q) + f"_b{args.batch}"
+        kw.pop("name")
+        kw["B"] = args.batch
+        if isinstance(kw["seq_lens"], list):
+            kw["seq_lens"] = kw["seq_lens"][:args.batch]
+        if kv is not None:
+            kw["kv_dtype"] = kv
+        if args.s_q is not None:
+            kw["s_q"] = args.s_q
+        return synth.make_case(seed=synth.SEED_OF[args.config] + 7919 * rank, name=name, **kw)
     case = synth.make_config(args.config, kv_dtype=kv, s_q=args.s_q)
     if rank:
         kw = dict(synth.CONFIGS[args.config])
