@@ -82,7 +82,7 @@ typedef struct mla_decode_params {
   int32_t batch;               /* B >= 1 */
   int32_t s_q;                 /* new query tokens per sequence, 1..512 */
   int32_t num_heads;           /* H >= 1; s_q * H <= 65536 */
-  int32_t page_size;           /* P: a multiple of 64, at most 1024 */
+  int32_t page_size;           /* P: a multiple of 8, at most 1024 (else UNSUPPORTED) */
   int32_t num_pages;           /* Np: pages in the pool */
   int32_t max_blocks_per_seq;  /* MB: row stride of block_table */
   int32_t max_seq_len;         /* host-known upper bound on seq_lens[], <= 2^20;

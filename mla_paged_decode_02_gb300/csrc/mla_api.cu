@@ -1,5 +1,6 @@
 // mla_api.cu — the C ABI (include/mla.h): argument checks, workspace layout, TMA
 // descriptors and the launch sequence  schedule -> decode -> combine  on one stream.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -78,7 +79,7 @@ mla_status check_params(const mla_decode_params* p) {
   if (p->kv_dtype != MLA_KV_BF16 && p->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
   if (p->causal != 0 && p->causal != 1) return MLA_ERR_INVALID_ARG;
   if (p->max_seq_len < p->s_q) return MLA_ERR_INVALID_ARG;
-  if (p->page_size % 64 != 0 || p->page_size > 1024) return MLA_ERR_UNSUPPORTED;
+  if (p->page_size % 8 != 0 || p->page_size > 1024) return MLA_ERR_UNSUPPORTED;
   if (p->s_q > kMaxSq || (int64_t)p->s_q * p->num_heads > kMaxRows) return MLA_ERR_UNSUPPORTED;
   if (p->batch > kMaxBatch || p->max_seq_len > kMaxSeqLen) return MLA_ERR_UNSUPPORTED;
   if ((int64_t)p->num_pages * p->page_size >= (int64_t)1 << 31) return MLA_ERR_UNSUPPORTED;
@@ -87,16 +88,16 @@ mla_status check_params(const mla_decode_params* p) {
 }
 
 // The cache as [rows / 8 groups][9 chunks][8 rows][64 elements] (strides 8 rows, one
-// chunk, one row): a box of `chunks` chunks x 8 groups (64 rows) lands in shared memory
+// chunk, one row): a box of `chunks` chunks x box_rows / 8 groups lands in shared memory
 // as [group][chunk][8 rows][64 elements]. bf16 rows (128 B) are 128-byte swizzled for
 // the MMA. E4M3 key rows (64 B) are 64-byte swizzled, so that 32 threads reading one
 // row each hit distinct banks; E4M3 value rows are left plain.
-bool encode_kv_map(CUtensorMap* m, const void* cache, int64_t rows, uint32_t chunks, bool fp8,
-                   bool keys) {
+bool encode_kv_map(CUtensorMap* m, const void* cache, int64_t rows, uint32_t chunks, uint32_t box_rows,
+                   bool fp8, bool keys) {
   const cuuint64_t es = fp8 ? 1 : 2;
   cuuint64_t dims[4] = {64, 8, 9, (cuuint64_t)(rows / 8)};
   cuuint64_t strides[3] = {kDQK * es, 64 * es, kDQK * es * 8};
-  cuuint32_t box[4] = {64, 8, chunks, 8};
+  cuuint32_t box[4] = {64, 8, chunks, box_rows / 8};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                         const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -260,6 +261,8 @@ static mla_status decode_impl(const mla_decode_params* p, const void* q, const v
 
   DecodeArgs da;
   std::memset(&da, 0, sizeof(da));
+  // key / value boxes of gcd(P, 64) rows never straddle a page
+  const int box_rows = std::min(64, p->page_size & -p->page_size);
   // a CTA of a pair holds 64 of its unit's 128 rows (as whole rows when R % 8 == 0)
   da.q_whole_rows = plan.pair && R % 8 == 0 ? 1 : 0;
   if (da.q_whole_rows ? !encode_q_rows_map(&da.tm_q, q, B, R) : !encode_q_map(&da.tm_q, q, B, R, plan.pair ? 64 : rc))
@@ -269,8 +272,8 @@ static mla_status decode_impl(const mla_decode_params* p, const void* q, const v
     // chunks per key / value box: a pair loads 2 / 4 adjacent chunks of each row
     const uint32_t kc = plan.pair ? 2u : (uint32_t)decode_key_chunks_per_slot(rc, fp8);
     const uint32_t vc = plan.pair ? 4u : (uint32_t)decode_value_chunks_per_box(rc, fp8);
-    if (!encode_kv_map(&da.tm_k, kv_cache, rows, kc, fp8, true) ||
-        !encode_kv_map(&da.tm_v, kv_cache, rows, vc, fp8, false))
+    if (!encode_kv_map(&da.tm_k, kv_cache, rows, kc, (uint32_t)box_rows, fp8, true) ||
+        !encode_kv_map(&da.tm_v, kv_cache, rows, vc, (uint32_t)box_rows, fp8, false))
       return MLA_ERR_INVALID_ARG;
   }
   da.kv_cache = kv_cache;
@@ -289,6 +292,7 @@ static mla_status decode_impl(const mla_decode_params* p, const void* q, const v
   da.H = p->num_heads;
   da.R = R;
   da.P = p->page_size;
+  da.box_rows = box_rows;
   da.MB = p->max_blocks_per_seq;
   da.num_pages = p->num_pages;
   da.causal = p->causal;

@@ -52,6 +52,7 @@
 #include <cuda_fp16.h>
 #include <type_traits>
 #include "mla_internal.h"
+#include "mla_pages.cuh"
 #include "mla_ptx.cuh"
 #include "../../include/mla.h"
 
@@ -171,15 +172,17 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 }
 
 // Walks the key tiles of this CTA's units in the order every role consumes them, with
-// the first global cache row of each 64-key half of the current tile: >= 0 a row, -1 a
-// half wholly past the sequence end. A block-table entry outside the pool is flagged in
-// the error word and its half reads page 0 instead.
+// per 64-key block h of the current tile the cache row of its first box (rb_h, -1 for a
+// block wholly past the sequence end) and the number of its boxes that are loaded (nb_h;
+// mla_pages.cuh). A block-table entry outside the pool is flagged in the error word and
+// page 0 is read instead.
 struct TileIter {
   int u;
   Unit U;
   int tile;
   int64_t rb0, rb1;
-  __device__ __forceinline__ int64_t row_base(int row) const { return row < 64 ? rb0 : rb1; }
+  int nb0, nb1;
+  __device__ __forceinline__ uint32_t boxes() const { return (uint32_t)(nb0 + nb1); }
 };
 
 __device__ __forceinline__ void iter_rows(TileIter& it, const DecodeArgs& a, uint32_t* err,
@@ -188,19 +191,20 @@ __device__ __forceinline__ void iter_rows(TileIter& it, const DecodeArgs& a, uin
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int tok = it.tile * kTileTokens + 64 * h;
-    int64_t r = -1;
-    if (tok < it.U.L) {
-      const int pg = __ldg(bt + tok / a.P);
-      if (pg < 0 || pg >= a.num_pages) {
-        if (report) atomicOr(err, MLA_DEVERR_BLOCK_TABLE);
-        r = tok % a.P;
-      } else {
-        r = (int64_t)pg * a.P + tok % a.P;
-      }
-    }
-    if (h == 0) it.rb0 = r;
-    else it.rb1 = r;
+    const int64_t r = tok < it.U.L ? page_row(bt, tok, a, err, report) : -1;
+    const int nb = block_boxes(it.U.L - tok, a.box_rows);
+    if (h == 0) { it.rb0 = r; it.nb0 = nb; }
+    else { it.rb1 = r; it.nb1 = nb; }
   }
+}
+
+// Issues the boxes of block h of the iterator's tile: issue(k, group) for box k.
+template <class F>
+__device__ __forceinline__ void issue_half(const TileIter& it, const DecodeArgs& a, uint32_t* err, int h, F&& issue) {
+  const int nb = h == 0 ? it.nb0 : it.nb1;
+  if (nb == 0) return;
+  issue_block(a.block_table + (int64_t)it.U.b * a.MB, a, err, it.tile * kTileTokens + 64 * h,
+              h == 0 ? it.rb0 : it.rb1, nb, issue);
 }
 
 __device__ __forceinline__ bool iter_begin(TileIter& it, const DecodeArgs& a, int u0, int u1,
@@ -389,17 +393,18 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       bool more = iter_begin(it, a, u0, u1, err, true);
       bool ok = true;
       uint32_t p = 0;
+      const uint32_t box_bytes = (C::kKSlotBytes / 128) * (uint32_t)a.box_rows;
       while (more && ok) {
-        const uint32_t nbox = (it.rb0 >= 0 ? 1u : 0u) + (it.rb1 >= 0 ? 1u : 0u);
         for (int sl = 0; sl < C::kSlotsPerTile; ++sl, ++p) {
           const uint32_t slot = p % NK;
           ok = wait(b_kempty + 8 * slot, ((p / NK) & 1) ^ 1);
           if (!ok) break;
           const uint32_t bar = b_kfull + 8 * slot, dst = sK + slot * C::kKSlotBytes;
-          mbar_arrive_expect_tx(bar, nbox * (C::kKSlotBytes / 2));
-          if (it.rb0 >= 0) tma_load_4d(dst, &a.tm_k, bar, 0, 0, sl * C::KC, (int32_t)(it.rb0 >> 3));
-          if (it.rb1 >= 0)
-            tma_load_4d(dst + C::kKSlotBytes / 2, &a.tm_k, bar, 0, 0, sl * C::KC, (int32_t)(it.rb1 >> 3));
+          mbar_arrive_expect_tx(bar, it.boxes() * box_bytes);
+          for (int h = 0; h < 2; ++h)
+            issue_half(it, a, err, h, [&](int k, int32_t grp) {
+              tma_load_4d(dst + h * (C::kKSlotBytes / 2) + k * box_bytes, &a.tm_k, bar, 0, 0, sl * C::KC, grp);
+            });
         }
         if (ok) more = iter_next(it, a, u1, err, true);
       }
@@ -418,10 +423,10 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     bool more = iter_begin(it, a, u0, u1, err, false);
     bool ok = true;
     uint32_t p = 0, aux = 0;
+    const uint32_t box_bytes = (kVSlotBytes / 128) * (uint32_t)a.box_rows;
     while (more && ok) {
       const int valid = it.U.L - it.tile * kTileTokens;
       const bool tail = valid < kTileTokens;
-      const uint32_t nbox = (it.rb0 >= 0 ? 1u : 0u) + (it.rb1 >= 0 ? 1u : 0u);
       for (int j = 0; j < kPairsPerTile; ++j, ++p) {
         const uint32_t slot = p % NV;
         ok = wait_warp(b_vempty + 8 * slot, ((p / NV) & 1) ^ 1);
@@ -429,9 +434,11 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         const uint32_t dst = sV + slot * kVSlotBytes;
         const uint32_t bar = tail ? b_vaux : b_vfull + 8 * slot;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar, nbox * (kVSlotBytes / 2));
-          if (it.rb0 >= 0) tma_load_4d(dst, &a.tm_v, bar, 0, 0, 2 * j, (int32_t)(it.rb0 >> 3));
-          if (it.rb1 >= 0) tma_load_4d(dst + kVSlotBytes / 2, &a.tm_v, bar, 0, 0, 2 * j, (int32_t)(it.rb1 >> 3));
+          mbar_arrive_expect_tx(bar, it.boxes() * box_bytes);
+          for (int h = 0; h < 2; ++h)
+            issue_half(it, a, err, h, [&](int k, int32_t grp) {
+              tma_load_4d(dst + h * (kVSlotBytes / 2) + k * box_bytes, &a.tm_v, bar, 0, 0, 2 * j, grp);
+            });
         }
         if (tail) {
           ok = wait_warp(b_vaux, aux & 1);
@@ -835,12 +842,14 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     auto top_up = [&]() {
       while (kimore && kip < kfreed + NKS) {
         const uint32_t sl = kip % NKS, bar = b_kstage + 8 * sl, dst = sKS + sl * C::kKStageBytes;
-        const uint32_t nbox = (ki.rb0 >= 0 ? 1u : 0u) + (ki.rb1 >= 0 ? 1u : 0u);
+        const uint32_t box_bytes = (C::kKStageBytes / 128) * (uint32_t)a.box_rows;
         // a whole-row stage (all 9 chunks) or the KC chunks of one position
         const int32_t c0 = C::kRawRows ? 0 : kic * C::KC;
-        mbar_arrive_expect_tx(bar, nbox * (C::kKStageBytes / 2));
-        if (ki.rb0 >= 0) tma_load_4d(dst, &a.tm_k, bar, 0, 0, c0, (int32_t)(ki.rb0 >> 3));
-        if (ki.rb1 >= 0) tma_load_4d(dst + C::kKStageBytes / 2, &a.tm_k, bar, 0, 0, c0, (int32_t)(ki.rb1 >> 3));
+        mbar_arrive_expect_tx(bar, ki.boxes() * box_bytes);
+        for (int h = 0; h < 2; ++h)
+          issue_half(ki, a, err, h, [&](int k, int32_t grp) {
+            tma_load_4d(dst + h * (C::kKStageBytes / 2) + k * box_bytes, &a.tm_k, bar, 0, 0, c0, grp);
+          });
         if (C::kRawRows || ++kic == C::kSlotsPerTile) { kic = 0; kimore = iter_next(ki, a, u1, err, false); }
         ++kip;
       }
@@ -945,11 +954,11 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     // two slots that would put the raw load's latency behind the slot's release).
     if (lane == 0) {
       TileIter it;
-      bool more = iter_begin(it, a, u0, u1, err, false);
+      bool more = iter_begin(it, a, u0, u1, err, true);   // reports bad block-table entries
       bool ok = true;
       uint32_t p = 0;
+      const uint32_t box_bytes = (C::kVStage / 128) * (uint32_t)a.box_rows;
       while (more && ok) {
-        const uint32_t nbox = (it.rb0 >= 0 ? 1u : 0u) + (it.rb1 >= 0 ? 1u : 0u);
         for (int j = 0; j < kPairsPerTile; j += C::kPairsPerVStage, ++p) {
           // stage p: value chunks 2j .. 2j + kVRawChunks - 1 of the tile's rows
           const uint32_t sl = p % NVS;
@@ -957,11 +966,13 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
                (NV < 3 || wait(b_vempty + 8 * (p % NV), ((p / NV) & 1) ^ 1));
           if (!ok) break;
           const uint32_t bar = b_vstage + 8 * sl, dst = sVS + sl * C::kVStage;
-          mbar_arrive_expect_tx(bar, nbox * (C::kVStage / 2));
-          if (it.rb0 >= 0) tma_load_4d(dst, &a.tm_v, bar, 0, 0, 2 * j, (int32_t)(it.rb0 >> 3));
-          if (it.rb1 >= 0) tma_load_4d(dst + C::kVStage / 2, &a.tm_v, bar, 0, 0, 2 * j, (int32_t)(it.rb1 >> 3));
+          mbar_arrive_expect_tx(bar, it.boxes() * box_bytes);
+          for (int h = 0; h < 2; ++h)
+            issue_half(it, a, err, h, [&](int k, int32_t grp) {
+              tma_load_4d(dst + h * (C::kVStage / 2) + k * box_bytes, &a.tm_v, bar, 0, 0, 2 * j, grp);
+            });
         }
-        if (ok) more = iter_next(it, a, u1, err, false);
+        if (ok) more = iter_next(it, a, u1, err, true);
       }
       volatile uint32_t no_abort = 0;
       for (uint32_t q = p > (uint32_t)NVS ? p - NVS : 0; q < p; ++q)

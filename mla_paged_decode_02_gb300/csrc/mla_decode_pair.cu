@@ -44,6 +44,7 @@
 // both CTAs drain and leave through a final cluster barrier.
 #include <cuda_bf16.h>
 #include "mla_internal.h"
+#include "mla_pages.cuh"
 #include "mla_ptx.cuh"
 #include "../../include/mla.h"
 
@@ -87,23 +88,14 @@ __device__ __forceinline__ PUnit load_punit(const DecodeArgs& a, int u) {
 
 // First global cache row of each 64-key block kb of super-tile `tile` (-1: past the
 // sequence end). A block-table entry outside the pool is flagged and reads page 0.
-__device__ __forceinline__ void block_rows(const DecodeArgs& a, const PUnit& U, int tile, int64_t* rb,
+__device__ __forceinline__ void block_rows(const DecodeArgs& a, const PUnit& U, int tile, int64_t* rb, int* nb,
                                            uint32_t* err, bool report) {
   const int32_t* bt = a.block_table + (int64_t)U.b * a.MB;
 #pragma unroll
   for (int kb = 0; kb < 4; ++kb) {
     const int tok = tile * kPairKeys + 64 * kb;
-    int64_t r = -1;
-    if (tok < U.L) {
-      const int pg = __ldg(bt + tok / a.P);
-      if (pg < 0 || pg >= a.num_pages) {
-        if (report) atomicOr(err, MLA_DEVERR_BLOCK_TABLE);
-        r = tok % a.P;
-      } else {
-        r = (int64_t)pg * a.P + tok % a.P;
-      }
-    }
-    rb[kb] = r;
+    rb[kb] = tok < U.L ? page_row(bt, tok, a, err, report) : -1;
+    nb[kb] = block_boxes(U.L - tok, a.box_rows);
   }
 }
 
@@ -226,11 +218,17 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
     const uint64_t pol_keep = l2_policy_evict_last(), pol_last = l2_policy_evict_first();
     // the block holding the sequence end gets the rows up to the end of its last 16-key MMA
     // step zeroed (the cache may hold NaN there, and 0 * NaN is NaN inside the MMA)
-    auto load_values = [&](const PUnit& U, int tile, const int64_t* rb) -> bool {
+    const int32_t* bt_all = a.block_table;
+    const uint32_t kbox_bytes = (kSlotBytes / 128) * (uint32_t)a.box_rows;   // one key box
+    const uint32_t vbox_bytes = (kSlotBytes / 64) * (uint32_t)a.box_rows;    // one value box
+    auto load_values = [&](const PUnit& U, int tile, const int64_t* rb, const int* nb) -> bool {
+      const int32_t* bt = bt_all + (int64_t)U.b * a.MB;
       for (int kb = 0; kb < 4; ++kb) {
         if (rb[kb] < 0) continue;
         const int valid = U.L - tile * kPairKeys - 64 * kb;
-        const bool zero = valid < 64 && (valid & 15) != 0;
+        // a block not loaded whole (boxes past the sequence end) completes its bytes itself
+        const bool zero = valid < 64 && ((valid & 15) != 0 || nb[kb] < 64 / a.box_rows);
+        const int tok0 = tile * kPairKeys + 64 * kb;
         const uint32_t slot = r % kRing;
         bool w_ok = lane != 0 || wait(b_empty + 8 * slot, ((r / kRing) & 1) ^ 1);
         if (!__all_sync(0xffffffffu, w_ok)) return false;
@@ -238,11 +236,16 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
         const int32_t c0 = 4 * (int)rank;            // this CTA's value columns 256 rank ..
         if (leader && lane == 0) mbar_arrive_expect_tx(b_full + 8 * slot, 2 * kSlotBytes);
         if (!zero) {
-          if (lane == 0) tma_load_4d_pair_hint(dst, &a.tm_v, lb, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
+          if (lane == 0)
+            issue_block(bt, a, err, tok0, rb[kb], nb[kb], [&](int k, int32_t grp) {
+              tma_load_4d_pair_hint(dst + k * vbox_bytes, &a.tm_v, lb, 0, 0, c0, grp, pol_last);
+            });
         } else {
           if (lane == 0) {
-            mbar_arrive_expect_tx(b_aux, kSlotBytes);
-            tma_load_4d_hint(dst, &a.tm_v, b_aux, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
+            mbar_arrive_expect_tx(b_aux, (uint32_t)nb[kb] * vbox_bytes);
+            issue_block(bt, a, err, tok0, rb[kb], nb[kb], [&](int k, int32_t grp) {
+              tma_load_4d_hint(dst + k * vbox_bytes, &a.tm_v, b_aux, 0, 0, c0, grp, pol_last);
+            });
           }
           w_ok = wait(b_aux, aux & 1);
           ++aux;
@@ -270,6 +273,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
     PUnit pu{};
     int ptile = -1;
     int64_t prb[4] = {-1, -1, -1, -1};
+    int pnb[4] = {0, 0, 0, 0};
     for (int u = u0; u < u1 && ok; ++u, ++uq) {
       const PUnit U = load_punit(a, u);
       // this CTA's 64 query rows of the unit (rows past R read as zeros), kept in L2 for the
@@ -288,10 +292,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       }
       for (int tile = U.tb; tile < U.te && ok; ++tile) {
         int64_t rb[4];
-        block_rows(a, U, tile, rb, err, leader);
-        const int64_t h0 = rb[2 * rank], h1 = rb[2 * rank + 1];
+        int nb[4];
+        block_rows(a, U, tile, rb, nb, err, leader);
+        const int32_t* bt = bt_all + (int64_t)U.b * a.MB;
         // bytes of both CTAs' key halves (the even CTA arms the barrier for both)
-        const uint32_t nbox = (rb[0] >= 0) + (rb[1] >= 0) + (rb[2] >= 0) + (rb[3] >= 0);
+        const uint32_t nbox = (uint32_t)(nb[0] + nb[1] + nb[2] + nb[3]);
         for (int ks = 0; ks < kKeySlots; ++ks) {
           const uint32_t slot = r % kRing;
           w_ok = lane != 0 || wait(b_empty + 8 * slot, ((r / kRing) & 1) ^ 1);
@@ -300,21 +305,26 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
           if (lane == 0) {
             // chunks 2ks, 2ks + 1 (the last slot: chunk 8 and a zero-filled chunk past the row)
             const uint32_t lb = lead(b_full + 8 * slot), dst = sR + slot * kSlotBytes;
-            if (leader) mbar_arrive_expect_tx(b_full + 8 * slot, nbox * (kSlotBytes / 2));
-            if (h0 >= 0) tma_load_4d_pair_hint(dst, &a.tm_k, lb, 0, 0, 2 * ks, (int32_t)(h0 >> 3), pol_keep);
-            if (h1 >= 0)
-              tma_load_4d_pair_hint(dst + kSlotBytes / 2, &a.tm_k, lb, 0, 0, 2 * ks, (int32_t)(h1 >> 3), pol_keep);
+            if (leader) mbar_arrive_expect_tx(b_full + 8 * slot, nbox * kbox_bytes);
+            for (int h = 0; h < 2; ++h) {
+              const int kb = 2 * (int)rank + h;
+              if (nb[kb] > 0)
+                issue_block(bt, a, err, tile * kPairKeys + 64 * kb, rb[kb], nb[kb], [&](int k, int32_t grp) {
+                  tma_load_4d_pair_hint(dst + h * (kSlotBytes / 2) + k * kbox_bytes, &a.tm_k, lb, 0, 0, 2 * ks, grp,
+                                        pol_keep);
+                });
+            }
           }
           ++r;
         }
         if (!ok) break;
-        if (ptile >= 0) ok = load_values(pu, ptile, prb);
+        if (ptile >= 0) ok = load_values(pu, ptile, prb, pnb);
         pu = U;
         ptile = tile;
-        for (int kb = 0; kb < 4; ++kb) prb[kb] = rb[kb];
+        for (int kb = 0; kb < 4; ++kb) { prb[kb] = rb[kb]; pnb[kb] = nb[kb]; }
       }
     }
-    if (ok && ptile >= 0) ok = load_values(pu, ptile, prb);
+    if (ok && ptile >= 0) ok = load_values(pu, ptile, prb, pnb);
     // after an abort the odd CTA cannot observe its own loads (they count on the even CTA's
     // barrier, whose phase may never complete): both producers wait 50 us, far longer than
     // a load takes, before leaving

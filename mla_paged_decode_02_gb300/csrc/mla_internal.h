@@ -96,7 +96,7 @@ struct DecodeArgs {
                          // R % 8 == 0: [B][R/8 groups][9 chunks][8 rows][64] (q_whole_rows),
                          // one box of 64 whole rows
   // the cache viewed as [Np*P/8 row groups][9 chunks][8 rows][64 columns]: a box of KC
-  // (keys) or 2 (values) chunks x 64 rows lands in shared memory as
+  // (keys) or 2 (values) chunks x box_rows rows lands in shared memory as
   // [group][chunk][8 rows][64 columns] (bf16: 128-byte swizzle; E4M3: plain)
   CUtensorMap tm_k, tm_v;
   const void* kv_cache;  // [Np][P][576] bf16 or E4M3 bytes
@@ -112,6 +112,7 @@ struct DecodeArgs {
   uint32_t* err;
   const float* kv_scale;
   int32_t s_q, H, R, P, MB, num_pages, causal;
+  int32_t box_rows;        // rows of one key/value TMA box: gcd(P, 64)
   float softmax_scale;
   uint64_t wait_limit_ns;  // bound of every pipeline wait (2 s; tests may shorten it)
   int32_t q_whole_rows;    // tm_q loads 64 whole rows per box (see tm_q)

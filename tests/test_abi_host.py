@@ -48,12 +48,17 @@ def test_workspace_size_is_bounded_and_rejects_bad_params(lib):
     assert 0 < n < 64 << 20
     big = api.make_params(512, 1, 128, 128, 7000, 16, 2000, api.KV_FP8_E4M3)
     assert lib.mla_decode_workspace_size(ctypes.byref(big), 148) < 256 << 20
-    for bad in (dict(batch=0), dict(s_q=0), dict(page_size=48), dict(kv_dtype=3), dict(causal=2),
-                dict(max_seq_len=0), dict(num_heads=0)):
+    for bad in (dict(batch=0), dict(s_q=0), dict(page_size=12), dict(page_size=1), dict(page_size=1032),
+                dict(kv_dtype=3), dict(causal=2), dict(max_seq_len=0), dict(num_heads=0)):
         q = api.make_params(2, 1, 16, 64, 10, 5, 300, api.KV_BF16)
         for k, v in bad.items():
             setattr(q, k, v)
         assert lib.mla_decode_workspace_size(ctypes.byref(q), 148) == 0, bad
+    # any multiple of 8 up to 1024 rows per page is supported (boxes of gcd(P, 64) rows)
+    for P in (8, 16, 24, 48, 1024):
+        q = api.make_params(2, 1, 16, P, 10, 5, 300, api.KV_BF16)
+        q.max_blocks_per_seq = -(-300 // P)
+        assert lib.mla_decode_workspace_size(ctypes.byref(q), 148) > 0, P
 
 
 def test_decode_rejects_null_and_misaligned_pointers_without_a_gpu(lib):

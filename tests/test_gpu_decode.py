@@ -108,6 +108,18 @@ SMALL = [
     (2, 16, 128, 64, [300, 2000], BF, True),         # 2048 rows
     (2, 8, 16, 64, [200, 700], F8, True),            # FP8, two 64-row groups
     (2, 32, 64, 128, [40, 600], F8, True),           # FP8, 2048 rows
+    # pages smaller than a 64-key block (boxes of gcd(P, 64) rows, several pages per block)
+    (2, 1, 16, 16, [100, 257], BF, True),
+    (3, 1, 16, 8, [1, 9, 300], BF, True),
+    (2, 1, 32, 24, [200, 129], BF, True),            # P = 24: 8-row boxes
+    (2, 1, 16, 1024, [300, 2000], BF, True),         # the largest page
+    (2, 1, 16, 32, [100, 257], F8, True),
+    (2, 1, 16, 48, [95, 700], F8, True),             # P = 48: 16-row boxes
+    (2, 1, 64, 16, [500, 129], F8, True),
+    (2, 4, 128, 32, [1000, 67], F8, True),
+    (3, 1, 128, 16, [1, 255, 513], BF, True),        # CTA pairs
+    (2, 1, 128, 8, [77, 1000], BF, True),
+    (2, 1, 128, 48, [300, 70], BF, True),
 ]
 
 
@@ -192,10 +204,14 @@ def test_profile_window_times_the_decode_kernels_and_changes_nothing():
     assert api.profile_end() == (0.0, 0)          # the window is closed
 
 
-def test_out_of_range_block_table_entry_is_reported_not_faulted():
-    case = synth.make_case(B=2, s_q=1, H=16, page_size=64, seq_lens=[100, 200], seed=45)
+@pytest.mark.parametrize("H,P,kv,entry", [
+    (16, 64, BF, (1, 2)), (16, 64, F8, (1, 2)), (128, 64, BF, (1, 2)), (64, 64, F8, (1, 2)),
+    (16, 16, BF, (1, 9)), (16, 16, F8, (1, 9)), (128, 16, BF, (1, 9)),   # not a block's first page
+])
+def test_out_of_range_block_table_entry_is_reported_not_faulted(H, P, kv, entry):
+    case = synth.make_case(B=2, s_q=1, H=H, page_size=P, seq_lens=[100, 200], seed=45, kv_dtype=kv)
     g = GpuCase(case)
-    g.block_table[1, 2] = case.num_pages + 7
+    g.block_table[entry] = case.num_pages + 7
     g.decode()
     st, bits = api.decode_check(g.workspace)
     assert st == -6
