@@ -314,6 +314,12 @@ static mla_status decode_impl(const mla_decode_params* p, const void* q, const v
   ca.w_slots = fw.num > 0 ? fw.slots : nullptr;
   ca.w_n = fw.num;
   ca.w_total_slots = (int64_t)p->num_pages * p->page_size;
+  ca.block_table = block_table;
+  ca.batch_info = batch_info;
+  ca.B = p->batch;
+  ca.MB = p->max_blocks_per_seq;
+  ca.P = p->page_size;
+  ca.num_pages = p->num_pages;
   ca.split_list = split_list;
   ca.part_o = po;
   ca.part_lse = plse;

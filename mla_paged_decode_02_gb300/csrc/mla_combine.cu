@@ -10,7 +10,9 @@
 // has `pieces` consecutive partial slots of RC rows. One warp per (cut stream, row):
 // lane l owns output columns [16l, 16l+16), read as four float4 per piece (coalesced
 // 2 KB rows). Persistent grid-stride loop over the list the scheduler wrote, so nothing
-// launches per sequence.
+// launches per sequence. The kernel also checks, for the whole call, the block-table
+// entries the decode read and the slots of a fused cache write (the error word was cleared
+// by the scheduler, which ran before it).
 #include "mla_internal.h"
 #include "mla_ptx.cuh"
 #include "../../include/mla.h"
@@ -19,10 +21,19 @@ namespace mla {
 
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   const int lane = threadIdx.x & 31;
-  // a fused cache write skipped slots outside the pool: report them (the error word was
-  // cleared by the scheduler, which ran before this kernel)
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < a.w_n; i += (int64_t)gridDim.x * blockDim.x)
+  // a fused cache write skipped slots outside the pool: report them
+  const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, gstride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = gtid; i < a.w_n; i += gstride)
     if (a.w_slots[i] >= a.w_total_slots) atomicOr(a.err, MLA_DEVERR_SLOT);
+  // block-table entries the decode read (the pages of each sequence up to its clamped
+  // length) that lie outside the pool: the decode kernels read page 0 for them
+  for (int64_t i = gtid; i < (int64_t)a.B * a.MB; i += gstride) {
+    const int b = (int)(i / a.MB), j = (int)(i - (int64_t)b * a.MB);
+    if ((int64_t)j * a.P < a.batch_info[b].z) {
+      const int pg = a.block_table[i];
+      if (pg < 0 || pg >= a.num_pages) atomicOr(a.err, MLA_DEVERR_BLOCK_TABLE);
+    }
+  }
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t tasks = (int64_t)a.hdr[2] * a.RC;

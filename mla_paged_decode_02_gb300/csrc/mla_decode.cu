@@ -174,8 +174,8 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 // Walks the key tiles of this CTA's units in the order every role consumes them, with
 // per 64-key block h of the current tile the cache row of its first box (rb_h, -1 for a
 // block wholly past the sequence end) and the number of its boxes that are loaded (nb_h;
-// mla_pages.cuh). A block-table entry outside the pool is flagged in the error word and
-// page 0 is read instead.
+// mla_pages.cuh). A block-table entry outside the pool reads page 0 instead (the combine
+// kernel reports it).
 struct TileIter {
   int u;
   Unit U;
@@ -185,46 +185,52 @@ struct TileIter {
   __device__ __forceinline__ uint32_t boxes() const { return (uint32_t)(nb0 + nb1); }
 };
 
-__device__ __forceinline__ void iter_rows(TileIter& it, const DecodeArgs& a, uint32_t* err,
-                                          bool report) {
+// kSub: pages smaller than 64 rows (boxes of a.box_rows rows), else one box per block.
+template <bool kSub>
+__device__ __forceinline__ void iter_rows(TileIter& it, const DecodeArgs& a) {
   const int32_t* bt = a.block_table + (int64_t)it.U.b * a.MB;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int tok = it.tile * kTileTokens + 64 * h;
-    const int64_t r = tok < it.U.L ? page_row(bt, tok, a, err, report) : -1;
-    const int nb = block_boxes(it.U.L - tok, a.box_rows);
+    const int64_t r = tok < it.U.L ? page_row(bt, tok, a) : -1;
+    const int nb = kSub ? block_boxes(it.U.L - tok, a.box_rows) : (tok < it.U.L ? 1 : 0);
     if (h == 0) { it.rb0 = r; it.nb0 = nb; }
     else { it.rb1 = r; it.nb1 = nb; }
   }
 }
 
-// Issues the boxes of block h of the iterator's tile: issue(k, group) for box k.
-template <class F>
-__device__ __forceinline__ void issue_half(const TileIter& it, const DecodeArgs& a, uint32_t* err, int h, F&& issue) {
+// Loads block h of the iterator's tile (chunks from `chunk`): its boxes land at dst,
+// dst + box_bytes, ... and complete on `bar`.
+template <bool kSub>
+__device__ __forceinline__ void load_half(const TileIter& it, const DecodeArgs& a, int h,
+                                          const CUtensorMap* map, uint32_t dst, uint32_t bar, int32_t chunk,
+                                          uint32_t box_bytes) {
   const int nb = h == 0 ? it.nb0 : it.nb1;
   if (nb == 0) return;
-  issue_block(a.block_table + (int64_t)it.U.b * a.MB, a, err, it.tile * kTileTokens + 64 * h,
-              h == 0 ? it.rb0 : it.rb1, nb, issue);
+  tma_load_4d(dst, map, bar, 0, 0, chunk, (int32_t)((h == 0 ? it.rb0 : it.rb1) >> 3));
+  if (kSub && nb > 1)
+    load_more_boxes(kBoxPlain, map, dst, bar, chunk, box_bytes, a.block_table + (int64_t)it.U.b * a.MB, a,
+                    it.tile * kTileTokens + 64 * h, nb, 0);
 }
 
-__device__ __forceinline__ bool iter_begin(TileIter& it, const DecodeArgs& a, int u0, int u1,
-                                           uint32_t* err, bool report) {
+template <bool kSub>
+__device__ __forceinline__ bool iter_begin(TileIter& it, const DecodeArgs& a, int u0, int u1) {
   it.u = u0;
   if (it.u >= u1) return false;
   it.U = load_unit(a, it.u);
   it.tile = it.U.tb;
-  iter_rows(it, a, err, report);
+  iter_rows<kSub>(it, a);
   return true;
 }
 
-__device__ __forceinline__ bool iter_next(TileIter& it, const DecodeArgs& a, int u1,
-                                          uint32_t* err, bool report) {
+template <bool kSub>
+__device__ __forceinline__ bool iter_next(TileIter& it, const DecodeArgs& a, int u1) {
   if (++it.tile == it.U.te) {
     if (++it.u >= u1) return false;
     it.U = load_unit(a, it.u);
     it.tile = it.U.tb;
   }
-  iter_rows(it, a, err, report);
+  iter_rows<kSub>(it, a);
   return true;
 }
 
@@ -268,7 +274,7 @@ __device__ __forceinline__ void convert_value_pair(const uint8_t* src, uint8_t* 
   }
 }
 
-template <int RC, bool FP8>
+template <int RC, bool FP8, bool kSub>
 __global__ void __launch_bounds__(Cfg<RC, FP8>::kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeArgs a) {
   using C = Cfg<RC, FP8>;
@@ -321,6 +327,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const uint32_t b_never = smem_u32(&bar_never);   // tests: a barrier nothing arrives on
   volatile uint32_t* abort_flag = &abort_s;
   uint32_t* err = a.err;
+  const uint32_t box_rows = kSub ? (uint32_t)a.box_rows : 64u;   // rows of one key/value box
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NK; ++i) {
@@ -390,10 +397,10 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     // are masked).
     if (lane == 0) {
       TileIter it;
-      bool more = iter_begin(it, a, u0, u1, err, true);
+      bool more = iter_begin<kSub>(it, a, u0, u1);
       bool ok = true;
       uint32_t p = 0;
-      const uint32_t box_bytes = (C::kKSlotBytes / 128) * (uint32_t)a.box_rows;
+      const uint32_t box_bytes = (C::kKSlotBytes / 128) * box_rows;
       while (more && ok) {
         for (int sl = 0; sl < C::kSlotsPerTile; ++sl, ++p) {
           const uint32_t slot = p % NK;
@@ -402,11 +409,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           const uint32_t bar = b_kfull + 8 * slot, dst = sK + slot * C::kKSlotBytes;
           mbar_arrive_expect_tx(bar, it.boxes() * box_bytes);
           for (int h = 0; h < 2; ++h)
-            issue_half(it, a, err, h, [&](int k, int32_t grp) {
-              tma_load_4d(dst + h * (C::kKSlotBytes / 2) + k * box_bytes, &a.tm_k, bar, 0, 0, sl * C::KC, grp);
-            });
+            load_half<kSub>(it, a, h, &a.tm_k, dst + h * (C::kKSlotBytes / 2), bar, sl * C::KC, box_bytes);
         }
-        if (ok) more = iter_next(it, a, u1, err, true);
+        if (ok) more = iter_next<kSub>(it, a, u1);
       }
       // the last loads issued have landed before the CTA may exit
       volatile uint32_t no_abort = 0;
@@ -420,10 +425,10 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     // of the last 16-key MMA step are overwritten with zeros (the cache may hold NaN there
     // and 0 * NaN is NaN inside the MMA); rows past that step are never read.
     TileIter it;
-    bool more = iter_begin(it, a, u0, u1, err, false);
+    bool more = iter_begin<kSub>(it, a, u0, u1);
     bool ok = true;
     uint32_t p = 0, aux = 0;
-    const uint32_t box_bytes = (kVSlotBytes / 128) * (uint32_t)a.box_rows;
+    const uint32_t box_bytes = (kVSlotBytes / 128) * box_rows;
     while (more && ok) {
       const int valid = it.U.L - it.tile * kTileTokens;
       const bool tail = valid < kTileTokens;
@@ -436,9 +441,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         if (lane == 0) {
           mbar_arrive_expect_tx(bar, it.boxes() * box_bytes);
           for (int h = 0; h < 2; ++h)
-            issue_half(it, a, err, h, [&](int k, int32_t grp) {
-              tma_load_4d(dst + h * (kVSlotBytes / 2) + k * box_bytes, &a.tm_v, bar, 0, 0, 2 * j, grp);
-            });
+            load_half<kSub>(it, a, h, &a.tm_v, dst + h * (kVSlotBytes / 2), bar, 2 * j, box_bytes);
         }
         if (tail) {
           ok = wait_warp(b_vaux, aux & 1);
@@ -456,7 +459,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           if (lane == 0) mbar_arrive(b_vfull + 8 * slot);
         }
       }
-      if (ok) more = iter_next(it, a, u1, err, false);
+      if (ok) more = iter_next<kSub>(it, a, u1);
     }
     if (lane == 0) {
       volatile uint32_t no_abort = 0;
@@ -834,23 +837,21 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     const int gi = threadIdx.x - 256;                   // 0..127 = key row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(warp & 3) << 21);   // (32 * (warp % 4)) << 16
     TileIter kc, ki;                                    // consume / issue cursors
-    bool kmore = iter_begin(kc, a, u0, u1, err, false);
-    bool kimore = gi == 0 && iter_begin(ki, a, u0, u1, err, false);
+    bool kmore = iter_begin<kSub>(kc, a, u0, u1);
+    bool kimore = gi == 0 && iter_begin<kSub>(ki, a, u0, u1);
     // raw stages: kip issued, kfreed read by every thread (free again), kwaited landed
     int kic = 0;
     uint32_t kip = 0, kcp = 0, uq = 0, kfreed = 0, kwaited = 0;
     auto top_up = [&]() {
       while (kimore && kip < kfreed + NKS) {
         const uint32_t sl = kip % NKS, bar = b_kstage + 8 * sl, dst = sKS + sl * C::kKStageBytes;
-        const uint32_t box_bytes = (C::kKStageBytes / 128) * (uint32_t)a.box_rows;
+        const uint32_t box_bytes = (C::kKStageBytes / 128) * box_rows;
         // a whole-row stage (all 9 chunks) or the KC chunks of one position
         const int32_t c0 = C::kRawRows ? 0 : kic * C::KC;
         mbar_arrive_expect_tx(bar, ki.boxes() * box_bytes);
         for (int h = 0; h < 2; ++h)
-          issue_half(ki, a, err, h, [&](int k, int32_t grp) {
-            tma_load_4d(dst + h * (C::kKStageBytes / 2) + k * box_bytes, &a.tm_k, bar, 0, 0, c0, grp);
-          });
-        if (C::kRawRows || ++kic == C::kSlotsPerTile) { kic = 0; kimore = iter_next(ki, a, u1, err, false); }
+          load_half<kSub>(ki, a, h, &a.tm_k, dst + h * (C::kKStageBytes / 2), bar, c0, box_bytes);
+        if (C::kRawRows || ++kic == C::kSlotsPerTile) { kic = 0; kimore = iter_next<kSub>(ki, a, u1); }
         ++kip;
       }
     };
@@ -937,7 +938,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           if (gi == 0) top_up();
         }
       }
-      if (ok) kmore = iter_next(kc, a, u1, err, false);
+      if (ok) kmore = iter_next<kSub>(kc, a, u1);
     }
     if (gi == 0) {
       volatile uint32_t no_abort = 0;
@@ -954,10 +955,10 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     // two slots that would put the raw load's latency behind the slot's release).
     if (lane == 0) {
       TileIter it;
-      bool more = iter_begin(it, a, u0, u1, err, true);   // reports bad block-table entries
+      bool more = iter_begin<kSub>(it, a, u0, u1);
       bool ok = true;
       uint32_t p = 0;
-      const uint32_t box_bytes = (C::kVStage / 128) * (uint32_t)a.box_rows;
+      const uint32_t box_bytes = (C::kVStage / 128) * box_rows;
       while (more && ok) {
         for (int j = 0; j < kPairsPerTile; j += C::kPairsPerVStage, ++p) {
           // stage p: value chunks 2j .. 2j + kVRawChunks - 1 of the tile's rows
@@ -968,11 +969,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           const uint32_t bar = b_vstage + 8 * sl, dst = sVS + sl * C::kVStage;
           mbar_arrive_expect_tx(bar, it.boxes() * box_bytes);
           for (int h = 0; h < 2; ++h)
-            issue_half(it, a, err, h, [&](int k, int32_t grp) {
-              tma_load_4d(dst + h * (C::kVStage / 2) + k * box_bytes, &a.tm_v, bar, 0, 0, 2 * j, grp);
-            });
+            load_half<kSub>(it, a, h, &a.tm_v, dst + h * (C::kVStage / 2), bar, 2 * j, box_bytes);
         }
-        if (ok) more = iter_next(it, a, u1, err, true);
+        if (ok) more = iter_next<kSub>(it, a, u1);
       }
       volatile uint32_t no_abort = 0;
       for (uint32_t q = p > (uint32_t)NVS ? p - NVS : 0; q < p; ++q)
@@ -987,17 +986,23 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   if (warp == 0) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int RC, bool FP8>
-static cudaError_t prepare_one() {
+template <int RC, bool FP8, bool kSub>
+static cudaError_t prepare_variant() {
   using C = Cfg<RC, FP8>;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<RC, FP8>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<RC, FP8, kSub>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kDynBytes);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes attr;
-  e = cudaFuncGetAttributes(&attr, decode_kernel<RC, FP8>);
+  e = cudaFuncGetAttributes(&attr, decode_kernel<RC, FP8, kSub>);
   if (e != cudaSuccess) return e;
   if ((int)attr.sharedSizeBytes > kStaticBudget) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
+}
+
+template <int RC, bool FP8>
+static cudaError_t prepare_one() {
+  const cudaError_t e = prepare_variant<RC, FP8, false>();
+  return e != cudaSuccess ? e : prepare_variant<RC, FP8, true>();
 }
 
 template <int RC, bool FP8>
@@ -1013,7 +1018,9 @@ static cudaError_t launch_one(const DecodeArgs& a, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<RC, FP8>, a);
+  // pages smaller than 64 rows take the kernel that loads a 64-key block as several boxes
+  return a.box_rows < 64 ? cudaLaunchKernelEx(&cfg, decode_kernel<RC, FP8, true>, a)
+                         : cudaLaunchKernelEx(&cfg, decode_kernel<RC, FP8, false>, a);
 }
 
 int decode_value_chunks_per_box(int rc, bool fp8) {

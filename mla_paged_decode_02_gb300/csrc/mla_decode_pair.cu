@@ -88,14 +88,15 @@ __device__ __forceinline__ PUnit load_punit(const DecodeArgs& a, int u) {
 
 // First global cache row of each 64-key block kb of super-tile `tile` (-1: past the
 // sequence end). A block-table entry outside the pool is flagged and reads page 0.
-__device__ __forceinline__ void block_rows(const DecodeArgs& a, const PUnit& U, int tile, int64_t* rb, int* nb,
-                                           uint32_t* err, bool report) {
+// kSub: pages smaller than 64 rows (boxes of a.box_rows rows), else one box per block.
+template <bool kSub>
+__device__ __forceinline__ void block_rows(const DecodeArgs& a, const PUnit& U, int tile, int64_t* rb, int* nb) {
   const int32_t* bt = a.block_table + (int64_t)U.b * a.MB;
 #pragma unroll
   for (int kb = 0; kb < 4; ++kb) {
     const int tok = tile * kPairKeys + 64 * kb;
-    rb[kb] = tok < U.L ? page_row(bt, tok, a, err, report) : -1;
-    nb[kb] = block_boxes(U.L - tok, a.box_rows);
+    rb[kb] = tok < U.L ? page_row(bt, tok, a) : -1;
+    nb[kb] = kSub ? block_boxes(U.L - tok, a.box_rows) : (tok < U.L ? 1 : 0);
   }
 }
 
@@ -111,7 +112,7 @@ __device__ __forceinline__ float unordered_p(int k) { return __int_as_float(k ^ 
 
 }  // namespace
 
-template <bool FP8>
+template <bool FP8, bool kSub>
 __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ uint8_t dsmem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kRing], bar_empty[kRing], bar_aux;
@@ -219,15 +220,16 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
     // the block holding the sequence end gets the rows up to the end of its last 16-key MMA
     // step zeroed (the cache may hold NaN there, and 0 * NaN is NaN inside the MMA)
     const int32_t* bt_all = a.block_table;
-    const uint32_t kbox_bytes = (kSlotBytes / 128) * (uint32_t)a.box_rows;   // one key box
-    const uint32_t vbox_bytes = (kSlotBytes / 64) * (uint32_t)a.box_rows;    // one value box
+    const uint32_t box_rows = kSub ? (uint32_t)a.box_rows : 64u;             // rows of one box
+    const uint32_t kbox_bytes = (kSlotBytes / 128) * box_rows;               // one key box
+    const uint32_t vbox_bytes = (kSlotBytes / 64) * box_rows;                // one value box
     auto load_values = [&](const PUnit& U, int tile, const int64_t* rb, const int* nb) -> bool {
       const int32_t* bt = bt_all + (int64_t)U.b * a.MB;
       for (int kb = 0; kb < 4; ++kb) {
         if (rb[kb] < 0) continue;
         const int valid = U.L - tile * kPairKeys - 64 * kb;
         // a block not loaded whole (boxes past the sequence end) completes its bytes itself
-        const bool zero = valid < 64 && ((valid & 15) != 0 || nb[kb] < 64 / a.box_rows);
+        const bool zero = valid < 64 && ((valid & 15) != 0 || (kSub && nb[kb] < (int)(64 / box_rows)));
         const int tok0 = tile * kPairKeys + 64 * kb;
         const uint32_t slot = r % kRing;
         bool w_ok = lane != 0 || wait(b_empty + 8 * slot, ((r / kRing) & 1) ^ 1);
@@ -236,16 +238,17 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
         const int32_t c0 = 4 * (int)rank;            // this CTA's value columns 256 rank ..
         if (leader && lane == 0) mbar_arrive_expect_tx(b_full + 8 * slot, 2 * kSlotBytes);
         if (!zero) {
-          if (lane == 0)
-            issue_block(bt, a, err, tok0, rb[kb], nb[kb], [&](int k, int32_t grp) {
-              tma_load_4d_pair_hint(dst + k * vbox_bytes, &a.tm_v, lb, 0, 0, c0, grp, pol_last);
-            });
+          if (lane == 0) {
+            tma_load_4d_pair_hint(dst, &a.tm_v, lb, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
+            if (kSub && nb[kb] > 1)
+              load_more_boxes(kBoxPairHint, &a.tm_v, dst, lb, c0, vbox_bytes, bt, a, tok0, nb[kb], pol_last);
+          }
         } else {
           if (lane == 0) {
-            mbar_arrive_expect_tx(b_aux, (uint32_t)nb[kb] * vbox_bytes);
-            issue_block(bt, a, err, tok0, rb[kb], nb[kb], [&](int k, int32_t grp) {
-              tma_load_4d_hint(dst + k * vbox_bytes, &a.tm_v, b_aux, 0, 0, c0, grp, pol_last);
-            });
+            mbar_arrive_expect_tx(b_aux, (kSub ? (uint32_t)nb[kb] : 1u) * vbox_bytes);
+            tma_load_4d_hint(dst, &a.tm_v, b_aux, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
+            if (kSub && nb[kb] > 1)
+              load_more_boxes(kBoxHint, &a.tm_v, dst, b_aux, c0, vbox_bytes, bt, a, tok0, nb[kb], pol_last);
           }
           w_ok = wait(b_aux, aux & 1);
           ++aux;
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       for (int tile = U.tb; tile < U.te && ok; ++tile) {
         int64_t rb[4];
         int nb[4];
-        block_rows(a, U, tile, rb, nb, err, leader);
+        block_rows<kSub>(a, U, tile, rb, nb);
         const int32_t* bt = bt_all + (int64_t)U.b * a.MB;
         // bytes of both CTAs' key halves (the even CTA arms the barrier for both)
         const uint32_t nbox = (uint32_t)(nb[0] + nb[1] + nb[2] + nb[3]);
@@ -308,11 +311,12 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
             if (leader) mbar_arrive_expect_tx(b_full + 8 * slot, nbox * kbox_bytes);
             for (int h = 0; h < 2; ++h) {
               const int kb = 2 * (int)rank + h;
-              if (nb[kb] > 0)
-                issue_block(bt, a, err, tile * kPairKeys + 64 * kb, rb[kb], nb[kb], [&](int k, int32_t grp) {
-                  tma_load_4d_pair_hint(dst + h * (kSlotBytes / 2) + k * kbox_bytes, &a.tm_k, lb, 0, 0, 2 * ks, grp,
-                                        pol_keep);
-                });
+              if (nb[kb] == 0) continue;
+              const uint32_t d = dst + h * (kSlotBytes / 2);
+              tma_load_4d_pair_hint(d, &a.tm_k, lb, 0, 0, 2 * ks, (int32_t)(rb[kb] >> 3), pol_keep);
+              if (kSub && nb[kb] > 1)
+                load_more_boxes(kBoxPairHint, &a.tm_k, d, lb, 2 * ks, kbox_bytes, bt, a, tile * kPairKeys + 64 * kb,
+                                nb[kb], pol_keep);
             }
           }
           ++r;
@@ -691,16 +695,22 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
   if (warp == 0) tmem_dealloc_pair(tmem, kPairTmemCols);
 }
 
-cudaError_t decode_pair_prepare(bool fp8) {
-  if (fp8) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <bool kSub>
+static cudaError_t prepare_pair_variant() {
+  cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<false, kSub>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kPairDynBytes);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes attr;
-  e = cudaFuncGetAttributes(&attr, decode_pair_kernel<false>);
+  e = cudaFuncGetAttributes(&attr, decode_pair_kernel<false, kSub>);
   if (e != cudaSuccess) return e;
   if ((int)attr.sharedSizeBytes > kPairStaticBudget) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
+}
+
+cudaError_t decode_pair_prepare(bool fp8) {
+  if (fp8) return cudaErrorInvalidValue;
+  const cudaError_t e = prepare_pair_variant<false>();
+  return e != cudaSuccess ? e : prepare_pair_variant<true>();
 }
 
 cudaError_t launch_decode_pair(const DecodeArgs& a, bool fp8, int pairs, cudaStream_t s) {
@@ -719,7 +729,9 @@ cudaError_t launch_decode_pair(const DecodeArgs& a, bool fp8, int pairs, cudaStr
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, decode_pair_kernel<false>, a);
+  // pages smaller than 64 rows take the kernel that loads a 64-key block as several boxes
+  return a.box_rows < 64 ? cudaLaunchKernelEx(&cfg, decode_pair_kernel<false, true>, a)
+                         : cudaLaunchKernelEx(&cfg, decode_pair_kernel<false, false>, a);
 }
 
 }  // namespace mla

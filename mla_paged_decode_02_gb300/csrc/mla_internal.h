@@ -125,6 +125,11 @@ struct CombineArgs {
   const int64_t* w_slots;  // fused cache write: its slots are checked here (w_n > 0)
   int64_t w_total_slots;
   int32_t w_n;
+  // the block-table entries the decode read are checked here: [B][MB], the first
+  // ceil(L_b / P) of row b (L_b the clamped length in batch_info[b].z)
+  const int32_t* block_table;
+  const int4* batch_info;
+  int32_t B, MB, P, num_pages;
   const int4* split_list;
   const float* part_o;
   const float* part_lse;

@@ -14,37 +14,44 @@
 #pragma once
 #include <cstdint>
 #include "mla_internal.h"
+#include "mla_ptx.cuh"
 #include "../../include/mla.h"
 
 namespace mla {
 
 // Cache row of token `tok` of the sequence whose block-table row is `bt`. An entry outside
-// the pool is reported in the error word (when `report`) and page 0 is read instead.
-__device__ __forceinline__ int64_t page_row(const int32_t* bt, int tok, const DecodeArgs& a, uint32_t* err,
-                                            bool report) {
+// the pool reads page 0 instead (the combine kernel reports it in the error word).
+__device__ __forceinline__ int64_t page_row(const int32_t* bt, int tok, const DecodeArgs& a) {
   const int pg = __ldg(bt + tok / a.P);
-  if (pg < 0 || pg >= a.num_pages) {
-    if (report) atomicOr(err, MLA_DEVERR_BLOCK_TABLE);
-    return tok % a.P;
-  }
+  if (pg < 0 || pg >= a.num_pages) return tok % a.P;
   return (int64_t)pg * a.P + tok % a.P;
 }
 
 // Boxes of the block with `valid` rows before the sequence end (<= 0: none) that are loaded.
+// box_rows is a power of two (a divisor of 64).
 __device__ __forceinline__ int block_boxes(int valid, int box_rows) {
   if (valid <= 0) return 0;
-  const int n = (valid + box_rows - 1) / box_rows, per = 64 / box_rows;
+  const int sh = 31 - __clz(box_rows);
+  const int n = (valid + box_rows - 1) >> sh, per = 64 >> sh;
   return n < per ? n : per;
 }
 
-// Issues the `nbox` boxes of the block starting at token `tok0` whose first box starts at
-// cache row `row0`: issue(k, first 8-row group of box k). Boxes after the first look their
-// page up again (and report a bad entry).
-template <class F>
-__device__ __forceinline__ void issue_block(const int32_t* bt, const DecodeArgs& a, uint32_t* err, int tok0,
-                                            int64_t row0, int nbox, F&& issue) {
-  issue(0, (int32_t)(row0 >> 3));
-  for (int k = 1; k < nbox; ++k) issue(k, (int32_t)(page_row(bt, tok0 + k * a.box_rows, a, err, true) >> 3));
+enum BoxLoad { kBoxPlain = 0, kBoxHint = 1, kBoxPairHint = 2 };
+
+// Boxes 1 .. nb - 1 of the block starting at token tok0 (pages smaller than 64 rows), each
+// looking its page up. Box k lands at dst + k * box_bytes, with
+// the mbarrier and the TMA form of box 0. Kept out of line, so that the usual case (one box
+// per block) stays small in the instruction cache that a CTA's roles share.
+static __device__ __noinline__ void load_more_boxes(int form, const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                             int32_t chunk, uint32_t box_bytes, const int32_t* bt,
+                                             const DecodeArgs& a, int tok0, int nb, uint64_t pol) {
+  for (int k = 1; k < nb; ++k) {
+    const int32_t grp = (int32_t)(page_row(bt, tok0 + k * a.box_rows, a) >> 3);
+    const uint32_t d = dst + (uint32_t)k * box_bytes;
+    if (form == kBoxPairHint) tma_load_4d_pair_hint(d, map, bar, 0, 0, chunk, grp, pol);
+    else if (form == kBoxHint) tma_load_4d_hint(d, map, bar, 0, 0, chunk, grp, pol);
+    else tma_load_4d(d, map, bar, 0, 0, chunk, grp);
+  }
 }
 
 }  // namespace mla
