@@ -31,14 +31,15 @@
 // peer's shared memory). At the end of a unit the row sums are exchanged the same way.
 //
 // Pipeline per CTA (384 threads). Warp 0: producer — one ring of 32 KB slots in the order
-// the MMAs consume them (the 5 key slots of tile n, then the 4 value slots of tile n-1), plus
-// each unit's Q. A TMA load's cost grows with the number of contiguous row pieces in its
+// the MMAs consume them (the 5 key slots of tile n, then the value slots of tile n-1; a
+// unit's last value slots right after its last key slots), plus each unit's Q. A TMA load's cost grows with the number of contiguous row pieces in its
 // box (measured on this GPU: about 22 GB/s per SM for 128-byte pieces from L2, 44 for 256,
 // 87 for 512), so key boxes take two adjacent 64-column chunks of each row and value boxes
 // four. Every load completes on the even CTA's barrier, which the even CTA alone arms with
 // the bytes of both CTAs (it knows which key halves its peer loads), so that no load needs a
 // cross-CTA arrival (each costs a fraction of a microsecond). Warp 1 of the even CTA: the
-// single MMA issuer, in program order QK^T(n), PV(n-1), QK^T(n+1), ...; its commits arrive
+// single MMA issuer, in program order QK^T(n), PV(n-1), QK^T(n+1), ..., a unit's last PV
+// before the next unit's first QK^T (so that the epilogue need not wait for it); its commits arrive
 // on the barrier at the same offset in both CTAs. Warps 4-7 and 8-11: softmax warpgroups 0
 // and 1, then the epilogue. Every wait is bounded; a stall sets the device error word, and
 // both CTAs drain and leave through a final cluster barrier.
@@ -209,8 +210,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
   if (warp == 0) {
     // ================================================================ producer
     // Ring order per super-tile n: its 5 key slots (chunk pairs 0-1, 2-3, 4-5, 6-7 and 8,
-    // 128 keys each), then the 4 value slots of tile n-1 (64 keys x this CTA's 256 value
-    // columns each). TMA cost grows with the number of contiguous row pieces a box has, not
+    // 128 keys each), then the value slots of tile n-1 (64 keys x this CTA's 256 value
+    // columns each, one per 64-key block before the sequence end); a unit's last value
+    // slots follow its last key slots. TMA cost grows with the number of contiguous row pieces a box has, not
     // with its bytes, so every box takes 2 (keys) or 4 (values) adjacent chunks of a row.
     uint32_t r = 0, uq = 0, aux = 0;
     bool ok = true;
@@ -327,8 +329,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
         ptile = tile;
         for (int kb = 0; kb < 4; ++kb) { prb[kb] = rb[kb]; pnb[kb] = nb[kb]; }
       }
+      // the unit's last value slots before the next unit's Q and keys (the MMA issuer takes
+      // the unit's last PV before the next unit's first QK^T)
+      if (ok && ptile >= 0) ok = load_values(pu, ptile, prb, pnb);
+      ptile = -1;
     }
-    if (ok && ptile >= 0) ok = load_values(pu, ptile, prb, pnb);
     // after an abort the odd CTA cannot observe its own loads (they count on the even CTA's
     // barrier, whose phase may never complete): both producers wait 50 us, far longer than
     // a load takes, before leaving
@@ -416,8 +421,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
           if (prev.tile >= 0) ok = issue_pv(prev);
           prev = Prev{U.L, U.tb + k, k == 0, uc};
         }
+        // the unit's last PV before the next unit's first QK^T: the epilogue waits for it,
+        // while the next unit's QK^T can run during the epilogue
+        if (ok && prev.tile >= 0) ok = issue_pv(prev);
+        prev.tile = -1;
       }
-      if (ok && prev.tile >= 0) ok = issue_pv(prev);
       // every MMA issued has completed before tensor memory is released
       umma_pair_commit(b_drain);
       volatile uint32_t no_abort = 0;
@@ -647,10 +655,20 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       }
       named_bar_sync(bar, 128);
       const bool direct = U.slot < 0;
-      // this thread's value column in M-tile jt is 256 rank + 128 jt + t; rows 64 wg + r
+      // Each warp holds value columns 256 rank + 128 jt + 32 wl + lane (its TMEM lanes) of 16
+      // rows per load. It transposes them through 2 KB of shared memory, 16-byte blocks
+      // XOR-swizzled by row, so that each lane stores 16 consecutive columns of one row
+      // (16-byte stores instead of one store per row and column). The scratch is this CTA's
+      // own half of the P^T buffer for the warpgroup whose rows live here (no other agent
+      // writes it before this warpgroup's next P^T), else the staging buffer once its last
+      // copy to the peer has been read.
+      if (!local_p) {
+        if (t == 0) bulk_wait_read0();
+        named_bar_sync(bar, 128);
+      }
+      float* stage = reinterpret_cast<float*>(local_p ? gP + (int)rank * kStageBytes : gStage) + wl * 512;
       const int nrows = min(64, R - row0);         // rows of this warpgroup that exist
-      __nv_bfloat16* obase = a.out + ((int64_t)U.b * R + row0) * kDV + 256 * (int)rank + t;
-      float* pbase = a.part_o + ((int64_t)U.slot * 128 + 64 * wg) * kDV + 256 * (int)rank + t;
+      const int si = lane >> 1, sh = lane & 1;
 #pragma unroll 1
       for (int jt = 0; jt < 2; ++jt) {
 #pragma unroll 1
@@ -665,12 +683,36 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
             if (leader && t == 0) mbar_arrive(b_oempty);
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int r = 16 * c + i;
-            const float v = o[i] * alpha_s[wg][r];
-            if (r < nrows) {
-              if (direct) obase[r * kDV + 128 * jt] = __float2bfloat16_rn(v);
-              else pbase[r * kDV + 128 * jt] = v;
+          for (int i = 0; i < 16; ++i)
+            stage[i * 32 + ((((lane >> 2) ^ (i & 7)) << 2) | (lane & 3))] = o[i] * alpha_s[wg][16 * c + i];
+          __syncwarp();
+          float v[16];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float4 x = *reinterpret_cast<const float4*>(stage + si * 32 + (((4 * sh + m) ^ (si & 7)) << 2));
+            v[4 * m] = x.x;
+            v[4 * m + 1] = x.y;
+            v[4 * m + 2] = x.z;
+            v[4 * m + 3] = x.w;
+          }
+          __syncwarp();
+          const int r = 16 * c + si;               // row 64 wg + r of the unit
+          const int col = 256 * (int)rank + 128 * jt + 32 * wl + 16 * sh;
+          if (r < nrows) {
+            if (direct) {
+              uint32_t w[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+                w[k] = *reinterpret_cast<uint32_t*>(&h);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)U.b * R + row0 + r) * kDV + col);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+              float4* dst = reinterpret_cast<float4*>(a.part_o + ((int64_t)U.slot * 128 + 64 * wg + r) * kDV + col);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) dst[m] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
             }
           }
         }
