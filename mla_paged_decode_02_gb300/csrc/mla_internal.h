@@ -21,17 +21,17 @@ constexpr int kMaxFusedWriteTokens = 1 << 17;   // new tokens the scheduler's la
 
 // Execution plan for the s_q * H query rows of a sequence. Rows are processed in groups
 // of RC rows (the N of every MMA). Up to 64 rows: one CTA per SM, RC = 16/32/64, 128-key
-// tiles. More than 64 rows with a bf16 cache: CTA pairs (a cluster of two CTAs on two
-// SMs) with RC = 128 and 256-key tiles, each CTA holding 128 of the keys and 64 of the
-// rows, so that every key tile is read once for 128 rows. The schedule's workers are
-// SMs or CTA pairs.
+// tiles. More than 64 rows: CTA pairs (a cluster of two CTAs on two SMs) with RC = 128
+// and 256-key tiles, each CTA holding 128 of the keys and 64 of the rows, so that every
+// key tile is read (and, with the FP8 cache, converted) once for 128 rows. The schedule's
+// workers are SMs or CTA pairs. The plan is the same for both cache types.
 struct Plan {
   int rc, G, tile;
   bool pair;
 };
-inline Plan make_plan(int rows, bool fp8) {
+inline Plan make_plan(int rows, bool /*fp8*/) {
   Plan p;
-  p.pair = rows > 64 && !fp8;
+  p.pair = rows > 64;
   p.rc = p.pair ? 128 : rows <= 16 ? 16 : rows <= 32 ? 32 : 64;
   p.G = (rows + p.rc - 1) / p.rc;
   p.tile = p.pair ? 2 * kTileTokens : kTileTokens;

@@ -424,15 +424,6 @@ __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_
 }  // namespace mla
 
 namespace mla {
-// Brings `bytes` (a multiple of 16) of global memory at `p` into L2, with no destination in
-// shared memory; used to start a later tile's DRAM reads early.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
-               : "memory");
-}
-}  // namespace mla
-
-namespace mla {
 // L2 eviction policies for TMA loads (createpolicy): lines a later load will read again
 // are kept (evict_last), lines read for the last time go first (evict_first).
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
@@ -486,5 +477,38 @@ __device__ __forceinline__ void tma_load_5d_pair_hint(uint32_t dst, const CUtens
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
          "l"(policy)
       : "memory");
+}
+}  // namespace mla
+
+namespace mla {
+// This CTA's own TMA loads with an L2 hint (completing on its own barrier), 3-D and 5-D.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0,
+                                                 int32_t c1, int32_t c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t c0,
+                                                 int32_t c1, int32_t c2, int32_t c3, int32_t c4, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+         "l"(policy)
+      : "memory");
+}
+
+// Per-warpgroup register budgets (every warp of a warpgroup executes the same one): the
+// launch allocation is redistributed, so the budgets of all warpgroups must add up to no
+// more than it.
+template <int N>
+__device__ __forceinline__ void regs_raise() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_lower() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(N));
 }
 }  // namespace mla

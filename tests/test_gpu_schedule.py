@@ -3,8 +3,8 @@
 The scheduler lays the (row group, sequence) streams of key tiles end to end and gives
 CTA c the positions [c q, (c + 1) q), q = ceil(W / grid); when the G row groups divide the
 grid, each group gets grid / G CTAs and the same partition of its N tiles instead
-(q = ceil(N / (grid / G))). With more than 64 rows and a bf16 cache the workers are CTA
-pairs (grid = #SM / 2), a row group is 128 rows and a tile 256 keys. Checked here on the device's own output: every tile of every
+(q = ceil(N / (grid / G))). With more than 64 rows the workers are CTA pairs
+(grid = #SM / 2), a row group is 128 rows and a tile 256 keys. Checked here on the device's own output: every tile of every
 stream is covered exactly once, every CTA's units are a contiguous range holding exactly
 its share of tiles, and only streams cut by a CTA boundary get partial slots (consecutive
 ones). The workspace offsets below restate the
@@ -28,7 +28,7 @@ def _cuda():
 
 
 def _plan(R, nsm):
-    """(rows per group, keys per tile, schedule workers) for R rows and a bf16 cache."""
+    """(rows per group, keys per tile, schedule workers) for R rows (either cache type)."""
     if R > 64:
         return 128, 256, nsm // 2
     return (16 if R <= 16 else 32 if R <= 32 else 64), 128, nsm
