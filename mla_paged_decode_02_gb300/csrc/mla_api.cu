@@ -272,9 +272,8 @@ static mla_status decode_impl(const mla_decode_params* p, const void* q, const v
     // chunks per key / value box: a pair loads 2 / 4 adjacent chunks of each row
     const uint32_t kc = plan.pair ? 2u : (uint32_t)decode_key_chunks_per_slot(rc, fp8);
     const uint32_t vc = plan.pair ? 4u : (uint32_t)decode_value_chunks_per_box(rc, fp8);
-    // E4M3 keys: 64-byte swizzled for the single-CTA kernel's converting threads; CTA pairs
-    // convert linear raw slots
-    if (!encode_kv_map(&da.tm_k, kv_cache, rows, kc, (uint32_t)box_rows, fp8, !plan.pair) ||
+    // E4M3 keys are 64-byte swizzled: the converting threads read one row each
+    if (!encode_kv_map(&da.tm_k, kv_cache, rows, kc, (uint32_t)box_rows, fp8, true) ||
         !encode_kv_map(&da.tm_v, kv_cache, rows, vc, (uint32_t)box_rows, fp8, false))
       return MLA_ERR_INVALID_ARG;
   }

@@ -70,11 +70,14 @@ constexpr float kPLn2 = 0.6931471805599453f;
 constexpr int kPairSmemLimit = 232448;
 constexpr int kPairStaticBudget = 9216;
 
-// bf16: 384 threads; a ring of three 32 KB operand slots filled by TMA, and a 16 KB
-// staging buffer for the P^T rows sent to the peer by one bulk copy.
-// FP8: 512 threads (a fourth warpgroup converts E4M3 to fp16); a ring of two 32 KB fp16
-// operand slots filled by the converters from a ring of three 16 KB raw E4M3 slots filled
-// by TMA; P^T rows for the peer go by st.async (no staging buffer).
+// bf16: 384 threads; a ring of three 32 KB operand slots (keys and values) filled by TMA,
+// and a 16 KB staging buffer for the P^T rows sent to the peer by one bulk copy; S^T
+// double-buffered in tensor memory.
+// FP8: 512 threads (a fourth warpgroup converts E4M3 to fp16); keys go to two tensor-memory
+// key slots (the QK^T MMAs read A from tensor memory), values to a ring of two 32 KB fp16
+// slots, both from a ring of three 16 KB raw E4M3 slots filled by TMA; S^T single-buffered
+// (its second buffer's columns hold the key slots); P^T rows for the peer go by st.async
+// (no staging buffer).
 template <bool FP8>
 struct PairCfg {
   static constexpr int kThreads = FP8 ? 512 : 384;
@@ -86,6 +89,8 @@ struct PairCfg {
   static_assert(kRing <= kMaxRing && kRawRing <= kMaxRing, "barrier arrays");
   static_assert(kDynBytes + kPairStaticBudget <= kPairSmemLimit, "shared memory budget");
 };
+constexpr int kKeyTSlots = 2;               // FP8: tensor-memory key slots (two chunks = 64 columns each)
+constexpr int kKeyCol = 128;                // FP8: their first column
 // FP8 register budgets per thread (setmaxnreg): warpgroup 0 (producer, MMA issuer), the two
 // softmax warpgroups, the converters. They redistribute the launch allocation of 128.
 constexpr int kRegsCtl = 96, kRegsSoftmax = 176, kRegsConv = 64;
@@ -143,6 +148,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
   __shared__ __align__(8) uint64_t bar_qfull, bar_qempty;
   // FP8: raw ring, Q landed (this CTA), Q converted (both CTAs, on the even CTA)
   __shared__ __align__(8) uint64_t bar_rfull[kMaxRing], bar_rempty[kMaxRing], bar_qraw, bar_qready;
+  __shared__ __align__(8) uint64_t bar_kfull[kKeyTSlots], bar_kempty[kKeyTSlots];   // FP8 key slots
   __shared__ __align__(16) uint32_t sig_s[4];        // landing place of the odd CTA's 16-byte signals
   __shared__ __align__(8) uint64_t bar_sfull[2], bar_sempty[2], bar_pfull, bar_pin, bar_pvdone, bar_oempty;
   __shared__ __align__(8) uint64_t bar_x[2][2];
@@ -183,6 +189,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
   const uint32_t b_never = smem_u32(&bar_never);   // tests: a barrier nothing arrives on
   const uint32_t b_rfull = smem_u32(bar_rfull), b_rempty = smem_u32(bar_rempty);
   const uint32_t b_qraw = smem_u32(&bar_qraw), b_qready = smem_u32(&bar_qready);
+  const uint32_t b_kfull = smem_u32(bar_kfull), b_kempty = smem_u32(bar_kempty);
   volatile uint32_t* abort_flag = &abort_s;
   uint32_t* err = a.err;
 
@@ -199,6 +206,10 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
     }
     mbar_init(b_qraw, 1);
     mbar_init(b_qready, 1);               // as b_full (FP8)
+    for (int i = 0; i < kKeyTSlots; ++i) {
+      mbar_init(b_kfull + 8 * i, 1);      // as b_full (FP8)
+      mbar_init(b_kempty + 8 * i, 1);
+    }
     mbar_init(b_aux, 1);
     mbar_init(b_qfull, 1);                // the even CTA's arrival, with both CTAs' bytes
     mbar_init(b_qempty, 1);
@@ -512,7 +523,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         // value slot [8 groups][4 chunks][8 rows][128 B]: MN-major, chunks 1 KB, groups 4 KB apart
         const uint64_t dV0 = make_sdesc(sR, 1024, 4096, kSwizzle128);
         const uint64_t dP0 = make_sdesc(sP, 1024, 1024, kSwizzle128);   // MN-major P^T
-        uint32_t r = 0, n = 0, uc = 0, pvn = 0;
+        uint32_t r = 0, n = 0, uc = 0, pvn = 0, kp = 0;   // kp: FP8 key positions
         bool ok = true;
         struct Prev {
           int L, tile;
@@ -548,25 +559,46 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
           const PUnit U = load_punit(a, u);
           ok = wait(FP8 ? b_qready : b_qfull, uc & 1);   // FP8: converted to fp16 in both CTAs
           for (int k = 0; k < U.te - U.tb && ok; ++k, ++n) {
-            ok = wait(b_sempty + 8 * (n & 1), ((n >> 1) & 1) ^ 1);
-            const uint32_t d = tmem + (n & 1) * 128;
-            for (int ks = 0; ks < kKeySlots && ok; ++ks, ++r) {
-              const uint32_t slot = r % kRing;
-              ok = wait(b_full + 8 * slot, (r / kRing) & 1);
-              if (!ok) break;
-              tc_fence_after();
-              const uint64_t ad = dK0 + (uint64_t)(slot * (kSlotBytes >> 4));
-              for (int cc = 0; cc < (ks == kKeySlots - 1 ? 1 : 2); ++cc) {
-                const int c = 2 * ks + cc;
-                const uint64_t bd = dQ0 + (uint64_t)(c * (q_chunk >> 4));
-  #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  umma_pair_f16(d, ad + (uint64_t)(cc * (1024 >> 4) + 2 * kk), bd + 2 * kk, idesc_qk, (c | kk) != 0);
+            // S^T buffer: two alternating (bf16), or one (FP8)
+            const uint32_t sb = FP8 ? 0u : (n & 1), sph = FP8 ? (n & 1) : ((n >> 1) & 1);
+            ok = wait(b_sempty + 8 * sb, sph ^ 1);
+            const uint32_t d = tmem + sb * 128;
+            for (int ks = 0; ks < kKeySlots && ok; ++ks) {
+              const int nc = ks == kKeySlots - 1 ? 1 : 2;     // chunks 2ks, 2ks + 1 (the last: 8)
+              if constexpr (FP8) {
+                const uint32_t kslot = kp % kKeyTSlots;
+                ok = wait(b_kfull + 8 * kslot, (kp / kKeyTSlots) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t at0 = tmem + kKeyCol + 64 * kslot;     // 32 columns per chunk
+                for (int cc = 0; cc < nc; ++cc) {
+                  const int c = 2 * ks + cc;
+                  const uint64_t bd = dQ0 + (uint64_t)(c * (q_chunk >> 4));
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    umma_pair_f16_ts(d, at0 + 32 * cc + 8 * kk, bd + 2 * kk, idesc_qk, (c | kk) != 0);
+                }
+                umma_pair_commit(b_kempty + 8 * kslot);
+                ++kp;
+              } else {
+                const uint32_t slot = r % kRing;
+                ok = wait(b_full + 8 * slot, (r / kRing) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t ad = dK0 + (uint64_t)(slot * (kSlotBytes >> 4));
+                for (int cc = 0; cc < nc; ++cc) {
+                  const int c = 2 * ks + cc;
+                  const uint64_t bd = dQ0 + (uint64_t)(c * (q_chunk >> 4));
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    umma_pair_f16(d, ad + (uint64_t)(cc * (1024 >> 4) + 2 * kk), bd + 2 * kk, idesc_qk, (c | kk) != 0);
+                }
+                umma_pair_commit(b_empty + 8 * slot);
+                ++r;
               }
-              umma_pair_commit(b_empty + 8 * slot);
             }
             if (!ok) break;
-            umma_pair_commit(b_sfull + 8 * (n & 1));
+            umma_pair_commit(b_sfull + 8 * sb);
             if (k == U.te - U.tb - 1) umma_pair_commit(b_qempty);
             if (prev.tile >= 0) ok = issue_pv(prev);
             prev = Prev{U.L, U.tb + k, k == 0, uc};
@@ -585,26 +617,73 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
   } else if (FP8 && warp >= 12) {
     if constexpr (FP8) regs_lower<kRegsConv>();
     // ================================================================ converters (FP8)
-    // Warps 12-15 take the raw slots in ring order and write each as the fp16 operand slot
-    // the MMAs read — keys [2 halves][8 groups][2 chunks][8 rows][128 B] (K-major), values
-    // [8 groups][4 chunks][8 rows][128 B] (MN-major), 128-byte swizzled as a TMA load of
-    // bf16 rows would land — with the exact hardware convert (two bytes per instruction).
-    // Value rows past the sequence end are written as zeros (the cache may hold NaN there,
-    // and 0 * NaN is NaN inside the MMA); key rows past it are masked by the softmax. Each
-    // unit's Q is converted from bf16 to fp16 in place first (a value beyond the fp16 range
-    // is flagged). The even CTA's MMA issuer needs both CTAs' halves of a slot: the even
-    // CTA's converters arrive on its barrier expecting 16 bytes, which the odd CTA's send
-    // with st.async (a remote arrival would hold the sending thread for ~0.85 us).
+    // Warps 12-15 take the raw slots in ring order, with the exact hardware convert (two
+    // bytes per instruction). Keys: thread gi converts key row gi of a key position (two
+    // chunks) into tensor-memory key slot kp % 2 at lane gi, from which the QK^T MMAs read
+    // their A operand (key rows past the sequence end are masked by the softmax). Values:
+    // the slot is written as the fp16 operand slot [8 groups][4 chunks][8 rows][128 B]
+    // (MN-major, 128-byte swizzled as a TMA load of bf16 rows would land), rows past the
+    // sequence end as zeros (the cache may hold NaN there, and 0 * NaN is NaN inside the
+    // MMA). Each unit's Q is converted from bf16 to fp16 in place first (a value beyond the
+    // fp16 range is flagged). The even CTA's MMA issuer needs both CTAs' halves of a slot:
+    // the even CTA's converters arrive on its barrier expecting 16 bytes, which the odd CTA's
+    // send with st.async (a remote arrival would hold the sending thread for ~0.85 us).
     const int gi = threadIdx.x - 384;
     constexpr uint32_t cbar = 3;                   // named barrier of the 128 converting threads
-    uint32_t rr = 0, fr = 0, uq = 0;
+    uint32_t rr = 0, fr = 0, kp = 0, uq = 0;       // raw slots, value slots, key positions, units
     bool ok = true;
     auto signal_lead = [&](uint32_t bar) {
       if (leader) mbar_arrive_expect_tx(bar, 16);
       else st_async_v4(lead(smem_u32(sig_s)), make_uint4(0u, 0u, 0u, 0u), lead(bar));
     };
-    // the raw slot rr into operand slot fr; value rows at or past `valid` are zeros
-    auto convert_slot = [&](bool values, int valid) -> bool {
+    // key row gi of a raw key slot [2 halves][8 groups][2 chunks][8 rows][64 B], 64-byte
+    // swizzled (the 16-byte unit u of row r at u ^ ((r / 2) % 4)), so that the 32 rows a
+    // warp reads fall in distinct banks
+    const int kr7 = gi & 7;
+    const uint32_t krow_off = (uint32_t)(gi >> 6) * (kRawSlotBytes / 2) + (uint32_t)((gi >> 3) & 7) * 1024u +
+                              (uint32_t)kr7 * 64u;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp & 3) << 21);   // lanes 32 (warp % 4) ..
+    auto convert_keys = [&]() -> bool {
+      const uint32_t rs = rr % kRawRing, ks = kp % kKeyTSlots;
+      const bool mine = gi != 0 || (wait(b_rfull + 8 * rs, (rr / kRawRing) & 1) &&
+                                    wait(b_kempty + 8 * ks, ((kp / kKeyTSlots) & 1) ^ 1));
+      if (named_bar_or(cbar, 128, !mine)) return false;
+      tc_fence_after();
+      const uint8_t* src = gRaw + rs * kRawSlotBytes + krow_off;
+      const uint32_t tbase = lane_base + kKeyCol + 64 * ks;
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        uint4 raw4[4];
+#pragma unroll
+        for (int u16 = 0; u16 < 4; ++u16)
+          raw4[u16] = *reinterpret_cast<const uint4*>(src + cc * 512 + ((u16 ^ ((kr7 >> 1) & 3)) << 4));
+        uint32_t w[32];
+#pragma unroll
+        for (int u16 = 0; u16 < 4; ++u16) {
+          const uint32_t b4[4] = {raw4[u16].x, raw4[u16].y, raw4[u16].z, raw4[u16].w};
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2) {
+            w[8 * u16 + 2 * k2] = e4m3x2_to_f16x2(b4[k2] & 0xFFFFu);
+            w[8 * u16 + 2 * k2 + 1] = e4m3x2_to_f16x2(b4[k2] >> 16);
+          }
+        }
+        tmem_st16u(tbase + 32 * cc, w);
+        tmem_st16u(tbase + 32 * cc + 16, w + 16);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      named_bar_sync(cbar, 128);
+      if (gi == 0) {
+        mbar_arrive(b_rempty + 8 * rs);
+        signal_lead(b_kfull + 8 * ks);
+      }
+      ++rr;
+      ++kp;
+      return true;
+    };
+    // one 64-key value block: raw slot rr [8 groups][4 chunks][8 rows][64 B] into value slot
+    // fr; rows at or past `valid` are zeros
+    auto convert_value_slot = [&](int valid) -> bool {
       const uint32_t rs = rr % kRawRing, fs = fr % kRing;
       const bool mine = gi != 0 || (wait(b_rfull + 8 * rs, (rr / kRawRing) & 1) &&
                                     wait(b_empty + 8 * fs, ((fr / kRing) & 1) ^ 1));
@@ -614,10 +693,10 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
 #pragma unroll 2
       for (int j = 0; j < 8; ++j) {
         // 16-byte raw unit idx: column q4 of row `row` of the 1 KB operand block idx / 32
-        // (keys: half, group, chunk; values: group, chunk)
+        // (group idx / 128, chunk (idx / 32) % 4)
         const int idx = gi + 128 * j, q4 = idx & 3, row = (idx >> 2) & 7;
         uint4 v = *reinterpret_cast<const uint4*>(src + 16 * idx);
-        if (values && (idx >> 7) * 8 + row >= valid) v = make_uint4(0u, 0u, 0u, 0u);
+        if ((idx >> 7) * 8 + row >= valid) v = make_uint4(0u, 0u, 0u, 0u);
         const uint32_t b4[4] = {v.x, v.y, v.z, v.w};
         uint32_t hh[8];
 #pragma unroll
@@ -642,7 +721,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
     auto convert_values = [&](const PUnit& U, int tile) -> bool {
       for (int kb = 0; kb < 4; ++kb) {
         const int valid = U.L - tile * kPairKeys - 64 * kb;
-        if (valid > 0 && !convert_slot(true, valid)) return false;
+        if (valid > 0 && !convert_value_slot(valid)) return false;
       }
       return true;
     };
@@ -673,7 +752,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
       }
       int pt = -1;
       for (int tile = U.tb; tile < U.te && ok; ++tile) {
-        for (int ks = 0; ks < kKeySlots && ok; ++ks) ok = convert_slot(false, 0);
+        for (int ks = 0; ks < kKeySlots && ok; ++ks) ok = convert_keys();
         if (ok && pt >= 0) ok = convert_values(U, pt);
         pt = tile;
       }
@@ -750,12 +829,13 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
           ok = wait_wg(b_never, 0);                  // tests: this wait runs out
           if (!ok) break;
         }
-        ok = wait_wg(b_sfull + 8 * (n & 1), (n >> 1) & 1);
+        const uint32_t sb = FP8 ? 0u : (n & 1), sph = FP8 ? (n & 1) : ((n >> 1) & 1);   // S^T buffer
+        ok = wait_wg(b_sfull + 8 * sb, sph);
         if (!ok) break;
         tc_fence_after();
         float s[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld16(tmem + lane_addr + (n & 1) * 128 + 64 * wg + 16 * c, s + 16 * c);
+        for (int c = 0; c < 4; ++c) tmem_ld16(tmem + lane_addr + sb * 128 + 64 * wg + 16 * c, s + 16 * c);
         tmem_wait_ld();
         tc_fence_before();
 
@@ -786,7 +866,11 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         }
         // the barrier also orders every thread's S^T reads before the even CTA's signal
         const bool need_local = named_bar_or(bar, 128, need);
-        if (leader && t == 0) mbar_arrive(b_sempty + 8 * (n & 1));
+        // bf16: the odd CTA's S^T reads precede its P^T signal, which the MMA issuer awaits
+        // before it reuses the buffer two tiles later. FP8 (one S^T buffer): the even CTA
+        // signals only once the odd CTA's message below has arrived, which that CTA sends
+        // after its own reads.
+        if (!FP8 && leader && t == 0) mbar_arrive(b_sempty + 8 * sb);
         if (need_local) {
 #pragma unroll
           for (int r = 0; r < 64; ++r) {
@@ -799,6 +883,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         }
         const float* px = exchange(need_local ? 1u : 0u, own_s[wg]);
         if (px == nullptr) { ok = false; break; }
+        if (FP8 && leader && t == 0) mbar_arrive(b_sempty + 8 * sb);
         const bool need_peer = __float_as_uint(px[0]) != 0u;
         bool rescale = false;
         if (need_local || need_peer) {

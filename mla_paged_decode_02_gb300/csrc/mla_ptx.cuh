@@ -383,6 +383,15 @@ __device__ __forceinline__ void umma_pair_f16(uint32_t d_tmem, uint64_t a_desc, 
                "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
                :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
+// The same with A in tensor memory: each CTA supplies its M/2 rows of A from its own
+// tensor memory at the same address (two 16-bit values per 32-bit column, K-ordered).
+__device__ __forceinline__ void umma_pair_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "setp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+               :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
 // Arrive once on the mbarrier at this offset in BOTH CTAs when every pair MMA this thread
 // issued so far has completed.
 __device__ __forceinline__ void umma_pair_commit(uint32_t bar) {
