@@ -130,12 +130,6 @@ __device__ __forceinline__ uint32_t p_off128(int row, int u) {   // 128-byte swi
   return (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u + ((uint32_t)(u ^ (row & 7)) << 4);
 }
 
-__device__ __forceinline__ int ordered_p(float x) {
-  int k = __float_as_int(x);
-  return k ^ ((k >> 31) & 0x7FFFFFFF);
-}
-__device__ __forceinline__ float unordered_p(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7FFFFFFF)); }
-
 }  // namespace
 
 template <bool FP8, bool kSub>
@@ -152,7 +146,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
   __shared__ __align__(16) uint32_t sig_s[4];        // landing place of the odd CTA's 16-byte signals
   __shared__ __align__(8) uint64_t bar_sfull[2], bar_sempty[2], bar_pfull, bar_pin, bar_pvdone, bar_oempty;
   __shared__ __align__(8) uint64_t bar_x[2][2];
-  __shared__ __align__(8) uint64_t bar_drain, bar_never;
+  __shared__ __align__(8) uint64_t bar_drain, bar_never, bar_epi;
   __shared__ uint32_t tmem_base_s, abort_s;
   __shared__ __align__(16) float xbuf[2][2][68];     // [warpgroup][parity]: word 0 flag, words 4..67 values
   __shared__ __align__(16) float mref_s[2][64];
@@ -187,6 +181,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
   const uint32_t b_oempty = smem_u32(&bar_oempty), b_drain = smem_u32(&bar_drain);
   const uint32_t b_x = smem_u32(bar_x);
   const uint32_t b_never = smem_u32(&bar_never);   // tests: a barrier nothing arrives on
+  const uint32_t b_epi = smem_u32(&bar_epi);       // FP8: a unit's epilogue scratch is free again
   const uint32_t b_rfull = smem_u32(bar_rfull), b_rempty = smem_u32(bar_rempty);
   const uint32_t b_qraw = smem_u32(&bar_qraw), b_qready = smem_u32(&bar_qready);
   const uint32_t b_kfull = smem_u32(bar_kfull), b_kempty = smem_u32(bar_kempty);
@@ -227,6 +222,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
     for (int i = 0; i < 4; ++i) mbar_init(b_x + 8 * i, 1);   // own arrival + the peer's bytes
     mbar_init(b_drain, 1);
     mbar_init(b_never, 1);
+    mbar_init(b_epi, 1);                  // FP8: the warpgroup whose P^T rows live in the peer
     abort_s = 0u;
     fence_mbarrier_init();
     tma_prefetch_desc(&a.tm_q);
@@ -809,8 +805,36 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
       }
     };
 
+    // The same with max over the rows of v, which is left unchanged: lane l gets the maxima of
+    // rows 2l and 2l + 1.
+    auto reduce_rows_max = [&](const float* v, float& m0, float& m1) {
+      float w[32];
+      {
+        const bool hi = (lane & 16) != 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float keep = hi ? v[i + 32] : v[i];
+          const float send = hi ? v[i] : v[i + 32];
+          w[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+        }
+      }
+#pragma unroll
+      for (int n = 32, off = 8; off > 0; n >>= 1, off >>= 1) {
+        const bool hi = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+          const float keep = hi ? w[i + n / 2] : w[i];
+          const float send = hi ? w[i] : w[i + n / 2];
+          w[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, off));
+        }
+      }
+      m0 = w[0];
+      m1 = w[1];
+    };
+
     float lsum[64];
     for (int u = u0; u < u1 && ok; ++u) {
+      const uint32_t ui = (uint32_t)(u - u0);     // this CTA's unit count
       const PUnit U = load_punit(a, u);
       const int T = U.te - U.tb;
       const int row0 = U.g * 128 + 64 * wg;        // first row of this warpgroup in the sequence
@@ -872,11 +896,13 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         // after its own reads.
         if (!FP8 && leader && t == 0) mbar_arrive(b_sempty + 8 * sb);
         if (need_local) {
-#pragma unroll
-          for (int r = 0; r < 64; ++r) {
-            const int m = __reduce_max_sync(0xffffffffu, ordered_p(s[r]));
-            if (lane == (r & 31)) wred_s[wg][wl][r] = unordered_p(m);
-          }
+          // column maxima of the warp's 32 keys for all 64 rows at once (reduce-scatter,
+          // as for the row sums; shuffles rather than 64 redux operations, which the
+          // converting warps' convert instructions slow down in the FP8 kernel)
+          float m0, m1;
+          reduce_rows_max(s, m0, m1);
+          wred_s[wg][wl][2 * lane] = m0;
+          wred_s[wg][wl][2 * lane + 1] = m1;
           named_bar_sync(bar, 128);
           if (t < 64)
             own_s[wg][t] = fmaxf(fmaxf(wred_s[wg][0][t], wred_s[wg][1][t]), fmaxf(wred_s[wg][2][t], wred_s[wg][3][t]));
@@ -923,6 +949,11 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         // P^T and O^T are free once the previous PV has completed; the staging buffer once
         // the previous copy out of it has been read
         if (!FP8 && t == 0 && !local_p) bulk_wait_read0();
+        // FP8: the other warpgroup's previous epilogue used the upper half of this P^T region
+        if (FP8 && local_p && k == 0 && ui > 0) {
+          ok = wait_wg(b_epi, (ui - 1) & 1);
+          if (!ok) break;
+        }
         if (n > 0) {
           ok = wait_wg(b_pvdone, (n - 1) & 1);
           if (!ok) break;
@@ -1015,13 +1046,14 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
       // own half of the P^T buffer for the warpgroup whose rows live here (no other agent
       // writes it before this warpgroup's next P^T), else the staging buffer once its last
       // copy to the peer has been read.
-      // (FP8 has no staging buffer: the other warpgroup stores one value per row and thread)
-      const bool vec = !FP8 || local_p;
+      // FP8 has no staging buffer: its other warpgroup uses the upper half of the same
+      // region, and the P^T rows of the next unit wait for it (b_epi).
       if (!FP8 && !local_p) {
         if (t == 0) bulk_wait_read0();
         named_bar_sync(bar, 128);
       }
-      float* stage = reinterpret_cast<float*>(local_p ? gP + (int)rank * kStageBytes : gStage) + wl * 512;
+      uint8_t* scratch = local_p ? gP + (int)rank * kStageBytes : FP8 ? gP + (int)rank * kStageBytes + 8192 : gStage;
+      float* stage = reinterpret_cast<float*>(scratch) + wl * 512;
       const int nrows = min(64, R - row0);         // rows of this warpgroup that exist
       const int si = lane >> 1, sh = lane & 1;
 #pragma unroll 1
@@ -1036,20 +1068,6 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
             tc_fence_before();
             named_bar_sync(bar, 128);
             if (leader && t == 0) mbar_arrive(b_oempty);
-          }
-          if (!vec) {
-            // value column 256 rank + 128 jt + t, rows 16 c + i
-            const int col = 256 * (int)rank + 128 * jt + t;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int r = 16 * c + i;
-              const float v = o[i] * alpha_s[wg][r];
-              if (r < nrows) {
-                if (direct) a.out[((int64_t)U.b * R + row0 + r) * kDV + col] = __float2bfloat16_rn(v);
-                else a.part_o[((int64_t)U.slot * 128 + 64 * wg + r) * kDV + col] = v;
-              }
-            }
-            continue;
           }
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -1092,6 +1110,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         else a.part_lse[(int64_t)U.slot * 128 + 64 * wg + t] = l;
       }
       named_bar_sync(bar, 128);
+      if (FP8 && !local_p && t == 0) mbar_arrive(b_epi);   // its scratch reads are done
       gn += T;
     }
     // a copy out of the staging buffer has landed before the CTA may leave
