@@ -210,8 +210,10 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
     mbar_init(b_qempty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_sfull + 8 * i, 1);
-      mbar_init(b_sempty + 8 * i, 2);     // the even CTA's two warpgroups (the odd CTA's
-    }                                     // reads precede its P^T signals)
+      // the even CTA's two warpgroups (bf16: the odd CTA's reads precede its P^T signals;
+      // FP8: each expects 16 bytes from the odd CTA's warpgroup of the same rows)
+      mbar_init(b_sempty + 8 * i, 2);
+    }
     // P^T of a tile is complete in both CTAs: the even CTA's warpgroup 0 (its own rows, and
     // it expects the odd CTA's bulk copy of rows for the even CTA's P^T) and the odd CTA's
     // warpgroup 1 (its own rows, once the even CTA's copy into its P^T has landed on b_pin)
@@ -891,10 +893,18 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         // the barrier also orders every thread's S^T reads before the even CTA's signal
         const bool need_local = named_bar_or(bar, 128, need);
         // bf16: the odd CTA's S^T reads precede its P^T signal, which the MMA issuer awaits
-        // before it reuses the buffer two tiles later. FP8 (one S^T buffer): the even CTA
-        // signals only once the odd CTA's message below has arrived, which that CTA sends
-        // after its own reads.
-        if (!FP8 && leader && t == 0) mbar_arrive(b_sempty + 8 * sb);
+        // before it reuses the buffer two tiles later. FP8 (one S^T buffer): the even CTA's
+        // warpgroups arrive expecting 16 bytes each, which the odd CTA's warpgroups send by
+        // st.async once their reads are done.
+        if (t == 0) {
+          if (!FP8) {
+            if (leader) mbar_arrive(b_sempty + 8 * sb);
+          } else if (leader) {
+            mbar_arrive_expect_tx(b_sempty + 8 * sb, 16);
+          } else {
+            st_async_v4(lead(smem_u32(sig_s)), make_uint4(0u, 0u, 0u, 0u), lead(b_sempty + 8 * sb));
+          }
+        }
         if (need_local) {
           // column maxima of the warp's 32 keys for all 64 rows at once (reduce-scatter,
           // as for the row sums; shuffles rather than 64 redux operations, which the
@@ -909,7 +919,6 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         }
         const float* px = exchange(need_local ? 1u : 0u, own_s[wg]);
         if (px == nullptr) { ok = false; break; }
-        if (FP8 && leader && t == 0) mbar_arrive(b_sempty + 8 * sb);
         const bool need_peer = __float_as_uint(px[0]) != 0u;
         bool rescale = false;
         if (need_local || need_peer) {
