@@ -1,5 +1,5 @@
-"""Compile the test-only tcgen05 layout probes into tests/native/libumma_probe.so and
-tests/native/libumma_pair_probe.so."""
+"""Compile the test-only tcgen05 layout probes into tests/native/libumma_probe.so,
+tests/native/libumma_pair_probe.so and tests/native/libumma_f8_probe.so."""
 import os
 import shutil
 import subprocess
@@ -23,8 +23,8 @@ def build_one(name: str) -> str:
 
 def build() -> list:
     from concurrent.futures import ThreadPoolExecutor
-    with ThreadPoolExecutor(max_workers=2) as ex:
-        return list(ex.map(build_one, ["umma_probe", "umma_pair_probe"]))
+    with ThreadPoolExecutor(max_workers=3) as ex:
+        return list(ex.map(build_one, ["umma_probe", "umma_pair_probe", "umma_f8_probe"]))
 
 
 if __name__ == "__main__":
