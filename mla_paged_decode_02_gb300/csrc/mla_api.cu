@@ -90,10 +90,11 @@ mla_status check_params(const mla_decode_params* p) {
 // The cache as [rows / 8 groups][9 chunks][8 rows][64 elements] (strides 8 rows, one
 // chunk, one row): a box of `chunks` chunks x box_rows / 8 groups lands in shared memory
 // as [group][chunk][8 rows][64 elements]. bf16 rows (128 B) are 128-byte swizzled for
-// the MMA. E4M3 key rows (64 B) are 64-byte swizzled, so that 32 threads reading one
-// row each hit distinct banks; E4M3 value rows are left plain.
+// the MMA. E4M3 rows (64 B) with sw64 are 64-byte swizzled: the layout of the 8-bit MMA
+// operands (CTA pairs), and one in which 32 threads reading one key row each hit distinct
+// banks (the converting threads of the single-CTA kernel); its E4M3 value rows are plain.
 bool encode_kv_map(CUtensorMap* m, const void* cache, int64_t rows, uint32_t chunks, uint32_t box_rows,
-                   bool fp8, bool keys) {
+                   bool fp8, bool sw64) {
   const cuuint64_t es = fp8 ? 1 : 2;
   cuuint64_t dims[4] = {64, 8, 9, (cuuint64_t)(rows / 8)};
   cuuint64_t strides[3] = {kDQK * es, 64 * es, kDQK * es * 8};
@@ -102,7 +103,7 @@ bool encode_kv_map(CUtensorMap* m, const void* cache, int64_t rows, uint32_t chu
   CUresult r = g_encode(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                         const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         !fp8 ? CU_TENSOR_MAP_SWIZZLE_128B
-                             : keys ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                             : sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -269,12 +270,13 @@ static mla_status decode_impl(const mla_decode_params* p, const void* q, const v
     return MLA_ERR_INVALID_ARG;
   {
     const int64_t rows = (int64_t)p->num_pages * p->page_size;
-    // chunks per key / value box: a pair loads 2 / 4 adjacent chunks of each row
-    const uint32_t kc = plan.pair ? 2u : (uint32_t)decode_key_chunks_per_slot(rc, fp8);
+    // chunks per key / value box: a pair loads 256-byte pieces of each key row (2 bf16 or 4
+    // E4M3 chunks) and 4 adjacent chunks of each value row
+    const uint32_t kc = plan.pair ? (fp8 ? 4u : 2u) : (uint32_t)decode_key_chunks_per_slot(rc, fp8);
     const uint32_t vc = plan.pair ? 4u : (uint32_t)decode_value_chunks_per_box(rc, fp8);
-    // E4M3 keys are 64-byte swizzled: the converting threads read one row each
+    // E4M3 keys are 64-byte swizzled; E4M3 values too where the MMAs read them as they land
     if (!encode_kv_map(&da.tm_k, kv_cache, rows, kc, (uint32_t)box_rows, fp8, true) ||
-        !encode_kv_map(&da.tm_v, kv_cache, rows, vc, (uint32_t)box_rows, fp8, false))
+        !encode_kv_map(&da.tm_v, kv_cache, rows, vc, (uint32_t)box_rows, fp8, plan.pair))
       return MLA_ERR_INVALID_ARG;
   }
   da.kv_cache = kv_cache;

@@ -22,27 +22,46 @@
 // read from DRAM once per 128 rows; the value columns a CTA needs of its peer's keys come
 // from L2 (the peer has just read them).
 //
+// The FP8 cache. The MMAs read the E4M3 bytes of the cache as TMA lands them (kind::f8f6f4,
+// E4M3 x E4M3 with float32 accumulation; the product of two E4M3 values is exact in
+// float32), so no thread converts a key or a value. The other operand of an MMA must then be
+// E4M3 as well; q and P are each written as two E4M3 terms whose sum keeps the precision
+// the result needs:
+//   q: this CTA's 64 rows of a unit are scaled per row by a power of two 2^e that puts the
+//      row's largest |q| in [128, 256), and q' = q 2^e is stored as hi = e4m3(q') and
+//      lo = e4m3(q' - hi). For a bf16 q the sum is exact wherever lo stays a normal E4M3
+//      number (|q'| >= 2^-2); smaller entries are off by at most 2^-10 in q' units (2^-17 of
+//      the row's largest). S = K.hi + K.lo, and the softmax multiplies row r by 2^-e_r.
+//   P: computed times 2^4 (so at most 2^8 with the lazy rescale threshold of 2^4 below) and
+//      split the same way from its fp16 rounding: about 8 significant bits, as bf16 P has.
+// Each MMA of the bf16 kernel (K = 16) thus becomes two of K = 32: the same tensor time for
+// half the bytes.
+//
 // Softmax coupling. Both CTAs' keys accumulate into the same O^T rows, so they share one
 // reference maximum per row. Each CTA runs two softmax warpgroups, warpgroup w for rows
 // 64w..64w+63 (one thread per key = one TMEM lane). Per tile the warpgroup tells the
 // same warpgroup of the peer whether any of its scores exceeds the reference by more than
-// 2^8 (and, only then, its row maxima) through distributed shared memory; both then move
-// the reference identically. P^T rows 64w.. go to CTA w's P^T buffer (its own or the
-// peer's shared memory). At the end of a unit the row sums are exchanged the same way.
+// the rescale threshold (and, only then, its row maxima) through distributed shared
+// memory; both then move the reference identically. P^T rows 64w.. go to CTA w's P^T
+// buffer (its own, or the peer's by one bulk copy). At the end of a unit the row sums are
+// exchanged the same way; with the FP8 cache the row factors 2^-e too, at its start.
 //
 // Pipeline per CTA (384 threads). Warp 0: producer — one ring of 32 KB slots in the order
-// the MMAs consume them (the 5 key slots of tile n, then the value slots of tile n-1; a
-// unit's last value slots right after its last key slots), plus each unit's Q. A TMA load's cost grows with the number of contiguous row pieces in its
-// box (measured on this GPU: about 22 GB/s per SM for 128-byte pieces from L2, 44 for 256,
-// 87 for 512), so key boxes take two adjacent 64-column chunks of each row and value boxes
-// four. Every load completes on the even CTA's barrier, which the even CTA alone arms with
-// the bytes of both CTAs (it knows which key halves its peer loads), so that no load needs a
-// cross-CTA arrival (each costs a fraction of a microsecond). Warp 1 of the even CTA: the
-// single MMA issuer, in program order QK^T(n), PV(n-1), QK^T(n+1), ..., a unit's last PV
-// before the next unit's first QK^T (so that the epilogue need not wait for it); its commits arrive
-// on the barrier at the same offset in both CTAs. Warps 4-7 and 8-11: softmax warpgroups 0
-// and 1, then the epilogue. Every wait is bounded; a stall sets the device error word, and
-// both CTAs drain and leave through a final cluster barrier.
+// the MMAs consume them (the key slots of tile n, then the value slots of tile n-1; a
+// unit's last value slots right after its last key slots), plus each unit's Q. A TMA load's
+// cost grows with the number of contiguous row pieces in its box (measured on this GPU:
+// about 22 GB/s per SM for 128-byte pieces from L2, 44 for 256, 87 for 512), so key boxes
+// take 256-byte pieces of each row (two 64-column bf16 chunks, or four E4M3 ones) and value
+// boxes four chunks. Every key and value load completes on the even CTA's barrier, which
+// the even CTA alone arms with the bytes of both CTAs (it knows which key halves its peer
+// loads), so that no load needs a cross-CTA arrival (each costs a fraction of a
+// microsecond). Warp 1 of the even CTA: the single MMA issuer, in program order QK^T(n),
+// PV(n-1), QK^T(n+1), ..., a unit's last PV before the next unit's first QK^T (so that the
+// epilogue need not wait for it); its commits arrive on the barrier at the same offset in
+// both CTAs. Warps 2-3 (FP8): turn each unit's bf16 Q into hi and lo in place. Warps 4-7
+// and 8-11: softmax warpgroups 0 and 1, then the epilogue. Every wait is bounded; a stall
+// sets the device error word, and both CTAs drain and leave through a final cluster
+// barrier.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include "mla_internal.h"
@@ -54,47 +73,41 @@ namespace mla {
 namespace {
 
 constexpr int kPairKeys = 256;              // keys per super-tile
-constexpr int kSlotBytes = 32768;           // ring slot: 128 keys x 128 columns, or 64 keys x 256 columns
-constexpr int kKeySlots = 5;                // key chunk pairs per super-tile (9 chunks, the last alone)
+constexpr int kSlotBytes = 32768;           // ring slot
 constexpr int kQChunk = 8192;               // 64 rows x 64 columns bf16
-constexpr int kPairQBytes = 9 * kQChunk;
-constexpr int kPairPBytes = kPairKeys * 128;  // P^T: 256 keys x 64 rows bf16
+constexpr int kPairQBytes = 9 * kQChunk;    // this CTA's 64 query rows: bf16, or E4M3 hi and lo
+constexpr int kPairPBytes = kPairKeys * 128;  // P^T for 256 keys x 64 rows: bf16, or E4M3 hi and lo
 constexpr int kStageBytes = 16384;         // P^T rows bound for the peer: 128 keys x 64 rows
-constexpr int kRawSlotBytes = 16384;       // FP8 raw slot: 128 keys x 2 chunks, or 64 keys x 4 chunks, E4M3
-constexpr int kMaxRing = 3;
+constexpr int kRing = 3;
+constexpr int kPairThreads = 384;
 constexpr int kPairTmemCols = 512;
 constexpr int kOCol = 256;                  // O^T M-tile j at columns 256 + 128 j
-constexpr float kPairRescaleLog2 = 8.0f;
 constexpr float kPLog2e = 1.4426950408889634f;
 constexpr float kPLn2 = 0.6931471805599453f;
 constexpr int kPairSmemLimit = 232448;
 constexpr int kPairStaticBudget = 9216;
+constexpr int kPairDynBytes = 1024 + kPairQBytes + kPairPBytes + kStageBytes + kRing * kSlotBytes;
+static_assert(kPairDynBytes + kPairStaticBudget <= kPairSmemLimit, "shared memory budget");
 
-// bf16: 384 threads; a ring of three 32 KB operand slots (keys and values) filled by TMA,
-// and a 16 KB staging buffer for the P^T rows sent to the peer by one bulk copy; S^T
-// double-buffered in tensor memory.
-// FP8: 512 threads (a fourth warpgroup converts E4M3 to fp16); keys go to two tensor-memory
-// key slots (the QK^T MMAs read A from tensor memory), values to a ring of two 32 KB fp16
-// slots, both from a ring of three 16 KB raw E4M3 slots filled by TMA; S^T single-buffered
-// (its second buffer's columns hold the key slots); P^T rows for the peer go by st.async
-// (no staging buffer).
+// Slot plans. A key slot is KC adjacent 64-column chunks of this CTA's 128 keys — bf16: 2
+// chunks of 128-byte rows (5 slots per super-tile); E4M3: 4 chunks of 64-byte rows (3
+// slots) — the last slot holding chunk 8 and zero-filled chunks past the row (TMA fills
+// them). A value slot holds this CTA's 256 value columns of one 64-key block (bf16) or two
+// (E4M3). Either way a key slot is [2 halves][8 groups][KC chunks][8 rows][row piece] with
+// 2 KB per 8-row group, and a value block [8 groups][4 chunks][8 rows][row piece].
 template <bool FP8>
 struct PairCfg {
-  static constexpr int kThreads = FP8 ? 512 : 384;
-  static constexpr int kRing = FP8 ? 2 : 3;
-  static constexpr int kStage = FP8 ? 0 : kStageBytes;
-  static constexpr int kRawRing = FP8 ? 3 : 0;
-  static constexpr int kDynBytes =
-      1024 + kPairQBytes + kPairPBytes + kStage + kRing * kSlotBytes + kRawRing * kRawSlotBytes;
-  static_assert(kRing <= kMaxRing && kRawRing <= kMaxRing, "barrier arrays");
-  static_assert(kDynBytes + kPairStaticBudget <= kPairSmemLimit, "shared memory budget");
+  static constexpr int kKeyChunks = FP8 ? 4 : 2;
+  static constexpr int kKeySlots = (9 + kKeyChunks - 1) / kKeyChunks;
+  static constexpr int kRowBytes = FP8 ? 64 : 128;      // one chunk of one row
+  static constexpr int kBlocksPerSlot = FP8 ? 2 : 1;    // 64-key value blocks per value slot
+  static constexpr int kBlockBytes = kSlotBytes / kBlocksPerSlot;
+  static constexpr int kKStep = FP8 ? 32 : 16;          // keys per MMA K step
+  static constexpr float kRescaleLog2 = FP8 ? 4.f : 8.f;  // lazy rescale threshold (log2 units)
+  static constexpr float kPOffLog2 = FP8 ? 4.f : 0.f;     // P is computed times 2^kPOffLog2
+  static_assert(4 * 8 * kRowBytes * 8 == kBlockBytes, "value block layout");
+  static_assert(kKeyChunks * 8 * kRowBytes == 2048, "key slot group stride");
 };
-constexpr int kKeyTSlots = 2;               // FP8: tensor-memory key slots (two chunks = 64 columns each)
-constexpr int kKeyCol = 128;                // FP8: their first column
-// FP8 register budgets per thread (setmaxnreg): warpgroup 0 (producer, MMA issuer), the two
-// softmax warpgroups, the converters. They redistribute the launch allocation of 128.
-constexpr int kRegsCtl = 96, kRegsSoftmax = 176, kRegsConv = 64;
-static_assert(kRegsCtl + 2 * kRegsSoftmax + kRegsConv <= 4 * 128, "register budgets exceed the launch allocation");
 
 struct PUnit {
   int b, g, tb, te, slot, L;
@@ -126,30 +139,54 @@ __device__ __forceinline__ void block_rows(const DecodeArgs& a, const PUnit& U, 
   }
 }
 
-__device__ __forceinline__ uint32_t p_off128(int row, int u) {   // 128-byte swizzled P^T row
+__device__ __forceinline__ uint32_t p_off128(int row, int u) {   // 128-byte swizzled bf16 P^T row
   return (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u + ((uint32_t)(u ^ (row & 7)) << 4);
+}
+__device__ __forceinline__ uint32_t p_off64(int row, int u) {    // 64-byte swizzled E4M3 P^T row
+  return (uint32_t)(row >> 3) * 512u + (uint32_t)(row & 7) * 64u + ((uint32_t)(u ^ ((row >> 1) & 3)) << 4);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// x0, x1 (|x| < 448) as E4M3 pairs hi = e4m3(x), lo = e4m3(x - hi), both rounded to nearest
+// even with saturation, taken on the fp16 roundings of x (x - hi is exact there: hi is x
+// rounded to 4 significant bits). Returns hi in bits 0-15 and lo in bits 16-31, element 0
+// in the lower byte of each.
+__device__ __forceinline__ uint32_t split_e4m3x2(float x0, float x1) {
+  uint32_t out;
+  asm("{\n\t.reg .b32 h, back, r;\n\t.reg .b16 hb, lb;\n\t"
+      "cvt.rn.f16x2.f32 h, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 hb, h;\n\t"
+      "cvt.rn.f16x2.e4m3x2 back, hb;\n\t"
+      "sub.rn.f16x2 r, h, back;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 lb, r;\n\t"
+      "mov.b32 %0, {hb, lb};\n\t}"
+      : "=r"(out) : "f"(x0), "f"(x1));
+  return out;
 }
 
 }  // namespace
 
 template <bool FP8, bool kSub>
-__global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __grid_constant__ DecodeArgs a) {
   using Cfg = PairCfg<FP8>;
-  // (the raw ring's depth is 1, not 0, in the bf16 kernel, where no code indexes it)
-  constexpr int kRing = Cfg::kRing, kRawRing = FP8 ? Cfg::kRawRing : 1;
+  constexpr int KC = Cfg::kKeyChunks, kKeySlots = Cfg::kKeySlots;
   extern __shared__ uint8_t dsmem_raw[];
-  __shared__ __align__(8) uint64_t bar_full[kMaxRing], bar_empty[kMaxRing], bar_aux;
+  __shared__ __align__(8) uint64_t bar_full[kRing], bar_empty[kRing], bar_aux;
   __shared__ __align__(8) uint64_t bar_qfull, bar_qempty;
-  // FP8: raw ring, Q landed (this CTA), Q converted (both CTAs, on the even CTA)
-  __shared__ __align__(8) uint64_t bar_rfull[kMaxRing], bar_rempty[kMaxRing], bar_qraw, bar_qready;
-  __shared__ __align__(8) uint64_t bar_kfull[kKeyTSlots], bar_kempty[kKeyTSlots];   // FP8 key slots
+  // FP8: Q landed (this CTA), Q converted (both CTAs, on the even CTA), this CTA's row
+  // factors written and read
+  __shared__ __align__(8) uint64_t bar_qraw, bar_qready, bar_qsc, bar_qfree;
   __shared__ __align__(16) uint32_t sig_s[4];        // landing place of the odd CTA's 16-byte signals
   __shared__ __align__(8) uint64_t bar_sfull[2], bar_sempty[2], bar_pfull, bar_pin, bar_pvdone, bar_oempty;
   __shared__ __align__(8) uint64_t bar_x[2][2];
-  __shared__ __align__(8) uint64_t bar_drain, bar_never, bar_epi;
+  __shared__ __align__(8) uint64_t bar_drain, bar_never;
   __shared__ uint32_t tmem_base_s, abort_s;
   __shared__ __align__(16) float xbuf[2][2][68];     // [warpgroup][parity]: word 0 flag, words 4..67 values
   __shared__ __align__(16) float mref_s[2][64];
+  __shared__ __align__(16) float rowc_s[2][64];     // FP8: score factor of each row (log2 units)
+  __shared__ float qf_s[64];                        // FP8: 2^-e of this CTA's 64 query rows
   __shared__ float alpha_s[2][64], own_s[2][64];
   __shared__ int nvis_s[2][64];
   __shared__ float wred_s[2][4][64];
@@ -166,54 +203,40 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
   const uint32_t sQ = base;
   const uint32_t sP = sQ + kPairQBytes;
   const uint32_t sStage = sP + kPairPBytes;
-  const uint32_t sR = sStage + Cfg::kStage;
-  const uint32_t sRaw = sR + kRing * kSlotBytes;     // FP8 raw ring
+  const uint32_t sR = sStage + kStageBytes;
   uint8_t* gQ = gbase;
   uint8_t* gP = gbase + kPairQBytes;
   uint8_t* gStage = gP + kPairPBytes;
-  uint8_t* gR = gStage + Cfg::kStage;
-  const uint8_t* gRaw = gR + kRing * kSlotBytes;
+  uint8_t* gR = gStage + kStageBytes;
 
   const uint32_t b_full = smem_u32(bar_full), b_empty = smem_u32(bar_empty), b_aux = smem_u32(&bar_aux);
   const uint32_t b_qfull = smem_u32(&bar_qfull), b_qempty = smem_u32(&bar_qempty);
+  const uint32_t b_qraw = smem_u32(&bar_qraw), b_qready = smem_u32(&bar_qready);
+  const uint32_t b_qsc = smem_u32(&bar_qsc), b_qfree = smem_u32(&bar_qfree);
   const uint32_t b_sfull = smem_u32(bar_sfull), b_sempty = smem_u32(bar_sempty);
   const uint32_t b_pfull = smem_u32(&bar_pfull), b_pin = smem_u32(&bar_pin), b_pvdone = smem_u32(&bar_pvdone);
   const uint32_t b_oempty = smem_u32(&bar_oempty), b_drain = smem_u32(&bar_drain);
   const uint32_t b_x = smem_u32(bar_x);
   const uint32_t b_never = smem_u32(&bar_never);   // tests: a barrier nothing arrives on
-  const uint32_t b_epi = smem_u32(&bar_epi);       // FP8: a unit's epilogue scratch is free again
-  const uint32_t b_rfull = smem_u32(bar_rfull), b_rempty = smem_u32(bar_rempty);
-  const uint32_t b_qraw = smem_u32(&bar_qraw), b_qready = smem_u32(&bar_qready);
-  const uint32_t b_kfull = smem_u32(bar_kfull), b_kempty = smem_u32(bar_kempty);
   volatile uint32_t* abort_flag = &abort_s;
   uint32_t* err = a.err;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRing; ++i) {
-      // bf16: the even CTA's producer, with both CTAs' bytes; FP8: the even CTA's
-      // converters, expecting the odd CTA's converters' 16-byte message
-      mbar_init(b_full + 8 * i, 1);
+      mbar_init(b_full + 8 * i, 1);       // the even CTA's producer, with both CTAs' bytes
       mbar_init(b_empty + 8 * i, 1);
     }
-    for (int i = 0; i < Cfg::kRawRing; ++i) {
-      mbar_init(b_rfull + 8 * i, 1);      // this CTA's producer, with its bytes
-      mbar_init(b_rempty + 8 * i, 1);     // this CTA's converters
-    }
-    mbar_init(b_qraw, 1);
-    mbar_init(b_qready, 1);               // as b_full (FP8)
-    for (int i = 0; i < kKeyTSlots; ++i) {
-      mbar_init(b_kfull + 8 * i, 1);      // as b_full (FP8)
-      mbar_init(b_kempty + 8 * i, 1);
-    }
     mbar_init(b_aux, 1);
-    mbar_init(b_qfull, 1);                // the even CTA's arrival, with both CTAs' bytes
+    mbar_init(b_qfull, 1);                // bf16: the even CTA's arrival, with both CTAs' bytes
     mbar_init(b_qempty, 1);
+    mbar_init(b_qraw, 1);                 // FP8: this CTA's producer, with its bytes
+    mbar_init(b_qready, 1);               // FP8: the even CTA's converters, expecting the odd CTA's 16-byte signal
+    mbar_init(b_qsc, 1);                  // FP8: this CTA's converters
+    mbar_init(b_qfree, 1);                // FP8: the softmax warpgroup of this CTA's rows
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_sfull + 8 * i, 1);
-      // the even CTA's two warpgroups (bf16: the odd CTA's reads precede its P^T signals;
-      // FP8: each expects 16 bytes from the odd CTA's warpgroup of the same rows)
-      mbar_init(b_sempty + 8 * i, 2);
-    }
+      mbar_init(b_sempty + 8 * i, 2);     // the even CTA's two warpgroups (the odd CTA's
+    }                                     // reads precede its P^T signals)
     // P^T of a tile is complete in both CTAs: the even CTA's warpgroup 0 (its own rows, and
     // it expects the odd CTA's bulk copy of rows for the even CTA's P^T) and the odd CTA's
     // warpgroup 1 (its own rows, once the even CTA's copy into its P^T has landed on b_pin)
@@ -224,7 +247,6 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
     for (int i = 0; i < 4; ++i) mbar_init(b_x + 8 * i, 1);   // own arrival + the peer's bytes
     mbar_init(b_drain, 1);
     mbar_init(b_never, 1);
-    mbar_init(b_epi, 1);                  // FP8: the warpgroup whose P^T rows live in the peer
     abort_s = 0u;
     fence_mbarrier_init();
     tma_prefetch_desc(&a.tm_q);
@@ -242,11 +264,6 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
   const int u0 = a.cta_first[pair], u1 = a.cta_first[pair + 1];
   const int R = a.R;
   auto lead = [&](uint32_t addr) { return map_to_rank(addr, 0); };
-  // arrive on a barrier of the even CTA (a local arrive there, a remote one from the odd CTA)
-  auto arrive_lead = [&](uint32_t addr) {
-    if (leader) mbar_arrive(addr);
-    else mbar_arrive_cluster(lead(addr));
-  };
   // A failed wait also raises the peer's abort flag, so that its waits end too.
   auto fail_peer = [&]() { st_cluster_u32(map_to_rank(smem_u32(&abort_s), peer), 1u); };
   auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
@@ -256,174 +273,74 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
   };
 
   if (warp < 4) {
-    // warpgroup 0: producer (warp 0) and MMA issuer (warp 1 of the even CTA). FP8: every
-    // warpgroup first sets its register budget (all four warps, before they split).
-    if constexpr (FP8) regs_lower<kRegsCtl>();
     if (warp == 0) {
-      if constexpr (FP8) {
-      // ================================================================ producer (FP8)
-      // Raw E4M3 rows into this CTA's raw ring in the order the converters (and then the
-      // MMAs) take them — per super-tile its 5 key slots, then the value slots of the
-      // previous one, a unit's last value slots right after its last key slots — and each
-      // unit's Q. Every load completes on this CTA's own barrier: only the converters' output
-      // is shared with the peer.
-      uint32_t rr = 0, uq = 0;
-      bool ok = true;
-      const uint64_t pol_keep = l2_policy_evict_last(), pol_last = l2_policy_evict_first();
-      const int32_t* bt_all = a.block_table;
-      const uint32_t box_rows = kSub ? (uint32_t)a.box_rows : 64u;
-      const uint32_t kbox_bytes = 128 * box_rows;        // raw key box: 2 chunks x 64 B per row
-      const uint32_t vbox_bytes = 256 * box_rows;        // raw value box: 4 chunks x 64 B per row
-      // the next raw slot once the converters have released it (-1: a wait gave up)
-      auto take_raw = [&]() -> int {
-        const uint32_t rs = rr % kRawRing;
-        const bool w_ok = lane != 0 || wait(b_rempty + 8 * rs, ((rr / kRawRing) & 1) ^ 1);
-        return __all_sync(0xffffffffu, w_ok) ? (int)rs : -1;
-      };
-      // raw value slot [8 key groups][4 chunks][8 rows][64 B]: this CTA's value columns of
-      // one 64-key block (rows past the sequence end are zeroed by the converters)
-      auto load_values = [&](const PUnit& U, int tile, const int64_t* rb, const int* nb) -> bool {
-        const int32_t* bt = bt_all + (int64_t)U.b * a.MB;
-        for (int kb = 0; kb < 4; ++kb) {
-          if (rb[kb] < 0) continue;
-          const int rs = take_raw();
-          if (rs < 0) return false;
-          if (lane == 0) {
-            const uint32_t bar = b_rfull + 8 * rs, dst = sRaw + rs * kRawSlotBytes;
-            const int32_t c0 = 4 * (int)rank;            // this CTA's value columns 256 rank ..
-            mbar_arrive_expect_tx(bar, (kSub ? (uint32_t)nb[kb] : 1u) * vbox_bytes);
-            tma_load_4d_hint(dst, &a.tm_v, bar, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
-            if (kSub && nb[kb] > 1)
-              load_more_boxes(kBoxHint, &a.tm_v, dst, bar, c0, vbox_bytes, bt, a, tile * kPairKeys + 64 * kb, nb[kb],
-                              pol_last);
-          }
-          ++rr;
-        }
-        return true;
-      };
-      PUnit pu{};
-      int ptile = -1;
-      int64_t prb[4] = {-1, -1, -1, -1};
-      int pnb[4] = {0, 0, 0, 0};
-      for (int u = u0; u < u1 && ok; ++u, ++uq) {
-        const PUnit U = load_punit(a, u);
-        // this CTA's 64 query rows (bf16; the converters turn them into fp16 in place) once
-        // the previous unit's QK^T MMAs are done with the buffer
-        bool w_ok = lane != 0 || wait(b_qempty, (uq & 1) ^ 1);
-        ok = __all_sync(0xffffffffu, w_ok);
-        if (!ok) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(b_qraw, kPairQBytes);
-          if (a.q_whole_rows)
-            tma_load_5d_hint(sQ, &a.tm_q, b_qraw, 0, 0, 0, (128 * U.g + 64 * (int)rank) / 8, U.b, pol_keep);
-          else
-            for (int c = 0; c < 9; ++c)
-              tma_load_3d_hint(sQ + c * kQChunk, &a.tm_q, b_qraw, 64 * c, 128 * U.g + 64 * (int)rank, U.b, pol_keep);
-        }
-        for (int tile = U.tb; tile < U.te && ok; ++tile) {
-          int64_t rb[4];
-          int nb[4];
-          block_rows<kSub>(a, U, tile, rb, nb);
-          const int32_t* bt = bt_all + (int64_t)U.b * a.MB;
-          const uint32_t nown = (uint32_t)(nb[2 * rank] + nb[2 * rank + 1]);   // this CTA's key boxes
-          // raw key slot [2 halves][8 groups][2 chunks][8 rows][64 B]: chunks 2ks, 2ks + 1 of
-          // this CTA's 128 keys (the last slot: chunk 8 and a zero-filled chunk past the row)
-          for (int ks = 0; ks < kKeySlots; ++ks) {
-            const int rs = take_raw();
-            if (rs < 0) { ok = false; break; }
-            if (lane == 0) {
-              const uint32_t bar = b_rfull + 8 * rs, dst = sRaw + rs * kRawSlotBytes;
-              mbar_arrive_expect_tx(bar, nown * kbox_bytes);
-              for (int h = 0; h < 2; ++h) {
-                const int kb = 2 * (int)rank + h;
-                if (nb[kb] == 0) continue;
-                const uint32_t d = dst + h * (kRawSlotBytes / 2);
-                tma_load_4d_hint(d, &a.tm_k, bar, 0, 0, 2 * ks, (int32_t)(rb[kb] >> 3), pol_keep);
-                if (kSub && nb[kb] > 1)
-                  load_more_boxes(kBoxHint, &a.tm_k, d, bar, 2 * ks, kbox_bytes, bt, a, tile * kPairKeys + 64 * kb,
-                                  nb[kb], pol_keep);
-              }
-            }
-            ++rr;
-          }
-          if (!ok) break;
-          if (ptile >= 0) ok = load_values(pu, ptile, prb, pnb);
-          pu = U;
-          ptile = tile;
-          for (int kb = 0; kb < 4; ++kb) { prb[kb] = rb[kb]; pnb[kb] = nb[kb]; }
-        }
-        if (ok && ptile >= 0) ok = load_values(pu, ptile, prb, pnb);
-        ptile = -1;
-      }
-      // this CTA's own loads have landed before it may leave
-      if (lane == 0) {
-        volatile uint32_t no_abort = 0;
-        for (uint32_t q = rr > (uint32_t)kRawRing ? rr - kRawRing : 0; q < rr; ++q)
-          mbar_wait(b_rfull + 8 * (q % kRawRing), (q / kRawRing) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT,
-                    a.wait_limit_ns);
-        if (uq > 0) mbar_wait(b_qraw, (uq - 1) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
-      }
-      } else {
       // ================================================================ producer
-      // Ring order per super-tile n: its 5 key slots (chunk pairs 0-1, 2-3, 4-5, 6-7 and 8,
-      // 128 keys each), then the value slots of tile n-1 (64 keys x this CTA's 256 value
-      // columns each, one per 64-key block before the sequence end); a unit's last value
-      // slots follow its last key slots. TMA cost grows with the number of contiguous row pieces a box has, not
-      // with its bytes, so every box takes 2 (keys) or 4 (values) adjacent chunks of a row.
+      // Ring order per super-tile n: its key slots (chunks KC ks .. KC ks + KC - 1 of this
+      // CTA's 128 keys each), then the value slots of tile n-1 (this CTA's 256 value columns
+      // of the 64-key blocks before the sequence end); a unit's last value slots follow its
+      // last key slots.
       uint32_t r = 0, uq = 0, aux = 0;
       bool ok = true;
       // a key's lines are read again (as values, by this CTA or its peer) about one tile later:
       // keep them in L2; the value read is their last use
       const uint64_t pol_keep = l2_policy_evict_last(), pol_last = l2_policy_evict_first();
-      // the block holding the sequence end gets the rows up to the end of its last 16-key MMA
-      // step zeroed (the cache may hold NaN there, and 0 * NaN is NaN inside the MMA)
       const int32_t* bt_all = a.block_table;
       const uint32_t box_rows = kSub ? (uint32_t)a.box_rows : 64u;             // rows of one box
       const uint32_t kbox_bytes = (kSlotBytes / 128) * box_rows;               // one key box
-      const uint32_t vbox_bytes = (kSlotBytes / 64) * box_rows;                // one value box
+      const uint32_t vbox_bytes = (Cfg::kBlockBytes / 64) * box_rows;          // one value box
       auto load_values = [&](const PUnit& U, int tile, const int64_t* rb, const int* nb) -> bool {
         const int32_t* bt = bt_all + (int64_t)U.b * a.MB;
-        for (int kb = 0; kb < 4; ++kb) {
-          if (rb[kb] < 0) continue;
-          const int valid = U.L - tile * kPairKeys - 64 * kb;
-          // a block not loaded whole (boxes past the sequence end) completes its bytes itself
-          const bool zero = valid < 64 && ((valid & 15) != 0 || (kSub && nb[kb] < (int)(64 / box_rows)));
-          const int tok0 = tile * kPairKeys + 64 * kb;
+        for (int vs = 0; vs < 4 / Cfg::kBlocksPerSlot; ++vs) {
+          int nvalid = 0;
+          for (int i = 0; i < Cfg::kBlocksPerSlot; ++i) nvalid += rb[vs * Cfg::kBlocksPerSlot + i] >= 0 ? 1 : 0;
+          if (nvalid == 0) continue;
           const uint32_t slot = r % kRing;
           bool w_ok = lane != 0 || wait(b_empty + 8 * slot, ((r / kRing) & 1) ^ 1);
           if (!__all_sync(0xffffffffu, w_ok)) return false;
-          const uint32_t dst = sR + slot * kSlotBytes, lb = lead(b_full + 8 * slot);
+          const uint32_t lb = lead(b_full + 8 * slot);
           const int32_t c0 = 4 * (int)rank;            // this CTA's value columns 256 rank ..
-          if (leader && lane == 0) mbar_arrive_expect_tx(b_full + 8 * slot, 2 * kSlotBytes);
-          if (!zero) {
-            if (lane == 0) {
-              tma_load_4d_pair_hint(dst, &a.tm_v, lb, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
-              if (kSub && nb[kb] > 1)
-                load_more_boxes(kBoxPairHint, &a.tm_v, dst, lb, c0, vbox_bytes, bt, a, tok0, nb[kb], pol_last);
-            }
-          } else {
-            if (lane == 0) {
-              mbar_arrive_expect_tx(b_aux, (kSub ? (uint32_t)nb[kb] : 1u) * vbox_bytes);
-              tma_load_4d_hint(dst, &a.tm_v, b_aux, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
-              if (kSub && nb[kb] > 1)
-                load_more_boxes(kBoxHint, &a.tm_v, dst, b_aux, c0, vbox_bytes, bt, a, tok0, nb[kb], pol_last);
-            }
-            w_ok = wait(b_aux, aux & 1);
-            ++aux;
-            if (!__all_sync(0xffffffffu, w_ok)) return false;
-            // slot layout [8 key groups][4 chunks][8 rows][128 B]: zero whole rows
-            const int nrow = ((valid + 15) & ~15) - valid;
-            uint8_t* g = gR + slot * kSlotBytes;
-            for (int idx = lane; idx < nrow * 32; idx += 32) {
-              const int row = valid + (idx >> 5), c = (idx >> 3) & 3, u16 = idx & 7;
-              *reinterpret_cast<uint4*>(g + (row >> 3) * 4096 + c * 1024 + (row & 7) * 128 + u16 * 16) =
-                  make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              fence_acq_rel_cluster();
-              mbar_complete_tx_cluster(lb, kSlotBytes);   // this CTA's share of the slot is in place
+          if (leader && lane == 0) mbar_arrive_expect_tx(b_full + 8 * slot, 2u * nvalid * Cfg::kBlockBytes);
+          for (int i = 0; i < Cfg::kBlocksPerSlot; ++i) {
+            const int kb = vs * Cfg::kBlocksPerSlot + i;
+            if (rb[kb] < 0) continue;
+            const int valid = U.L - tile * kPairKeys - 64 * kb;
+            // the block holding the sequence end gets its rows up to the end of its last MMA K
+            // step zeroed (the cache may hold NaN there, and 0 * NaN is NaN inside the MMA); a
+            // block not loaded whole completes its bytes itself
+            const bool zero = valid < 64 && ((valid % Cfg::kKStep) != 0 || (kSub && nb[kb] < (int)(64 / box_rows)));
+            const int tok0 = tile * kPairKeys + 64 * kb;
+            const uint32_t dst = sR + slot * kSlotBytes + i * Cfg::kBlockBytes;
+            if (!zero) {
+              if (lane == 0) {
+                tma_load_4d_pair_hint(dst, &a.tm_v, lb, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
+                if (kSub && nb[kb] > 1)
+                  load_more_boxes(kBoxPairHint, &a.tm_v, dst, lb, c0, vbox_bytes, bt, a, tok0, nb[kb], pol_last);
+              }
+            } else {
+              if (lane == 0) {
+                mbar_arrive_expect_tx(b_aux, (kSub ? (uint32_t)nb[kb] : 1u) * vbox_bytes);
+                tma_load_4d_hint(dst, &a.tm_v, b_aux, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
+                if (kSub && nb[kb] > 1)
+                  load_more_boxes(kBoxHint, &a.tm_v, dst, b_aux, c0, vbox_bytes, bt, a, tok0, nb[kb], pol_last);
+              }
+              w_ok = wait(b_aux, aux & 1);
+              ++aux;
+              if (!__all_sync(0xffffffffu, w_ok)) return false;
+              // block layout [8 key groups][4 chunks][8 rows][row piece]: zero whole rows
+              constexpr int kU = Cfg::kRowBytes / 16;
+              const int nrow = ((valid + Cfg::kKStep - 1) & ~(Cfg::kKStep - 1)) - valid;
+              uint8_t* g = gR + slot * kSlotBytes + i * Cfg::kBlockBytes;
+              for (int idx = lane; idx < nrow * 4 * kU; idx += 32) {
+                const int row = valid + idx / (4 * kU), c = (idx / kU) & 3, u16 = idx % kU;
+                *reinterpret_cast<uint4*>(g + (row >> 3) * (32 * Cfg::kRowBytes) + c * (8 * Cfg::kRowBytes) +
+                                          (row & 7) * Cfg::kRowBytes + u16 * 16) = make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                fence_acq_rel_cluster();
+                mbar_complete_tx_cluster(lb, Cfg::kBlockBytes);   // this CTA's share of the block is in place
+              }
             }
           }
           ++r;
@@ -438,18 +355,28 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
       for (int u = u0; u < u1 && ok; ++u, ++uq) {
         const PUnit U = load_punit(a, u);
         // this CTA's 64 query rows of the unit (rows past R read as zeros), kept in L2 for the
-        // re-reads of long sequences' units
+        // re-reads of long sequences' units. bf16: counted on the even CTA's barrier with both
+        // CTAs' bytes; FP8: on this CTA's own, for its converters
         bool w_ok = lane != 0 || wait(b_qempty, (uq & 1) ^ 1);
         ok = __all_sync(0xffffffffu, w_ok);
         if (!ok) break;
         if (lane == 0) {
-          const uint32_t lb = lead(b_qfull);
-          if (leader) mbar_arrive_expect_tx(b_qfull, 2 * kPairQBytes);
-          if (a.q_whole_rows)       // one box of 64 whole rows: [8 groups][9 chunks][8 rows][128 B]
-            tma_load_5d_pair_hint(sQ, &a.tm_q, lb, 0, 0, 0, (128 * U.g + 64 * (int)rank) / 8, U.b, pol_keep);
-          else                      // 9 boxes of one 64-column chunk: [9 chunks][64 rows][128 B]
-            for (int c = 0; c < 9; ++c)
-              tma_load_3d_pair_hint(sQ + c * kQChunk, &a.tm_q, lb, 64 * c, 128 * U.g + 64 * (int)rank, U.b, pol_keep);
+          const int32_t qg = (128 * U.g + 64 * (int)rank) / 8, q0 = 128 * U.g + 64 * (int)rank;
+          if constexpr (FP8) {
+            mbar_arrive_expect_tx(b_qraw, kPairQBytes);
+            if (a.q_whole_rows)     // one box of 64 whole rows: [8 groups][9 chunks][8 rows][128 B]
+              tma_load_5d_hint(sQ, &a.tm_q, b_qraw, 0, 0, 0, qg, U.b, pol_keep);
+            else                    // 9 boxes of one 64-column chunk: [9 chunks][64 rows][128 B]
+              for (int c = 0; c < 9; ++c) tma_load_3d_hint(sQ + c * kQChunk, &a.tm_q, b_qraw, 64 * c, q0, U.b, pol_keep);
+          } else {
+            const uint32_t lb = lead(b_qfull);
+            if (leader) mbar_arrive_expect_tx(b_qfull, 2 * kPairQBytes);
+            if (a.q_whole_rows)
+              tma_load_5d_pair_hint(sQ, &a.tm_q, lb, 0, 0, 0, qg, U.b, pol_keep);
+            else
+              for (int c = 0; c < 9; ++c)
+                tma_load_3d_pair_hint(sQ + c * kQChunk, &a.tm_q, lb, 64 * c, q0, U.b, pol_keep);
+          }
         }
         for (int tile = U.tb; tile < U.te && ok; ++tile) {
           int64_t rb[4];
@@ -464,16 +391,15 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
             ok = __all_sync(0xffffffffu, w_ok);
             if (!ok) break;
             if (lane == 0) {
-              // chunks 2ks, 2ks + 1 (the last slot: chunk 8 and a zero-filled chunk past the row)
               const uint32_t lb = lead(b_full + 8 * slot), dst = sR + slot * kSlotBytes;
               if (leader) mbar_arrive_expect_tx(b_full + 8 * slot, nbox * kbox_bytes);
               for (int h = 0; h < 2; ++h) {
                 const int kb = 2 * (int)rank + h;
                 if (nb[kb] == 0) continue;
                 const uint32_t d = dst + h * (kSlotBytes / 2);
-                tma_load_4d_pair_hint(d, &a.tm_k, lb, 0, 0, 2 * ks, (int32_t)(rb[kb] >> 3), pol_keep);
+                tma_load_4d_pair_hint(d, &a.tm_k, lb, 0, 0, KC * ks, (int32_t)(rb[kb] >> 3), pol_keep);
                 if (kSub && nb[kb] > 1)
-                  load_more_boxes(kBoxPairHint, &a.tm_k, d, lb, 2 * ks, kbox_bytes, bt, a, tile * kPairKeys + 64 * kb,
+                  load_more_boxes(kBoxPairHint, &a.tm_k, d, lb, KC * ks, kbox_bytes, bt, a, tile * kPairKeys + 64 * kb,
                                   nb[kb], pol_keep);
               }
             }
@@ -490,38 +416,45 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         if (ok && ptile >= 0) ok = load_values(pu, ptile, prb, pnb);
         ptile = -1;
       }
-      // after an abort the odd CTA cannot observe its own loads (they count on the even CTA's
-      // barrier, whose phase may never complete): both producers wait 50 us, far longer than
-      // a load takes, before leaving
+      // after an abort the odd CTA cannot observe its own key and value loads (they count on
+      // the even CTA's barrier, whose phase may never complete): both producers wait 50 us,
+      // far longer than a load takes, before leaving
       if (*abort_flag) {
         const uint64_t t0 = global_timer_ns();
         while (global_timer_ns() - t0 < 50000ull) {
         }
       }
-      // the even CTA waits until the last loads of both CTAs have landed (normally the MMA
-      // issuer already has); a CTA must not leave with copies into its memory in flight
-      if (leader && lane == 0) {
+      // a CTA must not leave with copies into its memory in flight: the even CTA waits until
+      // the last loads of both CTAs have landed (normally the MMA issuer already has), and
+      // with the FP8 cache each CTA for its own last Q
+      if (lane == 0) {
         volatile uint32_t no_abort = 0;
-        for (uint32_t q = r > (uint32_t)kRing ? r - kRing : 0; q < r; ++q)
-          mbar_wait(b_full + 8 * (q % kRing), (q / kRing) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
-        if (uq > 0) mbar_wait(b_qfull, (uq - 1) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
-      }
+        if (leader)
+          for (uint32_t q = r > (uint32_t)kRing ? r - kRing : 0; q < r; ++q)
+            mbar_wait(b_full + 8 * (q % kRing), (q / kRing) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
+        if (uq > 0) {
+          if (FP8) mbar_wait(b_qraw, (uq - 1) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
+          else if (leader) mbar_wait(b_qfull, (uq - 1) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
+        }
       }
     } else if (warp == 1 && leader) {
       // ================================================================ MMA issuer (even CTA)
       if (lane == 0) {
-        // operands bf16, or fp16 for the FP8 cache (E4M3 -> fp16 is exact)
+        // operands bf16 (kind::f16), or E4M3 (kind::f8f6f4: format code 0 is E4M3 there)
         const uint32_t idesc_qk = make_idesc(256, 128, FP8 ? 0u : 1u, 0, 0);
         const uint32_t idesc_pv = make_idesc(256, 128, FP8 ? 0u : 1u, 1, 1);
-        // key slot [2 halves][8 groups][2 chunks][8 rows][128 B]: K-major, 8-row groups 2 KB apart
-        const uint64_t dK0 = make_sdesc(sR, 16, 2048, kSwizzle128);
-        // Q chunk c: [64 rows][128 B] at sQ + 8 KB c, or chunk c of [8 groups][9 chunks][8 rows]
-        const uint64_t dQ0 = make_sdesc(sQ, 16, a.q_whole_rows ? 9 * 1024 : 1024, kSwizzle128);
+        constexpr uint32_t kSw = FP8 ? kSwizzle64 : kSwizzle128;
+        // key slot [2 halves][8 groups][KC chunks][8 rows][row piece]: K-major, 8-row groups 2 KB apart
+        const uint64_t dK0 = make_sdesc(sR, 16, 2048, kSw);
+        // Q chunk c: [64 rows][128 B] at sQ + 8 KB c, or chunk c of [8 groups][9 chunks][8 rows][128 B];
+        // E4M3: the first (hi) and second (lo) 512 bytes of each of those 1 KB blocks, 64-byte rows
+        const uint64_t dQ0 = make_sdesc(sQ, 16, a.q_whole_rows ? 9 * 1024 : 1024, kSw);
         const uint32_t q_chunk = a.q_whole_rows ? 1024 : kQChunk;
-        // value slot [8 groups][4 chunks][8 rows][128 B]: MN-major, chunks 1 KB, groups 4 KB apart
-        const uint64_t dV0 = make_sdesc(sR, 1024, 4096, kSwizzle128);
-        const uint64_t dP0 = make_sdesc(sP, 1024, 1024, kSwizzle128);   // MN-major P^T
-        uint32_t r = 0, n = 0, uc = 0, pvn = 0, kp = 0;   // kp: FP8 key positions
+        // value block [8 groups][4 chunks][8 rows][row piece]: MN-major, chunks 8 rows apart
+        const uint64_t dV0 = make_sdesc(sR, 8 * Cfg::kRowBytes, 32 * Cfg::kRowBytes, kSw);
+        // MN-major P^T: bf16 [256 keys][128 B]; E4M3 [key half][hi, lo][128 keys][64 B]
+        const uint64_t dP0 = FP8 ? make_sdesc(sP, 512, 512, kSwizzle64) : make_sdesc(sP, 1024, 1024, kSwizzle128);
+        uint32_t r = 0, n = 0, uc = 0, pvn = 0;
         bool ok = true;
         struct Prev {
           int L, tile;
@@ -530,22 +463,38 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         } prev{0, -1, false, 0};
         auto issue_pv = [&](const Prev& pv) -> bool {
           if (!wait(b_pfull, pvn & 1)) return false;
-          if (FP8) fence_proxy_async_smem();   // P^T rows that came by st.async, for the MMAs
           if (pv.first && !wait(b_oempty, (pv.uc & 1) ^ 1)) return false;
-          for (int kb = 0; kb < 4; ++kb) {
-            const int valid = pv.L - pv.tile * kPairKeys - 64 * kb;
-            if (valid <= 0) continue;
-            const int ksteps = valid >= 64 ? 4 : (valid + 15) / 16;
+          for (int vs = 0; vs < 4 / Cfg::kBlocksPerSlot; ++vs) {
+            // the producer loads a value slot only if its first block starts before the end
+            if (pv.L - pv.tile * kPairKeys - 64 * Cfg::kBlocksPerSlot * vs <= 0) continue;
             const uint32_t slot = r % kRing;
             if (!wait(b_full + 8 * slot, (r / kRing) & 1)) return false;
             tc_fence_after();
-            const uint64_t ad = dV0 + (uint64_t)(slot * (kSlotBytes >> 4));
-            const uint64_t bd = dP0 + (uint64_t)((64 * kb * 128) >> 4);
-            // M-tile j: output rows 128j.. of each CTA's 256 value columns (its chunks 2j, 2j+1)
-            for (int j = 0; j < 2; ++j)
-              for (int kk = 0; kk < ksteps; ++kk)
-                umma_pair_f16(tmem + kOCol + 128 * j, ad + (uint64_t)((2048 * j + 8192 * kk) >> 4),
-                              bd + kk * (2048 >> 4), idesc_pv, !(pv.first && kb == 0 && kk == 0));
+            for (int i = 0; i < Cfg::kBlocksPerSlot; ++i) {
+              const int kb = vs * Cfg::kBlocksPerSlot + i;
+              const int valid = pv.L - pv.tile * kPairKeys - 64 * kb;
+              if (valid <= 0) continue;
+              const int ksteps = valid >= 64 ? 64 / Cfg::kKStep : (valid + Cfg::kKStep - 1) / Cfg::kKStep;
+              const uint64_t ad = dV0 + (uint64_t)((slot * kSlotBytes + i * Cfg::kBlockBytes) >> 4);
+              if constexpr (FP8) {
+                // P^T of block kb: key half kb / 2, keys 64 (kb % 2) .. of it; lo 8 KB after hi
+                const uint64_t bd = dP0 + (uint64_t)(((kb >> 1) * 16384 + (kb & 1) * 4096) >> 4);
+                // M-tile j: this CTA's value columns 128 j .. (its chunks 2j, 2j + 1)
+                for (int j = 0; j < 2; ++j)
+                  for (int kk = 0; kk < ksteps; ++kk) {
+                    const uint64_t aj = ad + (uint64_t)((1024 * j + 8192 * kk) >> 4);
+                    const uint64_t bk = bd + (uint64_t)((2048 * kk) >> 4);
+                    umma_pair_f8(tmem + kOCol + 128 * j, aj, bk, idesc_pv, !(pv.first && kb == 0 && kk == 0));
+                    umma_pair_f8(tmem + kOCol + 128 * j, aj, bk + (8192 >> 4), idesc_pv, 1u);
+                  }
+              } else {
+                const uint64_t bd = dP0 + (uint64_t)((64 * kb * 128) >> 4);
+                for (int j = 0; j < 2; ++j)
+                  for (int kk = 0; kk < ksteps; ++kk)
+                    umma_pair_f16(tmem + kOCol + 128 * j, ad + (uint64_t)((2048 * j + 8192 * kk) >> 4),
+                                  bd + kk * (2048 >> 4), idesc_pv, !(pv.first && kb == 0 && kk == 0));
+              }
+            }
             umma_pair_commit(b_empty + 8 * slot);
             ++r;
           }
@@ -555,45 +504,36 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         };
         for (int u = u0; u < u1 && ok; ++u, ++uc) {
           const PUnit U = load_punit(a, u);
-          ok = wait(FP8 ? b_qready : b_qfull, uc & 1);   // FP8: converted to fp16 in both CTAs
+          ok = wait(FP8 ? b_qready : b_qfull, uc & 1);   // FP8: hi and lo written in both CTAs
           for (int k = 0; k < U.te - U.tb && ok; ++k, ++n) {
-            // S^T buffer: two alternating (bf16), or one (FP8)
-            const uint32_t sb = FP8 ? 0u : (n & 1), sph = FP8 ? (n & 1) : ((n >> 1) & 1);
+            const uint32_t sb = n & 1, sph = (n >> 1) & 1;   // S^T buffer
             ok = wait(b_sempty + 8 * sb, sph ^ 1);
             const uint32_t d = tmem + sb * 128;
             for (int ks = 0; ks < kKeySlots && ok; ++ks) {
-              const int nc = ks == kKeySlots - 1 ? 1 : 2;     // chunks 2ks, 2ks + 1 (the last: 8)
-              if constexpr (FP8) {
-                const uint32_t kslot = kp % kKeyTSlots;
-                ok = wait(b_kfull + 8 * kslot, (kp / kKeyTSlots) & 1);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t at0 = tmem + kKeyCol + 64 * kslot;     // 32 columns per chunk
-                for (int cc = 0; cc < nc; ++cc) {
-                  const int c = 2 * ks + cc;
-                  const uint64_t bd = dQ0 + (uint64_t)(c * (q_chunk >> 4));
+              const int nc = 9 - KC * ks < KC ? 9 - KC * ks : KC;   // chunks KC ks .. (the last slot: 8)
+              const uint32_t slot = r % kRing;
+              ok = wait(b_full + 8 * slot, (r / kRing) & 1);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t ad = dK0 + (uint64_t)(slot * (kSlotBytes >> 4));
+              for (int cc = 0; cc < nc; ++cc) {
+                const int c = KC * ks + cc;
+                const uint64_t bd = dQ0 + (uint64_t)(c * (q_chunk >> 4));
+                if constexpr (FP8) {
 #pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    umma_pair_f16_ts(d, at0 + 32 * cc + 8 * kk, bd + 2 * kk, idesc_qk, (c | kk) != 0);
-                }
-                umma_pair_commit(b_kempty + 8 * kslot);
-                ++kp;
-              } else {
-                const uint32_t slot = r % kRing;
-                ok = wait(b_full + 8 * slot, (r / kRing) & 1);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t ad = dK0 + (uint64_t)(slot * (kSlotBytes >> 4));
-                for (int cc = 0; cc < nc; ++cc) {
-                  const int c = 2 * ks + cc;
-                  const uint64_t bd = dQ0 + (uint64_t)(c * (q_chunk >> 4));
+                  for (int kk = 0; kk < 2; ++kk) {
+                    const uint64_t ak = ad + (uint64_t)(cc * (512 >> 4) + 2 * kk);
+                    umma_pair_f8(d, ak, bd + 2 * kk, idesc_qk, (c | kk) != 0);           // K . hi
+                    umma_pair_f8(d, ak, bd + (512 >> 4) + 2 * kk, idesc_qk, 1u);         // K . lo
+                  }
+                } else {
 #pragma unroll
                   for (int kk = 0; kk < 4; ++kk)
                     umma_pair_f16(d, ad + (uint64_t)(cc * (1024 >> 4) + 2 * kk), bd + 2 * kk, idesc_qk, (c | kk) != 0);
                 }
-                umma_pair_commit(b_empty + 8 * slot);
-                ++r;
               }
+              umma_pair_commit(b_empty + 8 * slot);
+              ++r;
             }
             if (!ok) break;
             umma_pair_commit(b_sfull + 8 * sb);
@@ -611,153 +551,73 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         volatile uint32_t no_abort = 0;
         mbar_wait(b_drain, 0, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
       }
-  }
-  } else if (FP8 && warp >= 12) {
-    if constexpr (FP8) regs_lower<kRegsConv>();
-    // ================================================================ converters (FP8)
-    // Warps 12-15 take the raw slots in ring order, with the exact hardware convert (two
-    // bytes per instruction). Keys: thread gi converts key row gi of a key position (two
-    // chunks) into tensor-memory key slot kp % 2 at lane gi, from which the QK^T MMAs read
-    // their A operand (key rows past the sequence end are masked by the softmax). Values:
-    // the slot is written as the fp16 operand slot [8 groups][4 chunks][8 rows][128 B]
-    // (MN-major, 128-byte swizzled as a TMA load of bf16 rows would land), rows past the
-    // sequence end as zeros (the cache may hold NaN there, and 0 * NaN is NaN inside the
-    // MMA). Each unit's Q is converted from bf16 to fp16 in place first (a value beyond the
-    // fp16 range is flagged). The even CTA's MMA issuer needs both CTAs' halves of a slot:
-    // the even CTA's converters arrive on its barrier expecting 16 bytes, which the odd CTA's
-    // send with st.async (a remote arrival would hold the sending thread for ~0.85 us).
-    const int gi = threadIdx.x - 384;
-    constexpr uint32_t cbar = 3;                   // named barrier of the 128 converting threads
-    uint32_t rr = 0, fr = 0, kp = 0, uq = 0;       // raw slots, value slots, key positions, units
-    bool ok = true;
-    auto signal_lead = [&](uint32_t bar) {
-      if (leader) mbar_arrive_expect_tx(bar, 16);
-      else st_async_v4(lead(smem_u32(sig_s)), make_uint4(0u, 0u, 0u, 0u), lead(bar));
-    };
-    // key row gi of a raw key slot [2 halves][8 groups][2 chunks][8 rows][64 B], 64-byte
-    // swizzled (the 16-byte unit u of row r at u ^ ((r / 2) % 4)), so that the 32 rows a
-    // warp reads fall in distinct banks
-    const int kr7 = gi & 7;
-    const uint32_t krow_off = (uint32_t)(gi >> 6) * (kRawSlotBytes / 2) + (uint32_t)((gi >> 3) & 7) * 1024u +
-                              (uint32_t)kr7 * 64u;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp & 3) << 21);   // lanes 32 (warp % 4) ..
-    auto convert_keys = [&]() -> bool {
-      const uint32_t rs = rr % kRawRing, ks = kp % kKeyTSlots;
-      const bool mine = gi != 0 || (wait(b_rfull + 8 * rs, (rr / kRawRing) & 1) &&
-                                    wait(b_kempty + 8 * ks, ((kp / kKeyTSlots) & 1) ^ 1));
-      if (named_bar_or(cbar, 128, !mine)) return false;
-      tc_fence_after();
-      const uint8_t* src = gRaw + rs * kRawSlotBytes + krow_off;
-      const uint32_t tbase = lane_base + kKeyCol + 64 * ks;
-#pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        uint4 raw4[4];
+    } else if (FP8 && warp >= 2) {
+      // ================================================================ Q converters (FP8)
+      // Each unit's 64 query rows of this CTA, bf16 as TMA landed them, become q' = q 2^e (the
+      // row's largest |q| in [128, 256)) written as E4M3 hi and lo in place: every 1 KB block
+      // of 8 rows x 64 columns (128-byte swizzled bf16) becomes hi in its first 512 bytes and
+      // lo in its second (8 rows x 64 bytes, 64-byte swizzled each), the QK^T MMAs' B operand.
+      // A warp owns whole 8-row groups (all 9 blocks of them), so its reads of a group precede
+      // its writes there; lane 4 q + p holds 16-byte units p and p + 4 of row q of each block.
+      // The row factors 2^-e go to qf_s for the softmax warpgroup of these rows.
+      constexpr uint32_t cbar = 3;                 // named barrier of the 64 converting threads
+      const int qrow = lane >> 2, part = lane & 3;
+      uint32_t uq = 0;
+      for (int u = u0; u < u1; ++u, ++uq) {
+        bool mine = wait(b_qraw, uq & 1);
+        if (mine && uq > 0) mine = wait(b_qfree, (uq - 1) & 1);   // the previous factors were read
+        if (named_bar_or(cbar, 64, !mine)) break;
+        for (int g = warp - 2; g < 8; g += 2) {
+          uint4 v[18];
+          float mx = 0.f;
 #pragma unroll
-        for (int u16 = 0; u16 < 4; ++u16)
-          raw4[u16] = *reinterpret_cast<const uint4*>(src + cc * 512 + ((u16 ^ ((kr7 >> 1) & 3)) << 4));
-        uint32_t w[32];
+          for (int c = 0; c < 9; ++c) {
+            const uint8_t* blk = gQ + (a.q_whole_rows ? g * 9216 + c * 1024 : c * kQChunk + g * 1024) + qrow * 128;
 #pragma unroll
-        for (int u16 = 0; u16 < 4; ++u16) {
-          const uint32_t b4[4] = {raw4[u16].x, raw4[u16].y, raw4[u16].z, raw4[u16].w};
+            for (int h = 0; h < 2; ++h) {
+              v[2 * c + h] = *reinterpret_cast<const uint4*>(blk + (((part + 4 * h) ^ qrow) << 4));
+              const uint32_t w[4] = {v[2 * c + h].x, v[2 * c + h].y, v[2 * c + h].z, v[2 * c + h].w};
 #pragma unroll
-          for (int k2 = 0; k2 < 4; ++k2) {
-            w[8 * u16 + 2 * k2] = e4m3x2_to_f16x2(b4[k2] & 0xFFFFu);
-            w[8 * u16 + 2 * k2 + 1] = e4m3x2_to_f16x2(b4[k2] >> 16);
+              for (int k = 0; k < 4; ++k) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+            }
           }
-        }
-        tmem_st16u(tbase + 32 * cc, w);
-        tmem_st16u(tbase + 32 * cc + 16, w + 16);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      named_bar_sync(cbar, 128);
-      if (gi == 0) {
-        mbar_arrive(b_rempty + 8 * rs);
-        signal_lead(b_kfull + 8 * ks);
-      }
-      ++rr;
-      ++kp;
-      return true;
-    };
-    // one 64-key value block: raw slot rr [8 groups][4 chunks][8 rows][64 B] into value slot
-    // fr; rows at or past `valid` are zeros
-    auto convert_value_slot = [&](int valid) -> bool {
-      const uint32_t rs = rr % kRawRing, fs = fr % kRing;
-      const bool mine = gi != 0 || (wait(b_rfull + 8 * rs, (rr / kRawRing) & 1) &&
-                                    wait(b_empty + 8 * fs, ((fr / kRing) & 1) ^ 1));
-      if (named_bar_or(cbar, 128, !mine)) return false;
-      const uint8_t* src = gRaw + rs * kRawSlotBytes;
-      uint8_t* dst = gR + fs * kSlotBytes;
-#pragma unroll 2
-      for (int j = 0; j < 8; ++j) {
-        // 16-byte raw unit idx: column q4 of row `row` of the 1 KB operand block idx / 32
-        // (group idx / 128, chunk (idx / 32) % 4)
-        const int idx = gi + 128 * j, q4 = idx & 3, row = (idx >> 2) & 7;
-        uint4 v = *reinterpret_cast<const uint4*>(src + 16 * idx);
-        if ((idx >> 7) * 8 + row >= valid) v = make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t b4[4] = {v.x, v.y, v.z, v.w};
-        uint32_t hh[8];
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          // e = 7 - floor(log2 max|q|), so that the row's largest |q'| lies in [128, 256)
+          int e = 0;
+          if (mx > 0.f) e = min(max(7 - ((int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127), -126), 126);
+          const float f = __uint_as_float((uint32_t)(e + 127) << 23);
+          __syncwarp();
 #pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-          hh[2 * k2] = e4m3x2_to_f16x2(b4[k2] & 0xFFFFu);
-          hh[2 * k2 + 1] = e4m3x2_to_f16x2(b4[k2] >> 16);
-        }
-        uint8_t* drow = dst + (idx >> 5) * 1024 + row * 128;
-        *reinterpret_cast<uint4*>(drow + (((2 * q4) ^ row) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-        *reinterpret_cast<uint4*>(drow + (((2 * q4 + 1) ^ row) << 4)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(cbar, 128);
-      if (gi == 0) {
-        mbar_arrive(b_rempty + 8 * rs);
-        signal_lead(b_full + 8 * fs);
-      }
-      ++rr;
-      ++fr;
-      return true;
-    };
-    auto convert_values = [&](const PUnit& U, int tile) -> bool {
-      for (int kb = 0; kb < 4; ++kb) {
-        const int valid = U.L - tile * kPairKeys - 64 * kb;
-        if (valid > 0 && !convert_value_slot(valid)) return false;
-      }
-      return true;
-    };
-    for (int u = u0; u < u1 && ok; ++u, ++uq) {
-      const PUnit U = load_punit(a, u);
-      // ---- Q, bf16 -> fp16 in place (the 128-byte swizzle moves whole 16-byte units)
-      {
-        const bool mine = gi != 0 || wait(b_qraw, uq & 1);
-        if (named_bar_or(cbar, 128, !mine)) { ok = false; break; }
-        bool q_bad = false;
-        for (int i = gi; i < kPairQBytes / 16; i += 128) {
-          uint4* qp = reinterpret_cast<uint4*>(gQ + 16 * i);
-          const uint4 v = *qp;
-          uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          for (int c = 0; c < 9; ++c) {
+            uint8_t* blk = gQ + (a.q_whole_rows ? g * 9216 + c * 1024 : c * kQChunk + g * 1024);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float lo = __uint_as_float(w[k] << 16), hi = __uint_as_float(w[k] & 0xFFFF0000u);
-            q_bad |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
-            __half2 h = __floats2half2_rn(lo, hi);
-            w[k] = *reinterpret_cast<uint32_t*>(&h);
+            for (int h = 0; h < 2; ++h) {
+              const int un = part + 4 * h;           // columns 8 un .. 8 un + 7 of the block
+              const uint32_t w[4] = {v[2 * c + h].x, v[2 * c + h].y, v[2 * c + h].z, v[2 * c + h].w};
+              uint32_t o[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) o[k] = split_e4m3x2(bf16_lo(w[k]) * f, bf16_hi(w[k]) * f);
+              // 8 bytes: half (un % 2) of the 16-byte unit un / 2 of the 64-byte row
+              const uint32_t off = qrow * 64 + (((un >> 1) ^ ((qrow >> 1) & 3)) << 4) + (un & 1) * 8;
+              *reinterpret_cast<uint2*>(blk + off) = make_uint2(__byte_perm(o[0], o[1], 0x5410), __byte_perm(o[2], o[3], 0x5410));
+              *reinterpret_cast<uint2*>(blk + 512 + off) =
+                  make_uint2(__byte_perm(o[0], o[1], 0x7632), __byte_perm(o[2], o[3], 0x7632));
+            }
           }
-          *qp = make_uint4(w[0], w[1], w[2], w[3]);
+          if (part == 0) qf_s[8 * g + qrow] = __uint_as_float((uint32_t)(127 - e) << 23);
         }
-        if (q_bad) atomicOr(err, MLA_DEVERR_Q_RANGE);
         fence_proxy_async_smem();
-        named_bar_sync(cbar, 128);
-        if (gi == 0) signal_lead(b_qready);
+        named_bar_sync(cbar, 64);
+        if (threadIdx.x == 64) {
+          mbar_arrive(b_qsc);
+          // the even CTA's MMA issuer needs both CTAs' Q: the odd CTA signals by st.async
+          if (leader) mbar_arrive_expect_tx(b_qready, 16);
+          else st_async_v4(lead(smem_u32(sig_s)), make_uint4(0u, 0u, 0u, 0u), lead(b_qready));
+        }
       }
-      int pt = -1;
-      for (int tile = U.tb; tile < U.te && ok; ++tile) {
-        for (int ks = 0; ks < kKeySlots && ok; ++ks) ok = convert_keys();
-        if (ok && pt >= 0) ok = convert_values(U, pt);
-        pt = tile;
-      }
-      if (ok && pt >= 0) ok = convert_values(U, pt);
     }
   } else if (warp >= 4) {
-    if constexpr (FP8) regs_raise<kRegsSoftmax>();
     // ================================================================ softmax / epilogue
     const int wg = (warp - 4) >> 2;                // rows 64 wg .. 64 wg + 63
     const int wl = warp & 3;                       // TMEM lane quarter
@@ -769,6 +629,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
     const float c_log2 = a.softmax_scale * kvs * kPLog2e;
     const float kvo = kvs;
     float* mref = mref_s[wg];
+    const float* rowc = rowc_s[wg];
     uint32_t gn = 0, xc = 0;
     bool ok = true;
     auto wait_wg = [&](uint32_t b, uint32_t parity) -> bool { return !named_bar_or(bar, 128, !wait(b, parity)); };
@@ -844,6 +705,19 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         mref[t] = -INFINITY;
         nvis_s[wg][t] = a.causal ? min(U.L, U.L - a.s_q + 1 + (row0 + t) / a.H) : U.L;
       }
+      if constexpr (FP8) {
+        // the unit's row factors 2^-e: from this CTA's converters for the warpgroup whose rows
+        // live here, which passes them to the same warpgroup of the peer
+        if (local_p) {
+          ok = wait_wg(b_qsc, ui & 1);
+          if (!ok) break;
+          if (t < 64) own_s[wg][t] = qf_s[t];
+        }
+        const float* px = exchange(0u, own_s[wg]);
+        if (px == nullptr) { ok = false; break; }
+        if (local_p && t == 0) mbar_arrive(b_qfree);
+        if (t < 64) rowc_s[wg][t] = c_log2 * (local_p ? own_s[wg][t] : px[4 + t]);
+      }
       const int mask_from = a.causal ? U.L - a.s_q + 1 : U.L;
 #pragma unroll
       for (int i = 0; i < 64; ++i) lsum[i] = 0.f;
@@ -855,7 +729,7 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
           ok = wait_wg(b_never, 0);                  // tests: this wait runs out
           if (!ok) break;
         }
-        const uint32_t sb = FP8 ? 0u : (n & 1), sph = FP8 ? (n & 1) : ((n >> 1) & 1);   // S^T buffer
+        const uint32_t sb = n & 1, sph = (n >> 1) & 1;   // S^T buffer
         ok = wait_wg(b_sfull + 8 * sb, sph);
         if (!ok) break;
         tc_fence_after();
@@ -867,15 +741,26 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
 
         const int j = tile * kPairKeys + 128 * (int)rank + t;
         bool need = false;
+        // the score factor of 4 rows: bf16 one constant, FP8 per row (2^-e of its q)
+        auto factors = [&](int r, float* cc) {
+          if constexpr (FP8) {
+            const float4 c4 = *reinterpret_cast<const float4*>(rowc + r);
+            cc[0] = c4.x; cc[1] = c4.y; cc[2] = c4.z; cc[3] = c4.w;
+          } else {
+            cc[0] = cc[1] = cc[2] = cc[3] = c_log2;
+          }
+        };
         if ((tile + 1) * kPairKeys <= mask_from) {
 #pragma unroll
           for (int r = 0; r < 64; r += 4) {
             const float4 m4 = *reinterpret_cast<const float4*>(mref + r);
             const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+            float cc[4];
+            factors(r, cc);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              s[r + i] *= c_log2;
-              need |= s[r + i] > mm[i] + kPairRescaleLog2;
+              s[r + i] *= cc[i];
+              need |= s[r + i] > mm[i] + Cfg::kRescaleLog2;
             }
           }
         } else {
@@ -883,32 +768,23 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
           for (int r = 0; r < 64; r += 4) {
             const float4 m4 = *reinterpret_cast<const float4*>(mref + r);
             const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+            float cc[4];
+            factors(r, cc);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              s[r + i] = j < nvis_s[wg][r + i] ? s[r + i] * c_log2 : -INFINITY;
-              need |= s[r + i] > mm[i] + kPairRescaleLog2;
+              s[r + i] = j < nvis_s[wg][r + i] ? s[r + i] * cc[i] : -INFINITY;
+              need |= s[r + i] > mm[i] + Cfg::kRescaleLog2;
             }
           }
         }
-        // the barrier also orders every thread's S^T reads before the even CTA's signal
+        // the barrier also orders every thread's S^T reads before the even CTA's signal; the
+        // odd CTA's S^T reads precede its P^T signal, which the MMA issuer awaits before it
+        // reuses the buffer two tiles later
         const bool need_local = named_bar_or(bar, 128, need);
-        // bf16: the odd CTA's S^T reads precede its P^T signal, which the MMA issuer awaits
-        // before it reuses the buffer two tiles later. FP8 (one S^T buffer): the even CTA's
-        // warpgroups arrive expecting 16 bytes each, which the odd CTA's warpgroups send by
-        // st.async once their reads are done.
-        if (t == 0) {
-          if (!FP8) {
-            if (leader) mbar_arrive(b_sempty + 8 * sb);
-          } else if (leader) {
-            mbar_arrive_expect_tx(b_sempty + 8 * sb, 16);
-          } else {
-            st_async_v4(lead(smem_u32(sig_s)), make_uint4(0u, 0u, 0u, 0u), lead(b_sempty + 8 * sb));
-          }
-        }
+        if (leader && t == 0) mbar_arrive(b_sempty + 8 * sb);
         if (need_local) {
           // column maxima of the warp's 32 keys for all 64 rows at once (reduce-scatter,
-          // as for the row sums; shuffles rather than 64 redux operations, which the
-          // converting warps' convert instructions slow down in the FP8 kernel)
+          // as for the row sums)
           float m0, m1;
           reduce_rows_max(s, m0, m1);
           wred_s[wg][wl][2 * lane] = m0;
@@ -935,34 +811,33 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
           for (int r = 0; r < 64; ++r) lsum[r] *= alpha_s[wg][r];
           rescale = k > 0;
         }
+        // bf16: 32 words of P^T pairs. FP8: P times 2^4, its hi bytes (words 0-15) and lo
+        // bytes (words 16-31), four rows per word
         uint32_t pw[32];
 #pragma unroll
         for (int r = 0; r < 64; r += 4) {
           const float4 m4 = *reinterpret_cast<const float4*>(mref + r);
-          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+          const float mm[4] = {m4.x - Cfg::kPOffLog2, m4.y - Cfg::kPOffLog2, m4.z - Cfg::kPOffLog2,
+                               m4.w - Cfg::kPOffLog2};
+          float p[4];
 #pragma unroll
-          for (int i = 0; i < 4; i += 2) {
-            const float p0 = s[r + i] == -INFINITY ? 0.f : ex2_approx(s[r + i] - mm[i]);
-            const float p1 = s[r + i + 1] == -INFINITY ? 0.f : ex2_approx(s[r + i + 1] - mm[i + 1]);
-            if constexpr (FP8) {                 // the MMA operand type: fp16 with the FP8 cache
-              __half2 h = __floats2half2_rn(p0, p1);
-              pw[(r + i) / 2] = *reinterpret_cast<uint32_t*>(&h);
-            } else {
-              __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-              pw[(r + i) / 2] = *reinterpret_cast<uint32_t*>(&h);
-            }
-            lsum[r + i] += p0;                 // the normaliser sums the unrounded values
-            lsum[r + i + 1] += p1;
+          for (int i = 0; i < 4; ++i) {
+            p[i] = s[r + i] == -INFINITY ? 0.f : ex2_approx(s[r + i] - mm[i]);
+            lsum[r + i] += p[i];                 // the normaliser sums the unrounded values
+          }
+          if constexpr (FP8) {
+            const uint32_t o0 = split_e4m3x2(p[0], p[1]), o1 = split_e4m3x2(p[2], p[3]);
+            pw[r / 4] = __byte_perm(o0, o1, 0x5410);
+            pw[16 + r / 4] = __byte_perm(o0, o1, 0x7632);
+          } else {
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(p[0], p[1]), h1 = __floats2bfloat162_rn(p[2], p[3]);
+            pw[r / 2] = *reinterpret_cast<uint32_t*>(&h0);
+            pw[r / 2 + 1] = *reinterpret_cast<uint32_t*>(&h1);
           }
         }
         // P^T and O^T are free once the previous PV has completed; the staging buffer once
         // the previous copy out of it has been read
-        if (!FP8 && t == 0 && !local_p) bulk_wait_read0();
-        // FP8: the other warpgroup's previous epilogue used the upper half of this P^T region
-        if (FP8 && local_p && k == 0 && ui > 0) {
-          ok = wait_wg(b_epi, (ui - 1) & 1);
-          if (!ok) break;
-        }
+        if (t == 0 && !local_p) bulk_wait_read0();
         if (n > 0) {
           ok = wait_wg(b_pvdone, (n - 1) & 1);
           if (!ok) break;
@@ -987,22 +862,24 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
           tmem_wait_st();
         }
         // P^T row of key 128 rank + t: into this CTA's P^T buffer (rows 64 rank ..), or, for
-        // the peer, into the staging buffer laid out as the peer's P^T rows 128 rank ..
-        // 128 rank + 127 (bf16), or straight into the peer's P^T by st.async, its bytes
-        // counted on the peer's barrier (FP8: no room for a staging buffer)
-        if (FP8 && !local_p) {
-          const uint32_t pdst = map_to_rank(sP + (uint32_t)rank * kStageBytes, peer);
-          const uint32_t pbar = map_to_rank(leader ? b_pin : b_pfull, peer);
+        // the peer, into the staging buffer laid out as the peer's P^T rows of keys
+        // 128 rank .. 128 rank + 127
+        {
+          uint8_t* prow = local_p ? gP + (int)rank * kStageBytes : gStage;
+          if constexpr (FP8) {
 #pragma unroll
-          for (int u16 = 0; u16 < 8; ++u16)
-            st_async_v4(pdst + p_off128(t, u16), make_uint4(pw[4 * u16], pw[4 * u16 + 1], pw[4 * u16 + 2], pw[4 * u16 + 3]),
-                        pbar);
-        } else {
-          uint8_t* prow = local_p ? gP + 128 * (int)rank * 128 : gStage;
+            for (int hl = 0; hl < 2; ++hl)
 #pragma unroll
-          for (int u16 = 0; u16 < 8; ++u16)
-            *reinterpret_cast<uint4*>(prow + p_off128(t, u16)) =
-                make_uint4(pw[4 * u16], pw[4 * u16 + 1], pw[4 * u16 + 2], pw[4 * u16 + 3]);
+              for (int u16 = 0; u16 < 4; ++u16)
+                *reinterpret_cast<uint4*>(prow + hl * 8192 + p_off64(t, u16)) =
+                    make_uint4(pw[16 * hl + 4 * u16], pw[16 * hl + 4 * u16 + 1], pw[16 * hl + 4 * u16 + 2],
+                               pw[16 * hl + 4 * u16 + 3]);
+          } else {
+#pragma unroll
+            for (int u16 = 0; u16 < 8; ++u16)
+              *reinterpret_cast<uint4*>(prow + p_off128(t, u16)) =
+                  make_uint4(pw[4 * u16], pw[4 * u16 + 1], pw[4 * u16 + 2], pw[4 * u16 + 3]);
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -1010,18 +887,15 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         if (t == 0) {
           if (!local_p) {
             // rows for the peer's P^T: one bulk copy, counted on the peer's barrier (the even
-            // CTA's P^T barrier, or the odd CTA's b_pin); FP8: already sent
-            if (!FP8) {
-              bulk_copy_to_cluster(map_to_rank(sP + (uint32_t)rank * kStageBytes, peer), sStage, kStageBytes,
-                                   map_to_rank(leader ? b_pin : b_pfull, peer));
-              bulk_commit();
-            }
+            // CTA's P^T barrier, or the odd CTA's b_pin)
+            bulk_copy_to_cluster(map_to_rank(sP + (uint32_t)rank * kStageBytes, peer), sStage, kStageBytes,
+                                 map_to_rank(leader ? b_pin : b_pfull, peer));
+            bulk_commit();
           } else if (leader) {
             mbar_arrive_expect_tx(b_pfull, kStageBytes);   // own rows; the odd CTA's copy to come
           } else {
             mbar_arrive_expect_tx(b_pin, kStageBytes);
             ok = mbar_wait(b_pin, n & 1, abort_flag, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);   // the even CTA's copy
-            if (FP8 && ok) fence_proxy_async_smem();   // rows that came by st.async, for the MMAs
             if (ok) mbar_arrive_cluster(lead(b_pfull));
             else fail_peer();
           }
@@ -1055,13 +929,11 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
       // own half of the P^T buffer for the warpgroup whose rows live here (no other agent
       // writes it before this warpgroup's next P^T), else the staging buffer once its last
       // copy to the peer has been read.
-      // FP8 has no staging buffer: its other warpgroup uses the upper half of the same
-      // region, and the P^T rows of the next unit wait for it (b_epi).
-      if (!FP8 && !local_p) {
+      if (!local_p) {
         if (t == 0) bulk_wait_read0();
         named_bar_sync(bar, 128);
       }
-      uint8_t* scratch = local_p ? gP + (int)rank * kStageBytes : FP8 ? gP + (int)rank * kStageBytes + 8192 : gStage;
+      uint8_t* scratch = local_p ? gP + (int)rank * kStageBytes : gStage;
       float* stage = reinterpret_cast<float*>(scratch) + wl * 512;
       const int nrows = min(64, R - row0);         // rows of this warpgroup that exist
       const int si = lane >> 1, sh = lane & 1;
@@ -1114,12 +986,12 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
         }
       }
       if (rank == 0 && t < 64 && row0 + t < R) {
-        const float l = tot > 0.f ? (mref[t] + __log2f(tot)) * kPLn2 : -INFINITY;
+        // P was computed times 2^kPOffLog2, and so was the row sum
+        const float l = tot > 0.f ? (mref[t] + __log2f(tot) - Cfg::kPOffLog2) * kPLn2 : -INFINITY;
         if (direct) a.lse[(int64_t)U.b * R + row0 + t] = l;
         else a.part_lse[(int64_t)U.slot * 128 + 64 * wg + t] = l;
       }
       named_bar_sync(bar, 128);
-      if (FP8 && !local_p && t == 0) mbar_arrive(b_epi);   // its scratch reads are done
       gn += T;
     }
     // a copy out of the staging buffer has landed before the CTA may leave
@@ -1136,26 +1008,22 @@ __global__ void __launch_bounds__(PairCfg<FP8>::kThreads, 1) decode_pair_kernel(
 
 template <bool FP8, bool kSub>
 static cudaError_t prepare_pair_variant() {
-  using Cfg = PairCfg<FP8>;
   cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<FP8, kSub>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg::kDynBytes);
+                                       kPairDynBytes);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes attr;
   e = cudaFuncGetAttributes(&attr, decode_pair_kernel<FP8, kSub>);
   if (e != cudaSuccess) return e;
   if ((int)attr.sharedSizeBytes > kPairStaticBudget) return cudaErrorInvalidConfiguration;
-  // the FP8 kernel's register budgets redistribute exactly 128 registers per thread
-  if (FP8 && attr.numRegs != 128) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
 
 template <bool FP8>
 static cudaError_t launch_pair_variant(const DecodeArgs& a, int pairs, cudaStream_t s) {
-  using Cfg = PairCfg<FP8>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(Cfg::kThreads);
-  cfg.dynamicSmemBytes = Cfg::kDynBytes;
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = kPairDynBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

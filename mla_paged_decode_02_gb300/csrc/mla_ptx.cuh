@@ -246,7 +246,8 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 // Instruction descriptor, kind::f16 with float32 accumulation (tcgen05 instruction
 // descriptor fields: D format [4,6), A format [7,10), B format [10,13), A major bit 15,
 // B major bit 16, N>>3 at [17,23), M>>4 at [24,29)).
-// ab_bf16: 1 = bf16 operands, 0 = fp16. a_mn / b_mn: 1 = MN-major, 0 = K-major.
+// ab_bf16: 1 = bf16 operands, 0 = fp16 (kind::f16) or E4M3 (kind::f8f6f4).
+// a_mn / b_mn: 1 = MN-major, 0 = K-major.
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t m, uint32_t n, uint32_t ab_bf16,
                                                   uint32_t a_mn, uint32_t b_mn) {
   return (1u << 4) | (ab_bf16 << 7) | (ab_bf16 << 10) | (a_mn << 15) | (b_mn << 16) |
@@ -391,6 +392,15 @@ __device__ __forceinline__ void umma_pair_f16_ts(uint32_t d_tmem, uint32_t a_tme
                "setp.ne.b32 p, %4, 0;\n\t"
                "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
                :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// The same with E4M3 operands from shared memory (kind::f8f6f4; format code 0 of the
+// instruction descriptor's A and B fields is E4M3 there), K = 32 per instruction.
+__device__ __forceinline__ void umma_pair_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "setp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+               :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 // Arrive once on the mbarrier at this offset in BOTH CTAs when every pair MMA this thread
 // issued so far has completed.
