@@ -383,8 +383,15 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
           int nb[4];
           block_rows<kSub>(a, U, tile, rb, nb);
           const int32_t* bt = bt_all + (int64_t)U.b * a.MB;
-          // bytes of both CTAs' key halves (the even CTA arms the barrier for both)
-          const uint32_t nbox = (uint32_t)(nb[0] + nb[1] + nb[2] + nb[3]);
+          // Bytes of both CTAs' key halves (the even CTA arms the barrier for both). Every key
+          // slot needs bytes from both CTAs: the odd CTA's half of a super-tile that lies past
+          // the sequence end gets one box of rows the even CTA reads anyway (the softmax masks
+          // those keys). Were it to load nothing, the slot could complete on the even CTA's
+          // bytes alone and be consumed and released again before the odd producer waits for
+          // its previous release, and a parity wait cannot tell those two phases apart.
+          const int nown = nb[2 * rank] + nb[2 * rank + 1];   // this CTA's key boxes
+          const int nodd = nb[2] + nb[3];
+          const uint32_t nbox = (uint32_t)(nb[0] + nb[1] + (nodd > 0 ? nodd : 1));
           for (int ks = 0; ks < kKeySlots; ++ks) {
             const uint32_t slot = r % kRing;
             w_ok = lane != 0 || wait(b_empty + 8 * slot, ((r / kRing) & 1) ^ 1);
@@ -393,6 +400,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
             if (lane == 0) {
               const uint32_t lb = lead(b_full + 8 * slot), dst = sR + slot * kSlotBytes;
               if (leader) mbar_arrive_expect_tx(b_full + 8 * slot, nbox * kbox_bytes);
+              if (nown == 0)        // odd CTA, half past the end: one box of the even CTA's first rows
+                tma_load_4d_pair_hint(dst, &a.tm_k, lb, 0, 0, KC * ks, (int32_t)(rb[0] >> 3), pol_keep);
               for (int h = 0; h < 2; ++h) {
                 const int kb = 2 * (int)rank + h;
                 if (nb[kb] == 0) continue;

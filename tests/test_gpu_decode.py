@@ -136,6 +136,26 @@ def test_decode_matches_oracle_small(B, s_q, H, P, lens, kv, causal):
     compare(case, out, lse, ro, rl)
 
 
+@pytest.mark.parametrize("kv", [BF, F8])
+def test_pair_units_whose_odd_half_is_past_the_end_never_stall(kv):
+    """CTA pairs: with 16 row groups over two sequences, pairs take a one-tile unit and then
+    a unit whose second super-tile holds keys only in the even CTA's half. Every key slot
+    needs bytes from both CTAs, so the odd CTA's producer stays in step with the slot's
+    releases; before that, one run in ~14 stalled until the wait bound. Repeated calls must
+    all succeed and give bit-identical results equal to the oracle's."""
+    case = synth.make_case(B=2, s_q=16, H=128, page_size=64, seq_lens=[300, 2000], seed=31 + 2 + 128,
+                           kv_dtype=kv, causal=True)
+    g = GpuCase(case)
+    out0, lse0 = [t.clone() for t in g.decode()]
+    assert api.decode_check(g.workspace) == (0, 0)
+    ro, rl = oracle_decode(case, g.cache_numpy())
+    compare(case, out0, lse0, ro, rl)
+    for _ in range(24):
+        out, lse = g.decode()
+        assert api.decode_check(g.workspace) == (0, 0)
+        assert torch.equal(out, out0) and torch.equal(lse, lse0)
+
+
 def test_config1_tiny_full():
     case = synth.make_config(1)
     g = GpuCase(case)
