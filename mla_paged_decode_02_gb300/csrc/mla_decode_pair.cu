@@ -146,6 +146,24 @@ __device__ __forceinline__ uint32_t p_off64(int row, int u) {    // 64-byte swiz
   return (uint32_t)(row >> 3) * 512u + (uint32_t)(row & 7) * 64u + ((uint32_t)(u ^ ((row >> 1) & 3)) << 4);
 }
 
+// 4 x 4 transpose inside each quad of lanes: lane j of the quad holds a[i] = M[i][j] before
+// and a[k] = M[j][k] after (2 x 2 blocks first, then the blocks).
+__device__ __forceinline__ void quad_transpose4(uint32_t* a, int j) {
+  const bool odd = (j & 1) != 0, up = (j & 2) != 0;
+#pragma unroll
+  for (int i = 0; i < 4; i += 2) {
+    const uint32_t r = __shfl_xor_sync(0xffffffffu, odd ? a[i] : a[i + 1], 1);
+    if (odd) a[i] = r;
+    else a[i + 1] = r;
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t r = __shfl_xor_sync(0xffffffffu, up ? a[i] : a[i + 2], 2);
+    if (up) a[i] = r;
+    else a[i + 2] = r;
+  }
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -577,33 +595,40 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
         if (mine && uq > 0) mine = wait(b_qfree, (uq - 1) & 1);   // the previous factors were read
         if (named_bar_or(cbar, 64, !mine)) break;
         for (int g = warp - 2; g < 8; g += 2) {
-          uint4 v[18];
-          float mx = 0.f;
+          auto block_of = [&](int c) -> uint8_t* {
+            return gQ + (a.q_whole_rows ? g * 9216 + c * 1024 : c * kQChunk + g * 1024);
+          };
+          // pass 1: the row's largest |q| (this lane's 18 units, then the row's 4 lanes)
+          __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
 #pragma unroll
-          for (int c = 0; c < 9; ++c) {
-            const uint8_t* blk = gQ + (a.q_whole_rows ? g * 9216 + c * 1024 : c * kQChunk + g * 1024) + qrow * 128;
+          for (int c = 0; c < 9; ++c)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              v[2 * c + h] = *reinterpret_cast<const uint4*>(blk + (((part + 4 * h) ^ qrow) << 4));
-              const uint32_t w[4] = {v[2 * c + h].x, v[2 * c + h].y, v[2 * c + h].z, v[2 * c + h].w};
+              const uint4 v = *reinterpret_cast<const uint4*>(block_of(c) + qrow * 128 + (((part + 4 * h) ^ qrow) << 4));
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int k = 0; k < 4; ++k) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+              for (int k = 0; k < 4; ++k) m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[k])));
             }
-          }
+          float mx = fmaxf(__low2float(m2), __high2float(m2));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
           // e = 7 - floor(log2 max|q|), so that the row's largest |q'| lies in [128, 256)
           int e = 0;
           if (mx > 0.f) e = min(max(7 - ((int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127), -126), 126);
           const float f = __uint_as_float((uint32_t)(e + 127) << 23);
-          __syncwarp();
-#pragma unroll
+          // pass 2, block by block: the warp's reads of a block precede its writes there
+#pragma unroll 3
           for (int c = 0; c < 9; ++c) {
-            uint8_t* blk = gQ + (a.q_whole_rows ? g * 9216 + c * 1024 : c * kQChunk + g * 1024);
+            uint8_t* blk = block_of(c);
+            uint4 v[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              v[h] = *reinterpret_cast<const uint4*>(blk + qrow * 128 + (((part + 4 * h) ^ qrow) << 4));
+            __syncwarp();
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int un = part + 4 * h;           // columns 8 un .. 8 un + 7 of the block
-              const uint32_t w[4] = {v[2 * c + h].x, v[2 * c + h].y, v[2 * c + h].z, v[2 * c + h].w};
+              const uint32_t w[4] = {v[h].x, v[h].y, v[h].z, v[h].w};
               uint32_t o[4];
 #pragma unroll
               for (int k = 0; k < 4; ++k) o[k] = split_e4m3x2(bf16_lo(w[k]) * f, bf16_hi(w[k]) * f);
@@ -932,20 +957,12 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       named_bar_sync(bar, 128);
       const bool direct = U.slot < 0;
       // Each warp holds value columns 256 rank + 128 jt + 32 wl + lane (its TMEM lanes) of 16
-      // rows per load. It transposes them through 2 KB of shared memory, 16-byte blocks
-      // XOR-swizzled by row, so that each lane stores 16 consecutive columns of one row
-      // (16-byte stores instead of one store per row and column). The scratch is this CTA's
-      // own half of the P^T buffer for the warpgroup whose rows live here (no other agent
-      // writes it before this warpgroup's next P^T), else the staging buffer once its last
-      // copy to the peer has been read.
-      if (!local_p) {
-        if (t == 0) bulk_wait_read0();
-        named_bar_sync(bar, 128);
-      }
-      uint8_t* scratch = local_p ? gP + (int)rank * kStageBytes : gStage;
-      float* stage = reinterpret_cast<float*>(scratch) + wl * 512;
+      // rows per load. Each quad of lanes transposes 4 x 4 blocks of them in registers (two
+      // shuffle steps), after which lane 4q + j holds row j of a block at 4 consecutive
+      // columns: 8-byte (bf16 output) or 16-byte (float32 partial) stores, and no shared
+      // memory traffic next to the MMAs of the next unit.
       const int nrows = min(64, R - row0);         // rows of this warpgroup that exist
-      const int si = lane >> 1, sh = lane & 1;
+      const int qj = lane & 3;
 #pragma unroll 1
       for (int jt = 0; jt < 2; ++jt) {
 #pragma unroll 1
@@ -960,36 +977,39 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
             if (leader && t == 0) mbar_arrive(b_oempty);
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            stage[i * 32 + ((((lane >> 2) ^ (i & 7)) << 2) | (lane & 3))] = o[i] * alpha_s[wg][16 * c + i];
-          __syncwarp();
-          float v[16];
+          for (int i = 0; i < 16; ++i) o[i] *= alpha_s[wg][16 * c + i];
+          const int col = 256 * (int)rank + 128 * jt + 32 * wl + 4 * (lane >> 2);
+          if (direct) {
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const float4 x = *reinterpret_cast<const float4*>(stage + si * 32 + (((4 * sh + m) ^ (si & 7)) << 2));
-            v[4 * m] = x.x;
-            v[4 * m + 1] = x.y;
-            v[4 * m + 2] = x.z;
-            v[4 * m + 3] = x.w;
-          }
-          __syncwarp();
-          const int r = 16 * c + si;               // row 64 wg + r of the unit
-          const int col = 256 * (int)rank + 128 * jt + 32 * wl + 16 * sh;
-          if (r < nrows) {
-            if (direct) {
-              uint32_t w[8];
+            for (int bp = 0; bp < 2; ++bp) {
+              // rows 8 bp + i (low halves) and 8 bp + 4 + i (high halves) as bf16 pairs
+              uint32_t w[4];
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
-                w[k] = *reinterpret_cast<uint32_t*>(&h);
+              for (int i = 0; i < 4; ++i) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(o[8 * bp + i], o[8 * bp + 4 + i]);
+                w[i] = *reinterpret_cast<uint32_t*>(&h);
               }
-              uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)U.b * R + row0 + r) * kDV + col);
-              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            } else {
-              float4* dst = reinterpret_cast<float4*>(a.part_o + ((int64_t)U.slot * 128 + 64 * wg + r) * kDV + col);
+              quad_transpose4(w, qj);
+              const int r0 = 16 * c + 8 * bp + qj;   // rows r0 (low halves) and r0 + 4 (high)
+              if (r0 < nrows)
+                *reinterpret_cast<uint2*>(a.out + ((int64_t)U.b * R + row0 + r0) * kDV + col) =
+                    make_uint2(__byte_perm(w[0], w[1], 0x5410), __byte_perm(w[2], w[3], 0x5410));
+              if (r0 + 4 < nrows)
+                *reinterpret_cast<uint2*>(a.out + ((int64_t)U.b * R + row0 + r0 + 4) * kDV + col) =
+                    make_uint2(__byte_perm(w[0], w[1], 0x7632), __byte_perm(w[2], w[3], 0x7632));
+            }
+          } else {
 #pragma unroll
-              for (int m = 0; m < 4; ++m) dst[m] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
+            for (int blk = 0; blk < 4; ++blk) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) w[i] = __float_as_uint(o[4 * blk + i]);
+              quad_transpose4(w, qj);
+              const int r = 16 * c + 4 * blk + qj;   // row 64 wg + r of the unit
+              if (r < nrows)
+                *reinterpret_cast<float4*>(a.part_o + ((int64_t)U.slot * 128 + 64 * wg + r) * kDV + col) =
+                    make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]),
+                                __uint_as_float(w[3]));
             }
           }
         }
