@@ -167,17 +167,19 @@ __device__ __forceinline__ void quad_transpose4(uint32_t* a, int j) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// x0, x1 (|x| < 448) as E4M3 pairs hi = e4m3(x), lo = e4m3(x - hi), both rounded to nearest
-// even with saturation, taken on the fp16 roundings of x (x - hi is exact there: hi is x
-// rounded to 4 significant bits). Returns hi in bits 0-15 and lo in bits 16-31, element 0
-// in the lower byte of each.
+// x0, x1 (|x| < 448) as E4M3 pairs hi and lo with hi + lo ~ x: on the fp16 roundings h of
+// x, hi is h truncated to 4 significant bits (its low 7 mantissa bits cleared), exact in
+// E4M3 wherever |h| >= 2^-6, and lo = h - hi (exact in fp16) rounded to E4M3 (nearest
+// even, saturating). A value with at most 8 significant bits (a bf16 q, say) is split
+// exactly while lo stays a normal E4M3 number. Returns hi in bits 0-15 and lo in bits
+// 16-31, element 0 in the lower byte of each.
 __device__ __forceinline__ uint32_t split_e4m3x2(float x0, float x1) {
   uint32_t out;
-  asm("{\n\t.reg .b32 h, back, r;\n\t.reg .b16 hb, lb;\n\t"
+  asm("{\n\t.reg .b32 h, t, r;\n\t.reg .b16 hb, lb;\n\t"
       "cvt.rn.f16x2.f32 h, %2, %1;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f16x2 hb, h;\n\t"
-      "cvt.rn.f16x2.e4m3x2 back, hb;\n\t"
-      "sub.rn.f16x2 r, h, back;\n\t"
+      "and.b32 t, h, 0xFF80FF80;\n\t"
+      "sub.rn.f16x2 r, h, t;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 hb, t;\n\t"
       "cvt.rn.satfinite.e4m3x2.f16x2 lb, r;\n\t"
       "mov.b32 %0, {hb, lb};\n\t}"
       : "=r"(out) : "f"(x0), "f"(x1));
@@ -965,17 +967,20 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       const int qj = lane & 3;
 #pragma unroll 1
       for (int jt = 0; jt < 2; ++jt) {
-#pragma unroll 1
+        // the warpgroup's 64 rows of these 128 value columns, in one batch of loads
+        float ob[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld16(tmem + lane_addr + kOCol + 128 * jt + 64 * wg + 16 * c, ob + 16 * c);
+        tmem_wait_ld();
+        if (jt == 1) {
+          // O^T has been read: the next unit's first PV may overwrite it
+          tc_fence_before();
+          named_bar_sync(bar, 128);
+          if (leader && t == 0) mbar_arrive(b_oempty);
+        }
+#pragma unroll
         for (int c = 0; c < 4; ++c) {
-          float o[16];
-          tmem_ld16(tmem + lane_addr + kOCol + 128 * jt + 64 * wg + 16 * c, o);
-          tmem_wait_ld();
-          if (jt == 1 && c == 3) {
-            // O^T has been read: the next unit's first PV may overwrite it
-            tc_fence_before();
-            named_bar_sync(bar, 128);
-            if (leader && t == 0) mbar_arrive(b_oempty);
-          }
+          float* o = ob + 16 * c;
 #pragma unroll
           for (int i = 0; i < 16; ++i) o[i] *= alpha_s[wg][16 * c + i];
           const int col = 256 * (int)rank + 128 * jt + 32 * wl + 4 * (lane >> 2);

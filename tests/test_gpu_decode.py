@@ -120,6 +120,15 @@ SMALL = [
     (3, 1, 128, 16, [1, 255, 513], BF, True),        # CTA pairs
     (2, 1, 128, 8, [77, 1000], BF, True),
     (2, 1, 128, 48, [300, 70], BF, True),
+    # more than 64 rows, FP8 cache: CTA pairs reading E4M3 directly (32-key MMA steps)
+    (2, 1, 128, 64, [1, 255], F8, True),             # a single key; one short of a super-tile
+    (3, 1, 128, 64, [256, 257, 513], F8, True),      # super-tile edges
+    (3, 1, 128, 128, [64, 65, 190], F8, True),       # block edges, ragged 32-key steps
+    (4, 1, 128, 128, [32, 33, 95, 96], F8, True),    # 32-key step edges
+    (2, 1, 100, 64, [500, 129], F8, True),           # rows not a multiple of 8: Q by chunks
+    (2, 2, 64, 64, [1000, 65], F8, True),            # 128 rows from s_q = 2
+    (3, 1, 128, 16, [1, 255, 513], F8, True),        # pages smaller than a block
+    (2, 1, 128, 24, [77, 1000], F8, True),
 ]
 
 
@@ -254,6 +263,35 @@ def test_fp8_query_beyond_the_float16_range_is_reported():
     assert api.decode_check(g.workspace) == (0, 0)
     ro, rl = oracle_decode(case, g.cache_numpy())
     compare(case, out, lse, ro, rl)
+
+
+def test_fp8_pairs_take_any_bf16_query_magnitude():
+    """With an FP8 cache and more than 64 rows, each unit's q rows are scaled per row by a
+    power of two before they are split into two E4M3 terms, so rows of very different
+    magnitude (here 1e30, 1e-30, 3e38 and an all-zero row) decode like any other: no error
+    bit, and the oracle's result within the FP8 tolerance."""
+    case = synth.make_case(B=2, s_q=1, H=128, page_size=64, seq_lens=[700, 300], seed=49, kv_dtype=F8)
+    q = torch.from_numpy(case.q_bits.view(np.int16).copy()).view(torch.bfloat16).float()
+    q[0, 0, 3, :] *= 1.0e30
+    q[0, 0, 77, :] *= 1.0e-30
+    q[1, 0, 5, :] = 0.0
+    q[1, 0, 9, :] = 0.0
+    q[1, 0, 9, 100] = 3.0e38
+    q[1, 0, 9, 101] = -1.0e-38
+    case.q_bits[...] = q.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    g = GpuCase(case)
+    out, lse = g.decode()
+    assert api.decode_check(g.workspace) == (0, 0)
+    ro, rl = oracle_decode(case, g.cache_numpy())
+    # the output contract on every row; the LSE of rows scaled by 1e30 or 3e38 is itself of
+    # that size, where one float32 step is ~1e23 to ~1e30: those get a relative bound
+    lg = lse.cpu().numpy().astype(np.float64)
+    big = np.abs(rl) > 1.0e6
+    assert big.sum() == 2
+    assert (np.abs(lg - rl)[big] <= 1.0e-6 * np.abs(rl[big])).all()
+    compare(case, out, lse, ro, rl, rows=np.argwhere(~big))
+    og = out.float().cpu().numpy().astype(np.float64)
+    assert (np.abs(og - ro)[big] <= 2.0e-2).all()
 
 
 @pytest.mark.parametrize("H,kv", [(16, BF), (16, F8), (128, BF), (128, F8)])
