@@ -270,13 +270,13 @@ static mla_status decode_impl(const mla_decode_params* p, const void* q, const v
     return MLA_ERR_INVALID_ARG;
   {
     const int64_t rows = (int64_t)p->num_pages * p->page_size;
-    // chunks per key / value box: a pair loads 256-byte pieces of each key row (2 bf16 or 4
-    // E4M3 chunks) and 4 adjacent chunks of each value row
-    const uint32_t kc = plan.pair ? (fp8 ? 4u : 2u) : (uint32_t)decode_key_chunks_per_slot(rc, fp8);
+    // chunks per key / value box: a pair loads 256-byte pieces of each bf16 key row (2
+    // chunks) or whole E4M3 key rows (9 chunks), and 4 adjacent chunks of each value row
+    const uint32_t kc = plan.pair ? (fp8 ? 9u : 2u) : (uint32_t)decode_key_chunks_per_slot(rc, fp8);
     const uint32_t vc = plan.pair ? 4u : (uint32_t)decode_value_chunks_per_box(rc, fp8);
-    // E4M3 keys are 64-byte swizzled; E4M3 values too where the MMAs read them as they land
+    // E4M3 keys and values are 64-byte swizzled: the MMAs read them as they land
     if (!encode_kv_map(&da.tm_k, kv_cache, rows, kc, (uint32_t)box_rows, fp8, true) ||
-        !encode_kv_map(&da.tm_v, kv_cache, rows, vc, (uint32_t)box_rows, fp8, plan.pair))
+        !encode_kv_map(&da.tm_v, kv_cache, rows, vc, (uint32_t)box_rows, fp8, true))
       return MLA_ERR_INVALID_ARG;
   }
   da.kv_cache = kv_cache;

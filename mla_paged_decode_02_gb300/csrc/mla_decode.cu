@@ -79,7 +79,7 @@ struct Cfg {
   static constexpr int kQBytes = RC * 1152;            // 9 chunks x RC rows x 128 B
   static constexpr int kPRow = RC * 2;                  // bytes of one P^T row (one key)
   static constexpr int kPBytes = 128 * kPRow;
-  static constexpr int kNumP = FP8 && (RC == 64 || RC == 16) ? 1 : 2;  // P^T buffers
+  static constexpr int kNumP = FP8 && RC == 64 ? 1 : 2;  // P^T buffers
   static constexpr uint32_t kPSwz = RC == 64 ? kSwizzle128 : RC == 32 ? kSwizzle64 : kSwizzle32;
   static constexpr int kTmemCols = FP8 || RC == 64 ? 512 : RC == 32 ? 256 : 128;
   static constexpr int kThreads = FP8 ? 384 : 256;
@@ -99,31 +99,43 @@ struct Cfg {
   static constexpr int kKTmemBase = 6 * RC;
   static constexpr int kKTmemSlotCols = KC * 32;
   static constexpr int NK = FP8 ? (RC == 32 ? 3 : 4) : (RC < 64 ? 2 : 3);
-  // FP8 raw staging. TMA cost grows with the number of contiguous row pieces a box has
-  // (about 6 ns per piece per SM), so with 16 rows the raw keys are whole 576-byte rows (one
-  // stage = the tile's two 64-row halves, 72 KB, feeding all of its TMEM positions) and the
-  // raw values 4-chunk boxes (256-byte pieces, 32 KB, feeding two value pairs). 32 and 64
-  // rows keep 1-3 chunk key stages and 2-chunk value stages: their Q and P^T leave no room.
-  static constexpr bool kRawRows = FP8 && RC == 16;
-  static constexpr int NV = kRawRows ? 2 : RC == 16 ? 3 : 2;
+  // FP8 raw staging (E4M3 as TMA landed it, 64-byte swizzle). With 16 or 32 rows a key stage
+  // is a tile's 128 whole 576-byte rows (two 64-row boxes, 72 KB), which feeds all of its
+  // TMEM key positions and, its first 512 bytes per row, the PV MMAs as well; two stages.
+  // 64 rows (whose Q and P^T leave no room for that) keep 1-chunk key stages and separate
+  // 4-chunk value stages (256 value columns of the tile's rows, 32 KB).
+  static constexpr bool kRawRows = FP8 && RC <= 32;
+  static constexpr int NV = FP8 ? 1 : RC == 16 ? 3 : 2;     // bf16 value slots (FP8: none)
   static constexpr int kKRawChunks = kRawRows ? 9 : KC;     // chunks of a row per raw key box
   static constexpr int kKStageBytes = kKRawChunks * 8192;   // 2 halves x 64 rows x chunks x 64 B
   static constexpr int kKPosPerStage = kRawRows ? kSlotsPerTile : 1;   // TMEM key positions per stage
-  static constexpr int kVRawChunks = kRawRows ? 4 : 2;      // chunks of a row per raw value box
+  static constexpr int kVRawChunks = 4;                     // chunks of a row per raw value box
   static constexpr int kVStage = kVRawChunks * 8192;        // 2 halves x 64 rows x chunks x 64 B
   static constexpr int kPairsPerVStage = kVRawChunks / 2;
-  static constexpr int NKS = FP8 ? (kRawRows ? 1 : RC == 64 ? 3 : 2) : 0;   // raw staging depths
-  static constexpr int NVS = FP8 ? (kRawRows ? 2 : RC == 64 ? 2 : 3) : 0;
+  static constexpr int NKS = FP8 ? (kRawRows ? 2 : 3) : 0;   // raw staging depths
+  // whole-row key stages also hold the values: the PV MMAs read them there, and a stage is
+  // loaded again only once its tile's PV has completed (no value stages); 64 rows keep
+  // 1-chunk key stages and 4-chunk value stages
+  static constexpr int kValueStages = FP8 && !kRawRows ? 3 : 0;
+  // E4M3 q' and P go into the MMAs as hi and lo parts. With whole-row stages each K step
+  // is one MMA whose N holds both parts (2 RC columns: S^T and O^T of the hi part and of the
+  // lo part, added when read), so that the A operand is read from shared memory once.
+  static constexpr int kNC = kRawRows ? 2 * RC : RC;   // tensor-memory columns of S^T / an O^T tile
+  static constexpr int kOBase = 2 * kNC;               // first O^T column (after both S^T)
+  static_assert(kOBase + 4 * kNC <= 512, "tensor memory budget (S^T and O^T)");
+  static constexpr int NVS = kValueStages > 0 ? kValueStages : 1;   // barrier arrays
   static constexpr int kKLoaders = FP8 ? 4 : 1;         // arrivals that fill a K slot
-  // FP8 values: 16-byte units a thread converts per unrolled round (code size against
-  // latency hiding; measured: 8 for 16 rows, 4 for 32 and 64)
-  static constexpr int kValueRound = RC == 16 ? 8 : 4;
   static constexpr int kVLoaders = 1;
+  // FP8: P is computed times 2^kPOffLog2 and written as exact E4M3 hi and lo parts; the
+  // reference max moves once a score exceeds it by kRescale (log2 units), so P < 2^8 fits
+  static constexpr float kPOffLog2 = FP8 ? 4.f : 0.f;
+  static constexpr float kRescale = FP8 ? 4.f : kRescaleLog2;
   static_assert(!FP8 || kKTmemBase + NK * kKTmemSlotCols <= 512, "tensor memory budget");
   static_assert(kSlotsPerTile * KC == 9, "a tile is 9 chunks");
   static constexpr int kDynBytes = 1024 + kQBytes + kNumP * kPBytes + (FP8 ? 0 : NK * kKSlotBytes) +
-                                   NV * kVSlotBytes + NKS * kKStageBytes + NVS * kVStage;
+                                   (FP8 ? 0 : NV * kVSlotBytes) + NKS * kKStageBytes + kValueStages * kVStage;
   static_assert(kDynBytes + kStaticBudget <= kSmemLimit, "shared memory budget");
+  static_assert(kNumP * kPBytes >= 8192, "the epilogue's transpose stage");
 };
 
 struct Unit {
@@ -234,46 +246,6 @@ __device__ __forceinline__ bool iter_next(TileIter& it, const DecodeArgs& a, int
   return true;
 }
 
-// One raw E4M3 value chunk pair (staging [half][8 groups][2 chunks][8 rows][64 B]) into an
-// fp16 value slot ([chunk][16 groups][8 rows][128 B], 128-byte swizzle), G threads, with
-// the exact hardware convert (two bytes per instruction), as for the keys. (An integer-only
-// conversion, chosen so that values and keys would not compete for the convert unit, was
-// measured 15% slower on the 16-row workload.) Rows at or past `valid` are written as
-// zeros.
-// The raw stage holds VC chunks of every row: [2 halves][8 groups][VC chunks][8 rows][64 B];
-// the pair is chunks cb, cb + 1 of it.
-template <int G, int kRound, int VC>
-__device__ __forceinline__ void convert_value_pair(const uint8_t* src, uint8_t* dst, int valid, int gi, int cb) {
-  constexpr int kPer = 1024 / G;                 // 16-byte units per thread
-  static_assert(kPer % kRound == 0, "whole rounds");
-#pragma unroll 1
-  for (int r0 = 0; r0 < kPer; r0 += kRound) {
-    uint4 v[kRound];
-#pragma unroll
-    for (int jj = 0; jj < kRound; ++jj) {
-      const int idx = gi + (r0 + jj) * G, row = (idx & 511) >> 2;   // chunk idx / 512, column idx % 4
-      v[jj] = make_uint4(0, 0, 0, 0);
-      if (row < valid)
-        v[jj] = *reinterpret_cast<const uint4*>(src + (row >> 6) * (VC * 4096) + ((row >> 3) & 7) * (VC * 512) +
-                                                (cb + (idx >> 9)) * 512 + (row & 7) * 64 + (idx & 3) * 16);
-    }
-#pragma unroll
-    for (int jj = 0; jj < kRound; ++jj) {
-      const int idx = gi + (r0 + jj) * G, row = (idx & 511) >> 2, q4 = idx & 3;
-      const uint32_t b4[4] = {v[jj].x, v[jj].y, v[jj].z, v[jj].w};
-      uint32_t hh[8];
-#pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2) {
-        hh[2 * k2] = e4m3x2_to_f16x2(b4[k2] & 0xFFFFu);
-        hh[2 * k2 + 1] = e4m3x2_to_f16x2(b4[k2] >> 16);
-      }
-      uint8_t* drow = dst + (idx >> 9) * kChunkBytes + (row >> 3) * 1024 + (row & 7) * 128;
-      *reinterpret_cast<uint4*>(drow + (((2 * q4) ^ (row & 7)) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-      *reinterpret_cast<uint4*>(drow + (((2 * q4 + 1) ^ (row & 7)) << 4)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
-    }
-  }
-}
-
 template <int RC, bool FP8, bool kSub>
 __global__ void __launch_bounds__(Cfg<RC, FP8>::kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeArgs a) {
@@ -285,7 +257,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ uint8_t dsmem_raw[];
   __shared__ __align__(8) uint64_t bar_kfull[NK], bar_kempty[NK], bar_vfull[NV], bar_vempty[NV];
   __shared__ __align__(8) uint64_t bar_qfull, bar_qready, bar_qempty;
-  __shared__ __align__(8) uint64_t bar_kstage[NKS], bar_vstage[NVS], bar_vsempty[NVS];
+  __shared__ __align__(8) uint64_t bar_kstage[NKS], bar_ksfree[NKS], bar_vstage[NVS], bar_vsempty[NVS];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_s_empty[2], bar_p_full[NP], bar_pv[NP];
   __shared__ __align__(8) uint64_t bar_o_empty, bar_drain[2], bar_vaux, bar_never;
   __shared__ uint32_t tmem_base_s;
@@ -293,6 +265,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   __shared__ __align__(16) float mref_s[RC];
   __shared__ float alpha_s[RC], tot_s[RC];
   __shared__ int nvis_s[RC];
+  __shared__ __align__(16) float qf_s[RC], rowc_s[RC];   // FP8, 16-32 rows: 2^-e of q, score factors
+  __shared__ __align__(8) uint64_t bar_qsc, bar_qfree;
   __shared__ float wmax_s[4 * RC];
 
   const int warp = threadIdx.x >> 5;
@@ -306,7 +280,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const uint32_t sP = sQ + C::kQBytes;
   const uint32_t sK = sP + NP * C::kPBytes;
   const uint32_t sV = sK + (FP8 ? 0 : NK * C::kKSlotBytes);
-  const uint32_t sKS = sV + NV * kVSlotBytes;
+  const uint32_t sKS = sV + (FP8 ? 0 : NV * kVSlotBytes);
   const uint32_t sVS = sKS + (FP8 ? NKS * C::kKStageBytes : 0);   // raw value stages, C::kVStage each
   uint8_t* gQ = gbase;
   uint8_t* gP = gbase + (sP - sQ);
@@ -318,7 +292,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const uint32_t b_vfull = smem_u32(bar_vfull), b_vempty = smem_u32(bar_vempty);
   const uint32_t b_qfull = smem_u32(&bar_qfull), b_qready = smem_u32(&bar_qready);
   const uint32_t b_qempty = smem_u32(&bar_qempty);
+  const uint32_t b_qsc = smem_u32(&bar_qsc), b_qfree = smem_u32(&bar_qfree);
   const uint32_t b_kstage = smem_u32(bar_kstage), b_vstage = smem_u32(bar_vstage);
+  const uint32_t b_ksfree = smem_u32(bar_ksfree);   // whole-row key stages: the tile's PV is done
   const uint32_t b_vsempty = smem_u32(bar_vsempty);
   const uint32_t b_s_full = smem_u32(bar_s_full), b_s_empty = smem_u32(bar_s_empty);
   const uint32_t b_p_full = smem_u32(bar_p_full), b_pv = smem_u32(bar_pv);
@@ -340,12 +316,17 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     }
     mbar_init(b_qfull, 1);
     mbar_init(b_qready, 4);
-    for (int i = 0; i < NKS; ++i) mbar_init(b_kstage + 8 * i, 1);
+    for (int i = 0; i < NKS; ++i) {
+      mbar_init(b_kstage + 8 * i, 1);
+      mbar_init(b_ksfree + 8 * i, 1);
+    }
     for (int i = 0; i < NVS; ++i) {
       mbar_init(b_vstage + 8 * i, 1);
       mbar_init(b_vsempty + 8 * i, 1);
     }
     mbar_init(b_qempty, 1);
+    mbar_init(b_qsc, 1);     // FP8, 16-32 rows: the Q converters, with the row factors
+    mbar_init(b_qfree, 1);   // the softmax warps, once they have read them
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_s_full + 8 * i, 1);
       mbar_init(b_s_empty + 8 * i, 128);
@@ -475,6 +456,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       // descriptors built once, advanced by constants (the start field counts 16 B units)
       const uint64_t dK0 = make_sdesc(sK, 16, C::kKGroupStride, kSwizzle128);
       const uint64_t dQ0 = make_sdesc(sQ, 16, 1024, kSwizzle128);
+      const uint64_t dKS = make_sdesc(sKS, 16, 9 * 512, kSwizzle64);
+      const uint64_t dQ8 = make_sdesc(sQ, 16, 512, kSwizzle64);
+      const uint32_t idesc_qk8 = make_idesc(128, 2 * RC, 0, 0, 0);
       uint32_t n = 0, kp = 0, uc = 0;
       bool ok = true;
       for (int u = u0; u < u1 && ok; ++u, ++uc) {
@@ -487,8 +471,27 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         ok = wait(FP8 ? b_qready : b_qfull, uc & 1);
         for (int k = 0; k < U.te - U.tb && ok; ++k, ++n) {
           ok = wait(b_s_empty + 8 * (n & 1), ((n >> 1) & 1) ^ 1);
-          const uint32_t d = tmem + (n & 1) * RC;
-          for (int sl = 0; sl < C::kSlotsPerTile && ok; ++sl, ++kp) {
+          const uint32_t d = tmem + (n & 1) * C::kNC;
+          if constexpr (C::kRawRows) {
+            // E4M3 keys straight from the tile's whole-row stage (K-major, 64-byte swizzle,
+            // 8-row groups 4.5 KB apart) against q' = q 2^e as E4M3 hi and lo (K-major, each
+            // 1 KB block of 8 rows x 64 columns: hi in its first 512 B, lo in its second)
+            const uint32_t st = n % NKS;
+            ok = ok && wait(b_kstage + 8 * st, (n / NKS) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t as = dKS + (uint64_t)(st * (C::kKStageBytes >> 4));
+            // N = 2 RC: the 512-byte groups of 8 rows alternate hi and lo, so that S^T column
+            // 16 g + i is row 8 g + i of K . hi and column 16 g + 8 + i the same row of K . lo
+#pragma unroll 1
+            for (int c = 0; c < 9; ++c) {
+              const uint64_t bd = dQ8 + (uint64_t)(c * (RC * 128 >> 4));
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk)
+                umma_f8(d, as + (uint64_t)(c * (512 >> 4) + 2 * kk), bd + 2 * kk, idesc_qk8, (c | kk) != 0);
+            }
+          }
+          for (int sl = 0; !C::kRawRows && sl < C::kSlotsPerTile && ok; ++sl, ++kp) {
             const uint32_t ks = kp % NK;
             ok = wait(b_kfull + 8 * ks, (kp / NK) & 1);
             if (!ok) break;
@@ -534,11 +537,25 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     // ============================================================ PV issuer
     // One thread, in program order: per tile the softmax's P^T (and, for the first tile of
     // a unit, the epilogue's release of O^T), then every value chunk pair: wait full,
-    // 8 MMAs (fewer on a partial last tile), release the slot when they complete.
+    // 8 MMAs (fewer on a partial last tile), release the slot when they complete. FP8: the
+    // MMAs read the raw E4M3 value stages as they landed (kind::f8f6f4, K = 32), each K
+    // step once with P's hi part and once with its lo part.
     if (lane == 0) {
       const uint32_t idesc_pv = make_idesc(128, RC, FP8 ? 0u : 1u, 1, 1);
       const uint64_t dV0 = make_sdesc(sV, C::kVChunkStride, C::kVGroupStride, kSwizzle128);
       const uint64_t dP0 = make_sdesc(sP, 8 * C::kPRow, 8 * C::kPRow, C::kPSwz);
+      // FP8 raw value stage [2 halves][8 groups][VC chunks][8 rows][64 B]: MN-major, chunks
+      // 512 B apart (leading offset), 8-key groups VC x 512 B apart. P^T hi (then lo, 128 RC
+      // bytes on): [8-key group][RC / 16 cores][8 keys][16 B], MN-major without swizzle, where
+      // the leading offset steps along K (8-key groups, 8 RC bytes) and the stride offset
+      // along MN (16-byte cores, 128 B).
+      constexpr uint32_t kVC = C::kVRawChunks;
+      const uint64_t dVS0 = make_sdesc(sVS, 512, kVC * 512, kSwizzle64);
+      const uint64_t dP8 = make_sdesc(sP, 8 * RC, 128, kSwizzleNone);
+      const uint64_t dKS0 = make_sdesc(sKS, 512, 9 * 512, kSwizzle64);   // whole-row key stages
+      // whole-row stages: P^T [8-key group][2 RC / 16 cores: hi, then lo][8 keys][16 B]
+      const uint64_t dP8s = make_sdesc(sP, 16 * RC, 128, kSwizzleNone);
+      const uint32_t idesc_pv8 = make_idesc(128, 2 * RC, 0, 1, 1);
       uint32_t n = 0, vp = 0, uc = 0;
       bool ok = true;
       for (int u = u0; u < u1 && ok; ++u, ++uc) {
@@ -548,26 +565,66 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           ok = wait(b_p_full + 8 * pb, (n / NP) & 1);
           if (ok && k == 0) ok = wait(b_oempty, (uc & 1) ^ 1);
           const int valid = U.L - (U.tb + k) * kTileTokens;
-          const int ksteps = valid >= kTileTokens ? 8 : (valid + 15) / 16;
-          const uint64_t bd0 = dP0 + (uint64_t)(pb * (C::kPBytes >> 4));
-          for (int j = 0; j < kPairsPerTile && ok; ++j, ++vp) {
-            const uint32_t vs = vp % NV;
-            ok = wait(b_vfull + 8 * vs, (vp / NV) & 1);
+          if constexpr (FP8 && C::kRawRows) {
+            // the values are the first 8 chunks of the tile's whole-row key stage
+            // ([2 halves][8 groups][9 chunks][8 rows][64 B]), released when these complete
+            const int ksteps = valid >= kTileTokens ? 4 : (valid + 31) / 32;
+            const uint32_t st = n % NKS;
+            ok = wait(b_kstage + 8 * st, (n / NKS) & 1);
             if (!ok) break;
             tc_fence_after();
-            const uint64_t ad0 = dV0 + (uint64_t)(vs * (kVSlotBytes >> 4));
-            const uint32_t d = tmem + (2 + j) * RC;
-            if (ksteps == 8) {
+            const uint64_t as = dKS0 + (uint64_t)(st * (C::kKStageBytes >> 4));
+            // N = 2 RC: P^T's cores hold hi (O^T columns 0 .. RC - 1) then lo (RC .. 2 RC - 1)
+            const uint64_t bs = dP8s + (uint64_t)(pb * (C::kPBytes >> 4));
+            // consecutive MMAs go to the four O^T tiles in turn (independent accumulators)
+            for (int kk = 0; kk < ksteps; ++kk)
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                umma_f16(d, ad0 + kk * (2 * C::kVGroupStride >> 4), bd0 + kk * (16 * C::kPRow >> 4), idesc_pv,
-                         !(k == 0 && kk == 0));
-            } else {
-              for (int kk = 0; kk < ksteps; ++kk)
-                umma_f16(d, ad0 + kk * (2 * C::kVGroupStride >> 4), bd0 + kk * (16 * C::kPRow >> 4), idesc_pv,
-                         !(k == 0 && kk == 0));
+              for (int j = 0; j < kPairsPerTile; ++j)
+                umma_f8(tmem + C::kOBase + j * C::kNC, as + (uint64_t)((2 * j * 512 + kk * 4 * 9 * 512) >> 4),
+                        bs + (uint64_t)((kk * 64 * RC) >> 4), idesc_pv8, !(k == 0 && kk == 0));
+            umma_commit(b_ksfree + 8 * st);
+          } else if constexpr (FP8) {
+            const int ksteps = valid >= kTileTokens ? 4 : (valid + 31) / 32;
+            const uint64_t bh = dP8 + (uint64_t)(pb * (C::kPBytes >> 4));
+            for (int j0 = 0; j0 < kPairsPerTile && ok; j0 += C::kPairsPerVStage, ++vp) {
+              const uint32_t st = vp % NVS;
+              ok = wait(b_vstage + 8 * st, (vp / NVS) & 1);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t as = dVS0 + (uint64_t)(st * (C::kVStage >> 4));
+              for (int pin = 0; pin < C::kPairsPerVStage; ++pin) {
+                const uint32_t d = tmem + (2 + j0 + pin) * RC;
+                for (int kk = 0; kk < ksteps; ++kk) {
+                  const uint64_t ad = as + (uint64_t)((2 * pin * 512 + kk * 4 * kVC * 512) >> 4);
+                  const uint64_t bd = bh + (uint64_t)((kk * 32 * RC) >> 4);
+                  umma_f8(d, ad, bd, idesc_pv, !(k == 0 && kk == 0));        // V . P hi
+                  umma_f8(d, ad, bd + (uint64_t)((128 * RC) >> 4), idesc_pv, 1u);   // V . P lo
+                }
+              }
+              umma_commit(b_vsempty + 8 * st);
             }
-            umma_commit(b_vempty + 8 * vs);
+          } else {
+            const int ksteps = valid >= kTileTokens ? 8 : (valid + 15) / 16;
+            const uint64_t bd0 = dP0 + (uint64_t)(pb * (C::kPBytes >> 4));
+            for (int j = 0; j < kPairsPerTile && ok; ++j, ++vp) {
+              const uint32_t vs = vp % NV;
+              ok = wait(b_vfull + 8 * vs, (vp / NV) & 1);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t ad0 = dV0 + (uint64_t)(vs * (kVSlotBytes >> 4));
+              const uint32_t d = tmem + (2 + j) * RC;
+              if (ksteps == 8) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                  umma_f16(d, ad0 + kk * (2 * C::kVGroupStride >> 4), bd0 + kk * (16 * C::kPRow >> 4), idesc_pv,
+                           !(k == 0 && kk == 0));
+              } else {
+                for (int kk = 0; kk < ksteps; ++kk)
+                  umma_f16(d, ad0 + kk * (2 * C::kVGroupStride >> 4), bd0 + kk * (16 * C::kPRow >> 4), idesc_pv,
+                           !(k == 0 && kk == 0));
+              }
+              umma_commit(b_vempty + 8 * vs);
+            }
           }
           if (ok) umma_commit(b_pv + 8 * pb);
         }
@@ -584,7 +641,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     const float kvs = FP8 ? __ldg(a.kv_scale) : 1.0f;
     const float c_log2 = a.softmax_scale * kvs * kLog2e;
     const float kvo = kvs;                              // value scale (FP8: kv_scale)
-    uint32_t gn = 0, vcp = 0;
+    uint32_t gn = 0;
     bool ok = true;
     float lsum[RC];
     for (int u = u0; u < u1 && ok; ++u) {
@@ -598,6 +655,14 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         nvis_s[t] = a.causal ? min(U.L, U.L - a.s_q + 1 + (row0 + t) / a.H) : U.L;
       }
       const int mask_from = a.causal ? U.L - a.s_q + 1 : U.L;
+      if constexpr (C::kRawRows) {
+        // the unit's score factors: softmax scale x log2 e x 2^-e of the row's q
+        ok = wait_softmax(b_qsc, (uint32_t)(u - u0) & 1);
+        if (!ok) break;
+        if (t < RC) rowc_s[t] = c_log2 * qf_s[t];
+        named_bar_sync(kSoftmaxBar, 128);
+        if (t == 0) mbar_arrive(b_qfree);
+      }
 #pragma unroll
       for (int r = 0; r < RC; ++r) lsum[r] = 0.f;
       named_bar_sync(kSoftmaxBar, 128);
@@ -611,8 +676,23 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         if (!ok) break;
         tc_fence_after();
         float s[RC];
+        if constexpr (C::kRawRows) {
+          // columns 16 g .. 16 g + 7: rows 8 g .. of K . hi; the next 8: the same rows of K . lo
 #pragma unroll
-        for (int c = 0; c < RC / 16; ++c) tmem_ld16(tmem + lane_addr + sb * RC + 16 * c, s + 16 * c);
+          for (int g = 0; g < RC / 8; g += 2) {
+            float v[2][16];
+            tmem_ld16(tmem + lane_addr + sb * C::kNC + 16 * g, v[0]);
+            tmem_ld16(tmem + lane_addr + sb * C::kNC + 16 * g + 16, v[1]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) s[8 * (g + h) + i] = v[h][i] + v[h][8 + i];
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < RC / 16; ++c) tmem_ld16(tmem + lane_addr + sb * RC + 16 * c, s + 16 * c);
+        }
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(b_s_empty + 8 * sb);
@@ -621,16 +701,27 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         // the reference maxima are read from shared memory (a broadcast) where they are
         // used, rather than held in RC registers
         auto mref4 = [&](int r) { return *reinterpret_cast<const float4*>(mref_s + r); };
+        // the score factor of 4 rows: one constant, or (E4M3 q') per row
+        auto factors = [&](int r, float* cc) {
+          if constexpr (C::kRawRows) {
+            const float4 c4 = *reinterpret_cast<const float4*>(rowc_s + r);
+            cc[0] = c4.x; cc[1] = c4.y; cc[2] = c4.z; cc[3] = c4.w;
+          } else {
+            cc[0] = cc[1] = cc[2] = cc[3] = c_log2;
+          }
+        };
         bool need = false;
         if ((U.tb + k + 1) * kTileTokens <= mask_from) {
 #pragma unroll
           for (int r = 0; r < RC; r += 4) {
             const float4 m4 = mref4(r);
             const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+            float cc[4];
+            factors(r, cc);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              s[r + i] *= c_log2;
-              need |= s[r + i] > mm[i] + kRescaleLog2;
+              s[r + i] *= cc[i];
+              need |= s[r + i] > mm[i] + C::kRescale;
             }
           }
         } else {
@@ -638,10 +729,12 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           for (int r = 0; r < RC; r += 4) {
             const float4 m4 = mref4(r);
             const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+            float cc[4];
+            factors(r, cc);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              s[r + i] = j < nvis_s[r + i] ? s[r + i] * c_log2 : -INFINITY;
-              need |= s[r + i] > mm[i] + kRescaleLog2;
+              s[r + i] = j < nvis_s[r + i] ? s[r + i] * cc[i] : -INFINITY;
+              need |= s[r + i] > mm[i] + C::kRescale;
             }
           }
         }
@@ -665,19 +758,27 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           for (int r = 0; r < RC; ++r) lsum[r] *= alpha_s[r];
           rescale = k > 0;
         }
-        // P^T row of this key, in registers until its buffer is free
+        // P^T row of this key, in registers until its buffer is free. bf16: RC / 2 words of
+        // pairs. FP8: P times 2^4 as E4M3 hi bytes (words 0 .. RC / 4 - 1) and lo bytes
+        // (the rest), four rows per word.
         uint32_t pw[RC / 2];
 #pragma unroll
         for (int r = 0; r < RC; r += 4) {
           const float4 m4 = mref4(r);
-          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+          const float mm[4] = {m4.x - C::kPOffLog2, m4.y - C::kPOffLog2, m4.z - C::kPOffLog2, m4.w - C::kPOffLog2};
+          float pr[4];
 #pragma unroll
-          for (int i = 0; i < 4; i += 2) {
-            const float p0 = s[r + i] == -INFINITY ? 0.f : ex2_approx(s[r + i] - mm[i]);
-            const float p1 = s[r + i + 1] == -INFINITY ? 0.f : ex2_approx(s[r + i + 1] - mm[i + 1]);
-            pw[(r + i) / 2] = pack2<FP8>(p0, p1);
-            lsum[r + i] += p0;      // the normaliser sums the unrounded probabilities
-            lsum[r + i + 1] += p1;
+          for (int i = 0; i < 4; ++i) {
+            pr[i] = s[r + i] == -INFINITY ? 0.f : ex2_approx(s[r + i] - mm[i]);
+            lsum[r + i] += pr[i];   // the normaliser sums the unrounded probabilities
+          }
+          if constexpr (FP8) {
+            const uint32_t o0 = split_e4m3x2(pr[0], pr[1]), o1 = split_e4m3x2(pr[2], pr[3]);
+            pw[r / 4] = __byte_perm(o0, o1, 0x5410);
+            pw[RC / 4 + r / 4] = __byte_perm(o0, o1, 0x7632);
+          } else {
+            pw[r / 2] = pack2<FP8>(pr[0], pr[1]);
+            pw[r / 2 + 1] = pack2<FP8>(pr[2], pr[3]);
           }
         }
         // the buffer's previous user, PV(n - NP), must have completed
@@ -686,10 +787,28 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           if (!ok) break;
         }
         uint8_t* prow = gP + pb * C::kPBytes;
+        if constexpr (C::kRawRows) {
+          // [8-key group][2 RC / 16 cores: hi, then lo][8 keys][16 B]
 #pragma unroll
-        for (int u16 = 0; u16 < C::kPRow / 16; ++u16)
-          *reinterpret_cast<uint4*>(prow + p_offset<C::kPRow>(t, u16)) =
-              make_uint4(pw[4 * u16], pw[4 * u16 + 1], pw[4 * u16 + 2], pw[4 * u16 + 3]);
+          for (int c = 0; c < RC / 8; ++c) {
+            uint8_t* q = prow + (t >> 3) * (16 * RC) + c * 128 + (t & 7) * 16;
+            *reinterpret_cast<uint4*>(q) = make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+          }
+        } else if constexpr (FP8) {
+          // [8-key group][RC / 16 cores][8 keys][16 B] for hi, the same for lo 128 RC bytes on
+#pragma unroll
+          for (int c = 0; c < RC / 16; ++c) {
+            uint8_t* q = prow + (t >> 3) * (8 * RC) + c * 128 + (t & 7) * 16;
+            *reinterpret_cast<uint4*>(q) = make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+            *reinterpret_cast<uint4*>(q + 128 * RC) =
+                make_uint4(pw[RC / 4 + 4 * c], pw[RC / 4 + 4 * c + 1], pw[RC / 4 + 4 * c + 2], pw[RC / 4 + 4 * c + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int u16 = 0; u16 < C::kPRow / 16; ++u16)
+            *reinterpret_cast<uint4*>(prow + p_offset<C::kPRow>(t, u16)) =
+                make_uint4(pw[4 * u16], pw[4 * u16 + 1], pw[4 * u16 + 2], pw[4 * u16 + 3]);
+        }
         fence_proxy_async_smem();
         if (rescale) {
           // O^T holds tiles up to k-1 of this unit: wait for PV(n-1), then scale in place
@@ -698,14 +817,15 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           tc_fence_after();
 #pragma unroll 1
           for (int jt = 0; jt < 4; ++jt) {
+            // whole-row stages: columns c >= RC / 16 hold the lo part of rows 16 c - RC ..
 #pragma unroll
-            for (int c = 0; c < RC / 16; ++c) {
+            for (int c = 0; c < C::kNC / 16; ++c) {
               float o[16];
-              const uint32_t ta = tmem + lane_addr + (2 + jt) * RC + 16 * c;
+              const uint32_t ta = tmem + lane_addr + C::kOBase + jt * C::kNC + 16 * c;
               tmem_ld16(ta, o);
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) o[i] *= alpha_s[16 * c + i];
+              for (int i = 0; i < 16; ++i) o[i] *= alpha_s[(16 * c + i) % RC];
               tmem_st16(ta, o);
             }
           }
@@ -713,33 +833,6 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
         }
         tc_fence_before();
         mbar_arrive(b_p_full + 8 * pb);
-        if (FP8) {
-          // ---- the values of this tile (FP8): raw E4M3 chunk pairs -> fp16 value ring,
-          // one pair at a time so that PV starts on each as soon as it is ready. Thread 0
-          // waits; the softmax barrier passes the outcome on.
-          const int valid = U.L - (U.tb + k) * kTileTokens;
-          for (int j = 0; j < kPairsPerTile && ok; ++j, ++vcp) {
-            // raw stage vst holds kPairsPerVStage pairs: waited for at its first pair and
-            // released after its last
-            const uint32_t vst = vcp / C::kPairsPerVStage, st = vst % NVS, vs = vcp % NV;
-            const int pin = (int)(vcp % C::kPairsPerVStage);
-            const bool first = pin == 0, last = pin == C::kPairsPerVStage - 1;
-            // the raw rows have landed and the fp16 slot is free (with three or more value
-            // slots the producer waited for the slot before loading the rows)
-            const bool mine = t != 0 || ((!first || wait(b_vstage + 8 * st, (vst / NVS) & 1)) &&
-                                         (NV >= 3 || wait(b_vempty + 8 * vs, ((vcp / NV) & 1) ^ 1)));
-            ok = !named_bar_or(kSoftmaxBar, 128, !mine);
-            if (!ok) break;
-            convert_value_pair<128, C::kValueRound, C::kVRawChunks>(gVS + st * C::kVStage, gV + vs * kVSlotBytes,
-                                                                    valid, t, 2 * pin);
-            fence_proxy_async_smem();
-            named_bar_sync(kSoftmaxBar, 128);
-            if (t == 0) {
-              mbar_arrive(b_vfull + 8 * vs);
-              if (last) mbar_arrive(b_vsempty + 8 * st);
-            }
-          }
-        }
       }
       if (!ok) break;
       // ---- epilogue: wait for the unit's last PV
@@ -776,7 +869,15 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
 #pragma unroll 1
         for (int c = 0; c < RC / 16; ++c) {
           float o[16];
-          tmem_ld16(tmem + lane_addr + (2 + jt) * RC + 16 * c, o);
+          tmem_ld16(tmem + lane_addr + C::kOBase + jt * C::kNC + 16 * c, o);
+          if constexpr (C::kRawRows) {
+            // plus the lo part's columns RC + 16 c ..
+            float o2[16];
+            tmem_ld16(tmem + lane_addr + C::kOBase + jt * C::kNC + RC + 16 * c, o2);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] += o2[i];
+          }
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -815,7 +916,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       }
       if (t < RC && row0 + t < R) {
         const float tot = tot_s[t];
-        const float l = tot > 0.f ? (mref_s[t] + __log2f(tot)) * kLn2 : -INFINITY;
+        // FP8: P was computed times 2^kPOffLog2, and so was the row sum
+        const float l = tot > 0.f ? (mref_s[t] + __log2f(tot) - C::kPOffLog2) * kLn2 : -INFINITY;
         if (direct) a.lse[(int64_t)U.b * R + row0 + t] = l;
         else a.part_lse[(int64_t)U.slot * RC + t] = l;
       }
@@ -823,6 +925,71 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       mbar_arrive(b_oempty);
       named_bar_sync(kSoftmaxBar, 128);
       gn += T;
+    }
+  } else if (FP8 && C::kRawRows && warp >= 8) {
+    // ============================================================ FP8 Q converters (16-32 rows)
+    // Each unit's RC query rows, bf16 as TMA landed them ([9 chunks][RC rows][128 B], 128-byte
+    // swizzle), become q' = q 2^e (the row's largest |q| in [128, 256)) written as E4M3 hi
+    // and lo in place: every 1 KB block of 8 rows x 64 columns becomes hi in its first 512
+    // bytes and lo in its second (8 rows x 64 bytes, 64-byte swizzled each), the QK^T MMAs'
+    // B operand. hi + lo is q' exactly (8 significant bits). A warp owns whole 8-row groups,
+    // so its reads of a block precede its writes there; lane 4 q + p holds 16-byte units p
+    // and p + 4 of row q of each block. The row factors 2^-e go to qf_s for the softmax.
+    const int qrow = lane >> 2, part = lane & 3;
+    uint32_t uq = 0;
+    for (int u = u0; u < u1; ++u, ++uq) {
+      const bool mine = threadIdx.x != 256 || (wait(b_qfull, uq & 1) && (uq == 0 || wait(b_qfree, (uq - 1) & 1)));
+      if (named_bar_or(kKeyDqBar, kKeyDqThreads, !mine)) break;
+      for (int g = warp - 8; g < RC / 8; g += 4) {
+        auto block_of = [&](int c) -> uint8_t* { return gQ + c * (RC * 128) + g * 1024; };
+        // pass 1: the row's largest |q| (this lane's 18 units, then the row's 4 lanes)
+        __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
+#pragma unroll
+        for (int c = 0; c < 9; ++c)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 v = *reinterpret_cast<const uint4*>(block_of(c) + qrow * 128 + (((part + 4 * h) ^ qrow) << 4));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[k])));
+          }
+        float mx = fmaxf(__low2float(m2), __high2float(m2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // e = 7 - floor(log2 max|q|), so that the row's largest |q'| lies in [128, 256)
+        int e = 0;
+        if (mx > 0.f) e = min(max(7 - ((int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127), -126), 126);
+        const float f = __uint_as_float((uint32_t)(e + 127) << 23);
+        // pass 2, block by block: the warp's reads of a block precede its writes there
+#pragma unroll 3
+        for (int c = 0; c < 9; ++c) {
+          uint8_t* blk = block_of(c);
+          uint4 v[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            v[h] = *reinterpret_cast<const uint4*>(blk + qrow * 128 + (((part + 4 * h) ^ qrow) << 4));
+          __syncwarp();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int un = part + 4 * h;           // columns 8 un .. 8 un + 7 of the block
+            const uint32_t w[4] = {v[h].x, v[h].y, v[h].z, v[h].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              o[k] = split_e4m3x2(__uint_as_float(w[k] << 16) * f, __uint_as_float(w[k] & 0xFFFF0000u) * f);
+            // 8 bytes: half (un % 2) of the 16-byte unit un / 2 of the 64-byte row
+            const uint32_t off = qrow * 64 + (((un >> 1) ^ ((qrow >> 1) & 3)) << 4) + (un & 1) * 8;
+            *reinterpret_cast<uint2*>(blk + off) = make_uint2(__byte_perm(o[0], o[1], 0x5410), __byte_perm(o[2], o[3], 0x5410));
+            *reinterpret_cast<uint2*>(blk + 512 + off) =
+                make_uint2(__byte_perm(o[0], o[1], 0x7632), __byte_perm(o[2], o[3], 0x7632));
+          }
+        }
+        if (part == 0) qf_s[8 * g + qrow] = __uint_as_float((uint32_t)(127 - e) << 23);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kKeyDqBar, kKeyDqThreads);
+      if (threadIdx.x == 256) mbar_arrive(b_qsc);
+      if (lane == 0) mbar_arrive(b_qready);
     }
   } else if (FP8 && warp >= 8) {
     // ============================================================ FP8 keys (+ Q)
@@ -838,7 +1005,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     const uint32_t lane_base = tmem + ((uint32_t)(warp & 3) << 21);   // (32 * (warp % 4)) << 16
     TileIter kc, ki;                                    // consume / issue cursors
     bool kmore = iter_begin<kSub>(kc, a, u0, u1);
-    bool kimore = gi == 0 && iter_begin<kSub>(ki, a, u0, u1);
+    // whole-row stages are loaded by warp 2 (they are released by the PV MMAs)
+    bool kimore = !C::kRawRows && gi == 0 && iter_begin<kSub>(ki, a, u0, u1);
     // raw stages: kip issued, kfreed read by every thread (free again), kwaited landed
     int kic = 0;
     uint32_t kip = 0, kcp = 0, uq = 0, kfreed = 0, kwaited = 0;
@@ -945,34 +1113,102 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       for (uint32_t q = kwaited; q < kip; ++q)
         mbar_wait(b_kstage + 8 * (q % NKS), (q / NKS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
     }
+  } else if (FP8 && C::kRawRows && warp == 2) {
+    // ============================================================ FP8 whole-row key stages
+    // Every tile's 128 key rows as two TMA boxes (one per 64-row page half) of all 9 chunks,
+    // into a stage once the PV MMAs of the tile that used it before have completed. The key
+    // group converts the stage into tensor memory, and the PV MMAs read its values. On a tile
+    // that ends inside a 32-key MMA step the warp loads the stage on its own barrier and
+    // zeroes the rows from the sequence end to the end of that step (the cache may hold NaN
+    // there, and 0 * NaN is NaN inside the MMA; those keys are masked) before it signals.
+    TileIter it;
+    bool more = iter_begin<kSub>(it, a, u0, u1);
+    bool ok = true;
+    uint32_t p = 0, aux = 0;
+    const uint32_t box_bytes = (C::kKStageBytes / 128) * box_rows;
+    while (more && ok) {
+      const int valid = it.U.L - it.tile * kTileTokens;
+      const bool tail = valid < kTileTokens && (valid & 31) != 0;
+      const uint32_t sl = p % NKS;
+      ok = wait_warp(b_ksfree + 8 * sl, ((p / NKS) & 1) ^ 1);
+      if (!ok) break;
+      const uint32_t bar = tail ? b_vaux : b_kstage + 8 * sl, dst = sKS + sl * C::kKStageBytes;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar, it.boxes() * box_bytes);
+        for (int h = 0; h < 2; ++h)
+          load_half<kSub>(it, a, h, &a.tm_k, dst + h * (C::kKStageBytes / 2), bar, 0, box_bytes);
+      }
+      if (tail) {
+        ok = wait_warp(b_vaux, aux & 1);
+        ++aux;
+        if (!ok) break;
+        // stage [2 halves][8 groups][9 chunks][8 rows][64 B]: the rows' 8 value chunks
+        const int nrow = ((valid + 31) & ~31) - valid;
+        uint8_t* g = gKS + sl * C::kKStageBytes;
+        for (int idx = lane; idx < nrow * 32; idx += 32) {
+          const int row = valid + (idx >> 5), c = (idx >> 2) & 7, u16 = idx & 3;
+          *reinterpret_cast<uint4*>(g + (row >> 6) * (9 * 4096) + ((row >> 3) & 7) * (9 * 512) + c * 512 +
+                                    (row & 7) * 64 + u16 * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_kstage + 8 * sl);
+      }
+      ++p;
+      more = iter_next<kSub>(it, a, u1);
+    }
+    if (lane == 0) {
+      volatile uint32_t no_abort = 0;
+      for (uint32_t q = p > (uint32_t)NKS ? p - NKS : 0; q < p; ++q)
+        mbar_wait(b_kstage + 8 * (q % NKS), (q / NKS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
+    }
   } else if (FP8 && warp == 2) {
     // ============================================================ FP8 raw value producer
-    // One thread: every value chunk pair of every tile as two TMA boxes (one per 64-row
-    // page half) into the raw staging ring; the softmax warps convert them (after writing
-    // the tile's P^T) and release the staging slot. With three or more value slots the
-    // thread issues pair p only once the fp16 slot it will be converted into is free as
-    // well, so that the landed raw rows are all the softmax warps need to wait for (with
-    // two slots that would put the raw load's latency behind the slot's release).
-    if (lane == 0) {
-      TileIter it;
-      bool more = iter_begin<kSub>(it, a, u0, u1);
-      bool ok = true;
-      uint32_t p = 0;
-      const uint32_t box_bytes = (C::kVStage / 128) * box_rows;
-      while (more && ok) {
-        for (int j = 0; j < kPairsPerTile; j += C::kPairsPerVStage, ++p) {
-          // stage p: value chunks 2j .. 2j + kVRawChunks - 1 of the tile's rows
-          const uint32_t sl = p % NVS;
-          ok = wait(b_vsempty + 8 * sl, ((p / NVS) & 1) ^ 1) &&
-               (NV < 3 || wait(b_vempty + 8 * (p % NV), ((p / NV) & 1) ^ 1));
-          if (!ok) break;
-          const uint32_t bar = b_vstage + 8 * sl, dst = sVS + sl * C::kVStage;
+    // Every tile's values as two stages of 4 chunks (256 value columns of its 128 rows),
+    // each two TMA boxes (one per 64-row page half), which the PV MMAs read as they landed.
+    // On a tile that ends inside a 32-key MMA step the warp loads each stage on its own
+    // barrier and zeroes the rows from the sequence end to the end of that step (the cache
+    // may hold NaN there, and 0 * NaN is NaN inside the MMA) before it signals the stage.
+    TileIter it;
+    bool more = iter_begin<kSub>(it, a, u0, u1);
+    bool ok = true;
+    uint32_t p = 0, aux = 0;
+    constexpr int kVC = C::kVRawChunks;
+    const uint32_t box_bytes = (C::kVStage / 128) * box_rows;
+    while (more && ok) {
+      const int valid = it.U.L - it.tile * kTileTokens;
+      const bool tail = valid < kTileTokens && (valid & 31) != 0;
+      for (int j = 0; j < kPairsPerTile; j += C::kPairsPerVStage, ++p) {
+        // stage p: value chunks 2j .. 2j + kVC - 1 of the tile's rows
+        const uint32_t sl = p % NVS;
+        ok = wait_warp(b_vsempty + 8 * sl, ((p / NVS) & 1) ^ 1);
+        if (!ok) break;
+        const uint32_t bar = tail ? b_vaux : b_vstage + 8 * sl, dst = sVS + sl * C::kVStage;
+        if (lane == 0) {
           mbar_arrive_expect_tx(bar, it.boxes() * box_bytes);
           for (int h = 0; h < 2; ++h)
             load_half<kSub>(it, a, h, &a.tm_v, dst + h * (C::kVStage / 2), bar, 2 * j, box_bytes);
         }
-        if (ok) more = iter_next<kSub>(it, a, u1);
+        if (tail) {
+          ok = wait_warp(b_vaux, aux & 1);
+          ++aux;
+          if (!ok) break;
+          // stage [2 halves][8 groups][kVC chunks][8 rows][64 B]: whole 64-byte rows
+          const int nrow = ((valid + 31) & ~31) - valid;
+          uint8_t* g = gVS + sl * C::kVStage;
+          for (int idx = lane; idx < nrow * kVC * 4; idx += 32) {
+            const int row = valid + idx / (kVC * 4), c = (idx >> 2) % kVC, u16 = idx & 3;
+            *reinterpret_cast<uint4*>(g + (row >> 6) * (kVC * 4096) + ((row >> 3) & 7) * (kVC * 512) + c * 512 +
+                                      (row & 7) * 64 + u16 * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_vstage + 8 * sl);
+        }
       }
+      if (ok) more = iter_next<kSub>(it, a, u1);
+    }
+    if (lane == 0) {
       volatile uint32_t no_abort = 0;
       for (uint32_t q = p > (uint32_t)NVS ? p - NVS : 0; q < p; ++q)
         mbar_wait(b_vstage + 8 * (q % NVS), (q / NVS) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);

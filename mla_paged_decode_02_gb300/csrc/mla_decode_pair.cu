@@ -78,7 +78,10 @@ constexpr int kQChunk = 8192;               // 64 rows x 64 columns bf16
 constexpr int kPairQBytes = 9 * kQChunk;    // this CTA's 64 query rows: bf16, or E4M3 hi and lo
 constexpr int kPairPBytes = kPairKeys * 128;  // P^T for 256 keys x 64 rows: bf16, or E4M3 hi and lo
 constexpr int kStageBytes = 16384;         // P^T rows bound for the peer: 128 keys x 64 rows
-constexpr int kRing = 3;
+constexpr int kRing = 3;                    // bf16: ring of key and value slots
+constexpr int kVRing = 2;                   // FP8: ring of 16 KB value blocks
+constexpr int kKTileBytes = 2 * 36864;      // FP8: this CTA's 128 keys as whole 576-byte rows
+constexpr int kVBlockBytes = 16384;         // FP8: 64 keys x this CTA's 256 value columns
 constexpr int kPairThreads = 384;
 constexpr int kPairTmemCols = 512;
 constexpr int kOCol = 256;                  // O^T M-tile j at columns 256 + 128 j
@@ -86,27 +89,31 @@ constexpr float kPLog2e = 1.4426950408889634f;
 constexpr float kPLn2 = 0.6931471805599453f;
 constexpr int kPairSmemLimit = 232448;
 constexpr int kPairStaticBudget = 9216;
-constexpr int kPairDynBytes = 1024 + kPairQBytes + kPairPBytes + kStageBytes + kRing * kSlotBytes;
-static_assert(kPairDynBytes + kPairStaticBudget <= kPairSmemLimit, "shared memory budget");
+// bf16: Q, P^T, the staging buffer of P^T rows bound for the peer, the ring. FP8: Q, P^T, the
+// key tile, the value ring (P^T rows for the peer go by st.async).
+constexpr int kPairDynBytes16 = 1024 + kPairQBytes + kPairPBytes + kStageBytes + kRing * kSlotBytes;
+constexpr int kPairDynBytes8 = 1024 + kPairQBytes + kPairPBytes + kKTileBytes + kVRing * kVBlockBytes;
+constexpr int pair_dyn_bytes(bool fp8) { return fp8 ? kPairDynBytes8 : kPairDynBytes16; }
+static_assert(kPairDynBytes16 + kPairStaticBudget <= kPairSmemLimit, "shared memory budget");
+static_assert(kPairDynBytes8 + kPairStaticBudget <= kPairSmemLimit, "shared memory budget");
 
-// Slot plans. A key slot is KC adjacent 64-column chunks of this CTA's 128 keys — bf16: 2
-// chunks of 128-byte rows (5 slots per super-tile); E4M3: 4 chunks of 64-byte rows (3
-// slots) — the last slot holding chunk 8 and zero-filled chunks past the row (TMA fills
-// them). A value slot holds this CTA's 256 value columns of one 64-key block (bf16) or two
-// (E4M3). Either way a key slot is [2 halves][8 groups][KC chunks][8 rows][row piece] with
-// 2 KB per 8-row group, and a value block [8 groups][4 chunks][8 rows][row piece].
+// The bf16 ring's slot plan: a key slot is KC = 2 adjacent 64-column chunks of this CTA's
+// 128 keys ([2 halves][8 groups][2 chunks][8 rows][128 B], 5 slots per super-tile, the last
+// holding chunk 8 and a zero-filled chunk past the row, which TMA fills); a value slot is
+// this CTA's 256 value columns of one 64-key block ([8 groups][4 chunks][8 rows][128 B]).
+// E4M3 value blocks have the same shape with 64-byte row pieces. Per cache type also the
+// softmax's lazy rescale threshold and the power of two P is computed times.
 template <bool FP8>
 struct PairCfg {
-  static constexpr int kKeyChunks = FP8 ? 4 : 2;
-  static constexpr int kKeySlots = (9 + kKeyChunks - 1) / kKeyChunks;
+  static constexpr int kKeyChunks = 2;
+  static constexpr int kKeySlots = 5;
   static constexpr int kRowBytes = FP8 ? 64 : 128;      // one chunk of one row
-  static constexpr int kBlocksPerSlot = FP8 ? 2 : 1;    // 64-key value blocks per value slot
-  static constexpr int kBlockBytes = kSlotBytes / kBlocksPerSlot;
-  static constexpr int kKStep = FP8 ? 32 : 16;          // keys per MMA K step
+  static constexpr int kBlockBytes = kSlotBytes;        // bf16: one 64-key value block per slot
   static constexpr float kRescaleLog2 = FP8 ? 4.f : 8.f;  // lazy rescale threshold (log2 units)
   static constexpr float kPOffLog2 = FP8 ? 4.f : 0.f;     // P is computed times 2^kPOffLog2
-  static_assert(4 * 8 * kRowBytes * 8 == kBlockBytes, "value block layout");
-  static_assert(kKeyChunks * 8 * kRowBytes == 2048, "key slot group stride");
+  static_assert(FP8 || 4 * 8 * kRowBytes * 8 == kBlockBytes, "value block layout");
+  static_assert(FP8 || kKeyChunks * 8 * kRowBytes == 2048, "key slot group stride");
+  static_assert(kKeySlots * kKeyChunks >= 9, "a tile is 9 chunks");
 };
 
 struct PUnit {
@@ -139,6 +146,35 @@ __device__ __forceinline__ void block_rows(const DecodeArgs& a, const PUnit& U, 
   }
 }
 
+// The page numbers of the four 64-key blocks of super-tile `tile` (the block-table index
+// clamped to the row, so that the load is safe past the sequence end), loaded ahead of use.
+__device__ __forceinline__ void tile_pages(const DecodeArgs& a, int b, int tile, int* pg) {
+  const int32_t* bt = a.block_table + (int64_t)b * a.MB;
+#pragma unroll
+  for (int kb = 0; kb < 4; ++kb) pg[kb] = __ldg(bt + min((tile * kPairKeys + 64 * kb) / a.P, a.MB - 1));
+}
+
+// block_rows from page numbers loaded before: the same rows and box counts.
+template <bool kSub>
+__device__ __forceinline__ void rows_from_pages(const DecodeArgs& a, int L, int tile, const int* pg, int64_t* rb,
+                                                int* nb) {
+#pragma unroll
+  for (int kb = 0; kb < 4; ++kb) {
+    const int tok = tile * kPairKeys + 64 * kb;
+    const int off = tok % a.P;
+    rb[kb] = tok >= L ? -1 : (pg[kb] < 0 || pg[kb] >= a.num_pages) ? (int64_t)off : (int64_t)pg[kb] * a.P + off;
+    nb[kb] = kSub ? block_boxes(L - tok, a.box_rows) : (tok < L ? 1 : 0);
+  }
+}
+
+// The rows of a key tile, kept for the value loads of the same tile that follow it.
+struct TileRows {
+  int64_t rb[4];
+  int nb[4];
+  int L, b, tile;
+};
+constexpr int kRowsQ = 4;   // key tiles whose values are not all loaded: at most 3
+
 __device__ __forceinline__ uint32_t p_off128(int row, int u) {   // 128-byte swizzled bf16 P^T row
   return (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u + ((uint32_t)(u ^ (row & 7)) << 4);
 }
@@ -164,27 +200,18 @@ __device__ __forceinline__ void quad_transpose4(uint32_t* a, int j) {
   }
 }
 
+// Non-blocking test of an mbarrier phase (a producer polling two rings).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// x0, x1 (|x| < 448) as E4M3 pairs hi and lo with hi + lo ~ x: on the fp16 roundings h of
-// x, hi is h truncated to 4 significant bits (its low 7 mantissa bits cleared), exact in
-// E4M3 wherever |h| >= 2^-6, and lo = h - hi (exact in fp16) rounded to E4M3 (nearest
-// even, saturating). A value with at most 8 significant bits (a bf16 q, say) is split
-// exactly while lo stays a normal E4M3 number. Returns hi in bits 0-15 and lo in bits
-// 16-31, element 0 in the lower byte of each.
-__device__ __forceinline__ uint32_t split_e4m3x2(float x0, float x1) {
-  uint32_t out;
-  asm("{\n\t.reg .b32 h, t, r;\n\t.reg .b16 hb, lb;\n\t"
-      "cvt.rn.f16x2.f32 h, %2, %1;\n\t"
-      "and.b32 t, h, 0xFF80FF80;\n\t"
-      "sub.rn.f16x2 r, h, t;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f16x2 hb, t;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f16x2 lb, r;\n\t"
-      "mov.b32 %0, {hb, lb};\n\t}"
-      : "=r"(out) : "f"(x0), "f"(x1));
-  return out;
-}
 
 }  // namespace
 
@@ -198,6 +225,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
   // FP8: Q landed (this CTA), Q converted (both CTAs, on the even CTA), this CTA's row
   // factors written and read
   __shared__ __align__(8) uint64_t bar_qraw, bar_qready, bar_qsc, bar_qfree;
+  __shared__ __align__(8) uint64_t bar_ktfull, bar_ktempty;   // FP8: the key tile
   __shared__ __align__(16) uint32_t sig_s[4];        // landing place of the odd CTA's 16-byte signals
   __shared__ __align__(8) uint64_t bar_sfull[2], bar_sempty[2], bar_pfull, bar_pin, bar_pvdone, bar_oempty;
   __shared__ __align__(8) uint64_t bar_x[2][2];
@@ -209,6 +237,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
   __shared__ float qf_s[64];                        // FP8: 2^-e of this CTA's 64 query rows
   __shared__ float alpha_s[2][64], own_s[2][64];
   __shared__ int nvis_s[2][64];
+  __shared__ TileRows rows_q[kRowsQ];               // FP8 producer: rows of issued key tiles
   __shared__ float wred_s[2][4][64];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -222,17 +251,19 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
   uint8_t* gbase = dsmem_raw + (base - raw);
   const uint32_t sQ = base;
   const uint32_t sP = sQ + kPairQBytes;
-  const uint32_t sStage = sP + kPairPBytes;
-  const uint32_t sR = sStage + kStageBytes;
+  const uint32_t sStage = sP + kPairPBytes;                     // bf16
+  const uint32_t sKT = sP + kPairPBytes;                        // FP8: key tile
+  const uint32_t sR = FP8 ? sKT + kKTileBytes : sStage + kStageBytes;   // the (value) ring
   uint8_t* gQ = gbase;
   uint8_t* gP = gbase + kPairQBytes;
   uint8_t* gStage = gP + kPairPBytes;
-  uint8_t* gR = gStage + kStageBytes;
+  uint8_t* gR = gbase + (sR - sQ);
 
   const uint32_t b_full = smem_u32(bar_full), b_empty = smem_u32(bar_empty), b_aux = smem_u32(&bar_aux);
   const uint32_t b_qfull = smem_u32(&bar_qfull), b_qempty = smem_u32(&bar_qempty);
   const uint32_t b_qraw = smem_u32(&bar_qraw), b_qready = smem_u32(&bar_qready);
   const uint32_t b_qsc = smem_u32(&bar_qsc), b_qfree = smem_u32(&bar_qfree);
+  const uint32_t b_ktfull = smem_u32(&bar_ktfull), b_ktempty = smem_u32(&bar_ktempty);
   const uint32_t b_sfull = smem_u32(bar_sfull), b_sempty = smem_u32(bar_sempty);
   const uint32_t b_pfull = smem_u32(&bar_pfull), b_pin = smem_u32(&bar_pin), b_pvdone = smem_u32(&bar_pvdone);
   const uint32_t b_oempty = smem_u32(&bar_oempty), b_drain = smem_u32(&bar_drain);
@@ -253,6 +284,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
     mbar_init(b_qready, 1);               // FP8: the even CTA's converters, expecting the odd CTA's 16-byte signal
     mbar_init(b_qsc, 1);                  // FP8: this CTA's converters
     mbar_init(b_qfree, 1);                // FP8: the softmax warpgroup of this CTA's rows
+    mbar_init(b_ktfull, 1);               // FP8: the even CTA's producer, with both CTAs' bytes
+    mbar_init(b_ktempty, 1);              // FP8: the MMA issuer's commit (both CTAs)
     for (int i = 0; i < 2; ++i) {
       mbar_init(b_sfull + 8 * i, 1);
       mbar_init(b_sempty + 8 * i, 2);     // the even CTA's two warpgroups (the odd CTA's
@@ -294,6 +327,186 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
 
   if (warp < 4) {
     if (warp == 0) {
+      if constexpr (FP8) {
+      // ================================================================ producer (FP8)
+      // One thread feeds three streams, polling their barriers: each unit's Q (this CTA's 64
+      // rows, on this CTA's barrier for its converters); the key tiles — this CTA's 128 keys
+      // of a super-tile as whole 576-byte rows, one TMA row piece per key, into the single key
+      // tile once the previous tile's QK^T MMAs are done with it; and the value blocks (64 keys
+      // x this CTA's 256 value columns) into a ring of two, one key tile behind, so that they
+      // read rows the key loads have brought into L2.
+      if (lane == 0) {
+        const uint64_t pol_keep = l2_policy_evict_last(), pol_last = l2_policy_evict_first();
+        const uint32_t box_rows = kSub ? (uint32_t)a.box_rows : 64u;
+        const uint32_t kbox_bytes = kDQK * box_rows;           // one whole-row key box
+        const uint32_t vbox_bytes = 256 * box_rows;             // one 4-chunk value box
+        uint32_t nq = 0, nkt = 0, rv = 0, aux = 0, vseq = 0;
+        int ku = u0, kt = 0, vkb = 0;
+        bool kq = true, kdone = u0 >= u1;
+        // Loads are issued well before their values are used, so that the one thread feeding
+        // three streams does not wait on them: the next unit's descriptor (its length one unit
+        // ahead, the raw descriptor two ahead) and the page numbers of the next key tile.
+        PUnit KU{}, KN{};
+        int4 n4 = make_int4(0, 0, 0, 0);
+        int kpg[4] = {0, 0, 0, 0};
+        auto next_unit = [&](int u) {           // KN <- unit u + 1 (from n4), n4 <- unit u + 2
+          KN.b = n4.x;
+          KN.g = n4.y;
+          KN.tb = n4.z & 0xFFFF;
+          KN.te = (int)((unsigned)n4.z >> 16);
+          KN.slot = n4.w;
+          KN.L = u + 1 < u1 ? __ldg(&a.batch_info[n4.x].z) : 0;
+          n4 = u + 2 < u1 ? __ldg(&a.units[u + 2]) : make_int4(0, 0, 0, 0);
+        };
+        if (!kdone) {
+          KU = load_punit(a, u0);
+          if (u0 + 1 < u1) n4 = __ldg(&a.units[u0 + 1]);
+          next_unit(u0);
+          kt = KU.tb;
+          tile_pages(a, KU.b, kt, kpg);
+        }
+        uint64_t t_last = global_timer_ns();
+        while (!(kdone && vseq == nkt)) {
+          bool prog = false;
+          if (!kdone) {
+            if (kq) {
+              if (mbar_test(b_qempty, (nq & 1) ^ 1)) {
+                const int32_t qg = (128 * KU.g + 64 * (int)rank) / 8, q0 = 128 * KU.g + 64 * (int)rank;
+                mbar_arrive_expect_tx(b_qraw, kPairQBytes);
+                if (a.q_whole_rows)     // one box of 64 whole rows: [8 groups][9 chunks][8 rows][128 B]
+                  tma_load_5d_hint(sQ, &a.tm_q, b_qraw, 0, 0, 0, qg, KU.b, pol_keep);
+                else                    // 9 boxes of one 64-column chunk: [9 chunks][64 rows][128 B]
+                  for (int c = 0; c < 9; ++c) tma_load_3d_hint(sQ + c * kQChunk, &a.tm_q, b_qraw, 64 * c, q0, KU.b, pol_keep);
+                ++nq;
+                kq = false;
+                prog = true;
+              }
+            } else if (mbar_test(b_ktempty, (nkt & 1) ^ 1)) {
+              TileRows& e = rows_q[nkt % kRowsQ];
+              int64_t rb[4];
+              int nb[4];
+              rows_from_pages<kSub>(a, KU.L, kt, kpg, rb, nb);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                e.rb[i] = rb[i];
+                e.nb[i] = nb[i];
+              }
+              e.L = KU.L;
+              e.b = KU.b;
+              e.tile = kt;
+              const int32_t* bt = a.block_table + (int64_t)KU.b * a.MB;
+              // every key tile takes bytes from both CTAs (see the bf16 ring below)
+              const int nown = nb[2 * rank] + nb[2 * rank + 1], nodd = nb[2] + nb[3];
+              const uint32_t nbox = (uint32_t)(nb[0] + nb[1] + (nodd > 0 ? nodd : 1));
+              const uint32_t lb = lead(b_ktfull);
+              if (leader) mbar_arrive_expect_tx(b_ktfull, nbox * kbox_bytes);
+              if (nown == 0) tma_load_4d_pair_hint(sKT, &a.tm_k, lb, 0, 0, 0, (int32_t)(rb[0] >> 3), pol_keep);
+              for (int h = 0; h < 2; ++h) {
+                const int kb = 2 * (int)rank + h;
+                if (nb[kb] == 0) continue;
+                const uint32_t d = sKT + h * (kKTileBytes / 2);
+                tma_load_4d_pair_hint(d, &a.tm_k, lb, 0, 0, 0, (int32_t)(rb[kb] >> 3), pol_keep);
+                if (kSub && nb[kb] > 1)
+                  load_more_boxes(kBoxPairHint, &a.tm_k, d, lb, 0, kbox_bytes, bt, a, kt * kPairKeys + 64 * kb, nb[kb],
+                                  pol_keep);
+              }
+              ++nkt;
+              prog = true;
+              if (++kt == KU.te) {
+                if (++ku == u1) {
+                  kdone = true;
+                } else {
+                  KU = KN;
+                  next_unit(ku);
+                  kt = KU.tb;
+                  kq = true;
+                }
+              }
+              if (!kdone) tile_pages(a, KU.b, kt, kpg);
+            }
+          }
+          // value block vkb of key tile vseq, once the next key tile has been issued (so this
+          // tile's key rows have landed) or the keys are done
+          if (vseq + 1 < nkt || (kdone && vseq < nkt)) {
+            const uint32_t slot = rv % kVRing;
+            if (mbar_test(b_empty + 8 * slot, ((rv / kVRing) & 1) ^ 1)) {
+              const TileRows& e = rows_q[vseq % kRowsQ];
+              const int kb = vkb;
+              const int valid = e.L - e.tile * kPairKeys - 64 * kb;
+              const int tok0 = e.tile * kPairKeys + 64 * kb;
+              const int32_t* vbt = a.block_table + (int64_t)e.b * a.MB;
+              const int64_t vrb = e.rb[kb];
+              const int vnb = e.nb[kb];
+              // a block not loaded whole (32-key MMA steps past the end, or boxes past it) is
+              // loaded here first, its rows up to the end of the last step zeroed (the cache may
+              // hold NaN there, and 0 * NaN is NaN inside the MMA), then its bytes counted
+              const bool zero = valid < 64 && ((valid & 31) != 0 || (kSub && vnb < (int)(64 / box_rows)));
+              const uint32_t lb = lead(b_full + 8 * slot), dst = sR + slot * kVBlockBytes;
+              const int32_t c0 = 4 * (int)rank;               // this CTA's value columns 256 rank ..
+              if (leader) mbar_arrive_expect_tx(b_full + 8 * slot, 2u * kVBlockBytes);
+              bool vok = true;
+              if (!zero) {
+                tma_load_4d_pair_hint(dst, &a.tm_v, lb, 0, 0, c0, (int32_t)(vrb >> 3), pol_last);
+                if (kSub && vnb > 1)
+                  load_more_boxes(kBoxPairHint, &a.tm_v, dst, lb, c0, vbox_bytes, vbt, a, tok0, vnb, pol_last);
+              } else {
+                mbar_arrive_expect_tx(b_aux, (kSub ? (uint32_t)vnb : 1u) * vbox_bytes);
+                tma_load_4d_hint(dst, &a.tm_v, b_aux, 0, 0, c0, (int32_t)(vrb >> 3), pol_last);
+                if (kSub && vnb > 1)
+                  load_more_boxes(kBoxHint, &a.tm_v, dst, b_aux, c0, vbox_bytes, vbt, a, tok0, vnb, pol_last);
+                vok = wait(b_aux, aux & 1);
+                ++aux;
+                if (vok) {
+                  // block [8 key groups][4 chunks][8 rows][64 B]: zero whole rows
+                  const int nrow = ((valid + 31) & ~31) - valid;
+                  uint8_t* g = gR + slot * kVBlockBytes;
+                  for (int idx = 0; idx < nrow * 16; ++idx) {
+                    const int row = valid + (idx >> 4), c = (idx >> 2) & 3, u16 = idx & 3;
+                    *reinterpret_cast<uint4*>(g + (row >> 3) * 2048 + c * 512 + (row & 7) * 64 + u16 * 16) =
+                        make_uint4(0, 0, 0, 0);
+                  }
+                  fence_proxy_async_smem();
+                  fence_acq_rel_cluster();
+                  mbar_complete_tx_cluster(lb, kVBlockBytes);   // this CTA's share of the block is in place
+                }
+              }
+              if (!vok) break;
+              ++rv;
+              prog = true;
+              if (++vkb == 4 || valid <= 64) {
+                vkb = 0;
+                ++vseq;
+              }
+            }
+          }
+          if (prog) {
+            t_last = global_timer_ns();
+          } else {
+            if (*abort_flag) break;
+            if (global_timer_ns() - t_last > a.wait_limit_ns) {
+              *abort_flag = 1u;
+              atomicOr(err, MLA_DEVERR_TIMEOUT);
+              fail_peer();
+              break;
+            }
+          }
+        }
+        if (*abort_flag) {     // see below: the odd CTA cannot observe its own loads then
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 50000ull) {
+          }
+        }
+        // no copy into this CTA's memory may be in flight when it leaves
+        volatile uint32_t no_abort = 0;
+        if (leader) {
+          if (nkt > 0)
+            mbar_wait(b_ktfull, (nkt - 1) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
+          for (uint32_t q = rv > (uint32_t)kVRing ? rv - kVRing : 0; q < rv; ++q)
+            mbar_wait(b_full + 8 * (q % kVRing), (q / kVRing) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
+        }
+        if (nq > 0) mbar_wait(b_qraw, (nq - 1) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
+      }
+      } else {
       // ================================================================ producer
       // Ring order per super-tile n: its key slots (chunks KC ks .. KC ks + KC - 1 of this
       // CTA's 128 keys each), then the value slots of tile n-1 (this CTA's 256 value columns
@@ -310,57 +523,50 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       const uint32_t vbox_bytes = (Cfg::kBlockBytes / 64) * box_rows;          // one value box
       auto load_values = [&](const PUnit& U, int tile, const int64_t* rb, const int* nb) -> bool {
         const int32_t* bt = bt_all + (int64_t)U.b * a.MB;
-        for (int vs = 0; vs < 4 / Cfg::kBlocksPerSlot; ++vs) {
-          int nvalid = 0;
-          for (int i = 0; i < Cfg::kBlocksPerSlot; ++i) nvalid += rb[vs * Cfg::kBlocksPerSlot + i] >= 0 ? 1 : 0;
-          if (nvalid == 0) continue;
+        for (int kb = 0; kb < 4; ++kb) {
+          if (rb[kb] < 0) break;                       // blocks past the sequence end
           const uint32_t slot = r % kRing;
           bool w_ok = lane != 0 || wait(b_empty + 8 * slot, ((r / kRing) & 1) ^ 1);
           if (!__all_sync(0xffffffffu, w_ok)) return false;
           const uint32_t lb = lead(b_full + 8 * slot);
           const int32_t c0 = 4 * (int)rank;            // this CTA's value columns 256 rank ..
-          if (leader && lane == 0) mbar_arrive_expect_tx(b_full + 8 * slot, 2u * nvalid * Cfg::kBlockBytes);
-          for (int i = 0; i < Cfg::kBlocksPerSlot; ++i) {
-            const int kb = vs * Cfg::kBlocksPerSlot + i;
-            if (rb[kb] < 0) continue;
-            const int valid = U.L - tile * kPairKeys - 64 * kb;
-            // the block holding the sequence end gets its rows up to the end of its last MMA K
-            // step zeroed (the cache may hold NaN there, and 0 * NaN is NaN inside the MMA); a
-            // block not loaded whole completes its bytes itself
-            const bool zero = valid < 64 && ((valid % Cfg::kKStep) != 0 || (kSub && nb[kb] < (int)(64 / box_rows)));
-            const int tok0 = tile * kPairKeys + 64 * kb;
-            const uint32_t dst = sR + slot * kSlotBytes + i * Cfg::kBlockBytes;
-            if (!zero) {
-              if (lane == 0) {
-                tma_load_4d_pair_hint(dst, &a.tm_v, lb, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
-                if (kSub && nb[kb] > 1)
-                  load_more_boxes(kBoxPairHint, &a.tm_v, dst, lb, c0, vbox_bytes, bt, a, tok0, nb[kb], pol_last);
-              }
-            } else {
-              if (lane == 0) {
-                mbar_arrive_expect_tx(b_aux, (kSub ? (uint32_t)nb[kb] : 1u) * vbox_bytes);
-                tma_load_4d_hint(dst, &a.tm_v, b_aux, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
-                if (kSub && nb[kb] > 1)
-                  load_more_boxes(kBoxHint, &a.tm_v, dst, b_aux, c0, vbox_bytes, bt, a, tok0, nb[kb], pol_last);
-              }
-              w_ok = wait(b_aux, aux & 1);
-              ++aux;
-              if (!__all_sync(0xffffffffu, w_ok)) return false;
-              // block layout [8 key groups][4 chunks][8 rows][row piece]: zero whole rows
-              constexpr int kU = Cfg::kRowBytes / 16;
-              const int nrow = ((valid + Cfg::kKStep - 1) & ~(Cfg::kKStep - 1)) - valid;
-              uint8_t* g = gR + slot * kSlotBytes + i * Cfg::kBlockBytes;
-              for (int idx = lane; idx < nrow * 4 * kU; idx += 32) {
-                const int row = valid + idx / (4 * kU), c = (idx / kU) & 3, u16 = idx % kU;
-                *reinterpret_cast<uint4*>(g + (row >> 3) * (32 * Cfg::kRowBytes) + c * (8 * Cfg::kRowBytes) +
-                                          (row & 7) * Cfg::kRowBytes + u16 * 16) = make_uint4(0, 0, 0, 0);
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                fence_acq_rel_cluster();
-                mbar_complete_tx_cluster(lb, Cfg::kBlockBytes);   // this CTA's share of the block is in place
-              }
+          if (leader && lane == 0) mbar_arrive_expect_tx(b_full + 8 * slot, 2u * Cfg::kBlockBytes);
+          const int valid = U.L - tile * kPairKeys - 64 * kb;
+          // the block holding the sequence end gets its rows up to the end of its last MMA K
+          // step zeroed (the cache may hold NaN there, and 0 * NaN is NaN inside the MMA); a
+          // block not loaded whole completes its bytes itself
+          const bool zero = valid < 64 && ((valid % 16) != 0 || (kSub && nb[kb] < (int)(64 / box_rows)));
+          const int tok0 = tile * kPairKeys + 64 * kb;
+          const uint32_t dst = sR + slot * kSlotBytes;
+          if (!zero) {
+            if (lane == 0) {
+              tma_load_4d_pair_hint(dst, &a.tm_v, lb, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
+              if (kSub && nb[kb] > 1)
+                load_more_boxes(kBoxPairHint, &a.tm_v, dst, lb, c0, vbox_bytes, bt, a, tok0, nb[kb], pol_last);
+            }
+          } else {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(b_aux, (kSub ? (uint32_t)nb[kb] : 1u) * vbox_bytes);
+              tma_load_4d_hint(dst, &a.tm_v, b_aux, 0, 0, c0, (int32_t)(rb[kb] >> 3), pol_last);
+              if (kSub && nb[kb] > 1)
+                load_more_boxes(kBoxHint, &a.tm_v, dst, b_aux, c0, vbox_bytes, bt, a, tok0, nb[kb], pol_last);
+            }
+            w_ok = wait(b_aux, aux & 1);
+            ++aux;
+            if (!__all_sync(0xffffffffu, w_ok)) return false;
+            // block layout [8 key groups][4 chunks][8 rows][128 B]: zero whole rows
+            const int nrow = ((valid + 15) & ~15) - valid;   // to the end of the 16-key step
+            uint8_t* g = gR + slot * kSlotBytes;
+            for (int idx = lane; idx < nrow * 32; idx += 32) {
+              const int row = valid + (idx >> 5), c = (idx >> 3) & 3, u16 = idx & 7;
+              *reinterpret_cast<uint4*>(g + (row >> 3) * 4096 + c * 1024 + (row & 7) * 128 + u16 * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              fence_acq_rel_cluster();
+              mbar_complete_tx_cluster(lb, Cfg::kBlockBytes);   // this CTA's share of the block is in place
             }
           }
           ++r;
@@ -375,28 +581,21 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       for (int u = u0; u < u1 && ok; ++u, ++uq) {
         const PUnit U = load_punit(a, u);
         // this CTA's 64 query rows of the unit (rows past R read as zeros), kept in L2 for the
-        // re-reads of long sequences' units. bf16: counted on the even CTA's barrier with both
-        // CTAs' bytes; FP8: on this CTA's own, for its converters
+        // re-reads of long sequences' units, counted on the even CTA's barrier with both CTAs'
+        // bytes: as one box of 64 whole rows ([8 groups][9 chunks][8 rows][128 B]) or as 9
+        // boxes of one 64-column chunk ([9 chunks][64 rows][128 B])
         bool w_ok = lane != 0 || wait(b_qempty, (uq & 1) ^ 1);
         ok = __all_sync(0xffffffffu, w_ok);
         if (!ok) break;
         if (lane == 0) {
           const int32_t qg = (128 * U.g + 64 * (int)rank) / 8, q0 = 128 * U.g + 64 * (int)rank;
-          if constexpr (FP8) {
-            mbar_arrive_expect_tx(b_qraw, kPairQBytes);
-            if (a.q_whole_rows)     // one box of 64 whole rows: [8 groups][9 chunks][8 rows][128 B]
-              tma_load_5d_hint(sQ, &a.tm_q, b_qraw, 0, 0, 0, qg, U.b, pol_keep);
-            else                    // 9 boxes of one 64-column chunk: [9 chunks][64 rows][128 B]
-              for (int c = 0; c < 9; ++c) tma_load_3d_hint(sQ + c * kQChunk, &a.tm_q, b_qraw, 64 * c, q0, U.b, pol_keep);
-          } else {
-            const uint32_t lb = lead(b_qfull);
-            if (leader) mbar_arrive_expect_tx(b_qfull, 2 * kPairQBytes);
-            if (a.q_whole_rows)
-              tma_load_5d_pair_hint(sQ, &a.tm_q, lb, 0, 0, 0, qg, U.b, pol_keep);
-            else
-              for (int c = 0; c < 9; ++c)
-                tma_load_3d_pair_hint(sQ + c * kQChunk, &a.tm_q, lb, 64 * c, q0, U.b, pol_keep);
-          }
+          const uint32_t lb = lead(b_qfull);
+          if (leader) mbar_arrive_expect_tx(b_qfull, 2 * kPairQBytes);
+          if (a.q_whole_rows)
+            tma_load_5d_pair_hint(sQ, &a.tm_q, lb, 0, 0, 0, qg, U.b, pol_keep);
+          else
+            for (int c = 0; c < 9; ++c)
+              tma_load_3d_pair_hint(sQ + c * kQChunk, &a.tm_q, lb, 64 * c, q0, U.b, pol_keep);
         }
         for (int tile = U.tb; tile < U.te && ok; ++tile) {
           int64_t rb[4];
@@ -454,17 +653,13 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
         }
       }
       // a CTA must not leave with copies into its memory in flight: the even CTA waits until
-      // the last loads of both CTAs have landed (normally the MMA issuer already has), and
-      // with the FP8 cache each CTA for its own last Q
-      if (lane == 0) {
+      // the last loads of both CTAs have landed (normally the MMA issuer already has)
+      if (lane == 0 && leader) {
         volatile uint32_t no_abort = 0;
-        if (leader)
-          for (uint32_t q = r > (uint32_t)kRing ? r - kRing : 0; q < r; ++q)
-            mbar_wait(b_full + 8 * (q % kRing), (q / kRing) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
-        if (uq > 0) {
-          if (FP8) mbar_wait(b_qraw, (uq - 1) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
-          else if (leader) mbar_wait(b_qfull, (uq - 1) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
-        }
+        for (uint32_t q = r > (uint32_t)kRing ? r - kRing : 0; q < r; ++q)
+          mbar_wait(b_full + 8 * (q % kRing), (q / kRing) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
+        if (uq > 0) mbar_wait(b_qfull, (uq - 1) & 1, &no_abort, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);
+      }
       }
     } else if (warp == 1 && leader) {
       // ================================================================ MMA issuer (even CTA)
@@ -483,7 +678,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
         const uint64_t dV0 = make_sdesc(sR, 8 * Cfg::kRowBytes, 32 * Cfg::kRowBytes, kSw);
         // MN-major P^T: bf16 [256 keys][128 B]; E4M3 [key half][hi, lo][128 keys][64 B]
         const uint64_t dP0 = FP8 ? make_sdesc(sP, 512, 512, kSwizzle64) : make_sdesc(sP, 1024, 1024, kSwizzle128);
-        uint32_t r = 0, n = 0, uc = 0, pvn = 0;
+        // FP8 key tile [16 groups][9 chunks][8 rows][64 B]: K-major, 8-row groups 4.5 KB apart
+        const uint64_t dKT0 = make_sdesc(sKT, 16, 9 * 512, kSwizzle64);
+        uint32_t r = 0, n = 0, uc = 0, pvn = 0, nkt = 0;
         bool ok = true;
         struct Prev {
           int L, tile;
@@ -492,44 +689,56 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
         } prev{0, -1, false, 0};
         auto issue_pv = [&](const Prev& pv) -> bool {
           if (!wait(b_pfull, pvn & 1)) return false;
+          if (FP8) fence_proxy_async_smem();   // P^T rows that came from the peer by st.async
           if (pv.first && !wait(b_oempty, (pv.uc & 1) ^ 1)) return false;
-          for (int vs = 0; vs < 4 / Cfg::kBlocksPerSlot; ++vs) {
-            // the producer loads a value slot only if its first block starts before the end
-            if (pv.L - pv.tile * kPairKeys - 64 * Cfg::kBlocksPerSlot * vs <= 0) continue;
+          if constexpr (FP8) {
+            // value blocks of 64 keys from the ring of two
+            for (int kb = 0; kb < 4; ++kb) {
+              const int valid = pv.L - pv.tile * kPairKeys - 64 * kb;
+              if (valid <= 0) break;
+              const int ksteps = valid >= 64 ? 2 : (valid + 31) / 32;
+              const uint32_t slot = r % kVRing;
+              if (!wait(b_full + 8 * slot, (r / kVRing) & 1)) return false;
+              tc_fence_after();
+              const uint64_t ad = dV0 + (uint64_t)((slot * kVBlockBytes) >> 4);
+              // P^T of block kb: key half kb / 2, keys 64 (kb % 2) .. of it; lo 8 KB after hi
+              const uint64_t bd = dP0 + (uint64_t)(((kb >> 1) * 16384 + (kb & 1) * 4096) >> 4);
+              // M-tile j: this CTA's value columns 128 j .. (its chunks 2j, 2j + 1)
+              for (int j = 0; j < 2; ++j)
+                for (int kk = 0; kk < ksteps; ++kk) {
+                  const uint64_t aj = ad + (uint64_t)((1024 * j + 8192 * kk) >> 4);
+                  const uint64_t bk = bd + (uint64_t)((2048 * kk) >> 4);
+                  umma_pair_f8(tmem + kOCol + 128 * j, aj, bk, idesc_pv, !(pv.first && kb == 0 && kk == 0));
+                  umma_pair_f8(tmem + kOCol + 128 * j, aj, bk + (8192 >> 4), idesc_pv, 1u);
+                }
+              umma_pair_commit(b_empty + 8 * slot);
+              ++r;
+            }
+            umma_pair_commit(b_pvdone);
+            ++pvn;
+            return true;
+          } else {
+          // bf16: a value slot per 64-key block before the sequence end
+          for (int kb = 0; kb < 4; ++kb) {
+            const int valid = pv.L - pv.tile * kPairKeys - 64 * kb;
+            if (valid <= 0) break;
+            const int ksteps = valid >= 64 ? 4 : (valid + 15) / 16;
             const uint32_t slot = r % kRing;
             if (!wait(b_full + 8 * slot, (r / kRing) & 1)) return false;
             tc_fence_after();
-            for (int i = 0; i < Cfg::kBlocksPerSlot; ++i) {
-              const int kb = vs * Cfg::kBlocksPerSlot + i;
-              const int valid = pv.L - pv.tile * kPairKeys - 64 * kb;
-              if (valid <= 0) continue;
-              const int ksteps = valid >= 64 ? 64 / Cfg::kKStep : (valid + Cfg::kKStep - 1) / Cfg::kKStep;
-              const uint64_t ad = dV0 + (uint64_t)((slot * kSlotBytes + i * Cfg::kBlockBytes) >> 4);
-              if constexpr (FP8) {
-                // P^T of block kb: key half kb / 2, keys 64 (kb % 2) .. of it; lo 8 KB after hi
-                const uint64_t bd = dP0 + (uint64_t)(((kb >> 1) * 16384 + (kb & 1) * 4096) >> 4);
-                // M-tile j: this CTA's value columns 128 j .. (its chunks 2j, 2j + 1)
-                for (int j = 0; j < 2; ++j)
-                  for (int kk = 0; kk < ksteps; ++kk) {
-                    const uint64_t aj = ad + (uint64_t)((1024 * j + 8192 * kk) >> 4);
-                    const uint64_t bk = bd + (uint64_t)((2048 * kk) >> 4);
-                    umma_pair_f8(tmem + kOCol + 128 * j, aj, bk, idesc_pv, !(pv.first && kb == 0 && kk == 0));
-                    umma_pair_f8(tmem + kOCol + 128 * j, aj, bk + (8192 >> 4), idesc_pv, 1u);
-                  }
-              } else {
-                const uint64_t bd = dP0 + (uint64_t)((64 * kb * 128) >> 4);
-                for (int j = 0; j < 2; ++j)
-                  for (int kk = 0; kk < ksteps; ++kk)
-                    umma_pair_f16(tmem + kOCol + 128 * j, ad + (uint64_t)((2048 * j + 8192 * kk) >> 4),
-                                  bd + kk * (2048 >> 4), idesc_pv, !(pv.first && kb == 0 && kk == 0));
-              }
-            }
+            const uint64_t ad = dV0 + (uint64_t)((slot * kSlotBytes) >> 4);
+            const uint64_t bd = dP0 + (uint64_t)((64 * kb * 128) >> 4);
+            for (int j = 0; j < 2; ++j)
+              for (int kk = 0; kk < ksteps; ++kk)
+                umma_pair_f16(tmem + kOCol + 128 * j, ad + (uint64_t)((2048 * j + 8192 * kk) >> 4), bd + kk * (2048 >> 4),
+                              idesc_pv, !(pv.first && kb == 0 && kk == 0));
             umma_pair_commit(b_empty + 8 * slot);
             ++r;
           }
           umma_pair_commit(b_pvdone);
           ++pvn;
           return true;
+          }
         };
         for (int u = u0; u < u1 && ok; ++u, ++uc) {
           const PUnit U = load_punit(a, u);
@@ -538,7 +747,24 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
             const uint32_t sb = n & 1, sph = (n >> 1) & 1;   // S^T buffer
             ok = wait(b_sempty + 8 * sb, sph ^ 1);
             const uint32_t d = tmem + sb * 128;
-            for (int ks = 0; ks < kKeySlots && ok; ++ks) {
+            if constexpr (FP8) {
+              // the whole key tile: 9 chunks x 2 K steps, each K . hi then K . lo
+              ok = ok && wait(b_ktfull, nkt & 1);
+              if (!ok) break;
+              tc_fence_after();
+              for (int c = 0; c < 9; ++c) {
+                const uint64_t bd = dQ0 + (uint64_t)(c * (q_chunk >> 4));
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                  const uint64_t ak = dKT0 + (uint64_t)(c * (512 >> 4) + 2 * kk);
+                  umma_pair_f8(d, ak, bd + 2 * kk, idesc_qk, (c | kk) != 0);           // K . hi
+                  umma_pair_f8(d, ak, bd + (512 >> 4) + 2 * kk, idesc_qk, 1u);         // K . lo
+                }
+              }
+              umma_pair_commit(b_ktempty);
+              ++nkt;
+            }
+            for (int ks = 0; !FP8 && ks < kKeySlots && ok; ++ks) {
               const int nc = 9 - KC * ks < KC ? 9 - KC * ks : KC;   // chunks KC ks .. (the last slot: 8)
               const uint32_t slot = r % kRing;
               ok = wait(b_full + 8 * slot, (r / kRing) & 1);
@@ -548,18 +774,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
               for (int cc = 0; cc < nc; ++cc) {
                 const int c = KC * ks + cc;
                 const uint64_t bd = dQ0 + (uint64_t)(c * (q_chunk >> 4));
-                if constexpr (FP8) {
 #pragma unroll
-                  for (int kk = 0; kk < 2; ++kk) {
-                    const uint64_t ak = ad + (uint64_t)(cc * (512 >> 4) + 2 * kk);
-                    umma_pair_f8(d, ak, bd + 2 * kk, idesc_qk, (c | kk) != 0);           // K . hi
-                    umma_pair_f8(d, ak, bd + (512 >> 4) + 2 * kk, idesc_qk, 1u);         // K . lo
-                  }
-                } else {
-#pragma unroll
-                  for (int kk = 0; kk < 4; ++kk)
-                    umma_pair_f16(d, ad + (uint64_t)(cc * (1024 >> 4) + 2 * kk), bd + 2 * kk, idesc_qk, (c | kk) != 0);
-                }
+                for (int kk = 0; kk < 4; ++kk)
+                  umma_pair_f16(d, ad + (uint64_t)(cc * (1024 >> 4) + 2 * kk), bd + 2 * kk, idesc_qk, (c | kk) != 0);
               }
               umma_pair_commit(b_empty + 8 * slot);
               ++r;
@@ -873,7 +1090,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
         }
         // P^T and O^T are free once the previous PV has completed; the staging buffer once
         // the previous copy out of it has been read
-        if (t == 0 && !local_p) bulk_wait_read0();
+        if (!FP8 && t == 0 && !local_p) bulk_wait_read0();
         if (n > 0) {
           ok = wait_wg(b_pvdone, (n - 1) & 1);
           if (!ok) break;
@@ -898,40 +1115,48 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
           tmem_wait_st();
         }
         // P^T row of key 128 rank + t: into this CTA's P^T buffer (rows 64 rank ..), or, for
-        // the peer, into the staging buffer laid out as the peer's P^T rows of keys
-        // 128 rank .. 128 rank + 127
-        {
+        // the peer: bf16 into the staging buffer laid out as the peer's P^T rows of keys
+        // 128 rank .. 128 rank + 127 (sent by one bulk copy below); FP8 straight into the
+        // peer's P^T by st.async, its bytes counted on the peer's barrier
+        if constexpr (FP8) {
+          const uint32_t pdst = local_p ? sP + (uint32_t)rank * kStageBytes
+                                        : map_to_rank(sP + (uint32_t)rank * kStageBytes, peer);
+          const uint32_t pbar = map_to_rank(leader ? b_pin : b_pfull, peer);
+#pragma unroll
+          for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+            for (int u16 = 0; u16 < 4; ++u16) {
+              const uint32_t off = hl * 8192 + p_off64(t, u16);
+              const uint4 v = make_uint4(pw[16 * hl + 4 * u16], pw[16 * hl + 4 * u16 + 1], pw[16 * hl + 4 * u16 + 2],
+                                         pw[16 * hl + 4 * u16 + 3]);
+              if (local_p) *reinterpret_cast<uint4*>(gP + (pdst - sP) + off) = v;
+              else st_async_v4(pdst + off, v, pbar);
+            }
+        } else {
           uint8_t* prow = local_p ? gP + (int)rank * kStageBytes : gStage;
-          if constexpr (FP8) {
 #pragma unroll
-            for (int hl = 0; hl < 2; ++hl)
-#pragma unroll
-              for (int u16 = 0; u16 < 4; ++u16)
-                *reinterpret_cast<uint4*>(prow + hl * 8192 + p_off64(t, u16)) =
-                    make_uint4(pw[16 * hl + 4 * u16], pw[16 * hl + 4 * u16 + 1], pw[16 * hl + 4 * u16 + 2],
-                               pw[16 * hl + 4 * u16 + 3]);
-          } else {
-#pragma unroll
-            for (int u16 = 0; u16 < 8; ++u16)
-              *reinterpret_cast<uint4*>(prow + p_off128(t, u16)) =
-                  make_uint4(pw[4 * u16], pw[4 * u16 + 1], pw[4 * u16 + 2], pw[4 * u16 + 3]);
-          }
+          for (int u16 = 0; u16 < 8; ++u16)
+            *reinterpret_cast<uint4*>(prow + p_off128(t, u16)) =
+                make_uint4(pw[4 * u16], pw[4 * u16 + 1], pw[4 * u16 + 2], pw[4 * u16 + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         named_bar_sync(bar, 128);
         if (t == 0) {
           if (!local_p) {
-            // rows for the peer's P^T: one bulk copy, counted on the peer's barrier (the even
-            // CTA's P^T barrier, or the odd CTA's b_pin)
-            bulk_copy_to_cluster(map_to_rank(sP + (uint32_t)rank * kStageBytes, peer), sStage, kStageBytes,
-                                 map_to_rank(leader ? b_pin : b_pfull, peer));
-            bulk_commit();
+            // bf16: the rows for the peer's P^T in one bulk copy, counted on the peer's barrier
+            // (the even CTA's P^T barrier, or the odd CTA's b_pin); FP8: already sent
+            if (!FP8) {
+              bulk_copy_to_cluster(map_to_rank(sP + (uint32_t)rank * kStageBytes, peer), sStage, kStageBytes,
+                                   map_to_rank(leader ? b_pin : b_pfull, peer));
+              bulk_commit();
+            }
           } else if (leader) {
-            mbar_arrive_expect_tx(b_pfull, kStageBytes);   // own rows; the odd CTA's copy to come
+            mbar_arrive_expect_tx(b_pfull, kStageBytes);   // own rows; the odd CTA's rows to come
           } else {
             mbar_arrive_expect_tx(b_pin, kStageBytes);
-            ok = mbar_wait(b_pin, n & 1, abort_flag, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);   // the even CTA's copy
+            ok = mbar_wait(b_pin, n & 1, abort_flag, err, MLA_DEVERR_TIMEOUT, a.wait_limit_ns);   // the even CTA's rows
+            if (FP8 && ok) fence_proxy_async_smem();   // rows that came by st.async, for the MMAs
             if (ok) mbar_arrive_cluster(lead(b_pfull));
             else fail_peer();
           }
@@ -1029,7 +1254,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
       gn += T;
     }
     // a copy out of the staging buffer has landed before the CTA may leave
-    if (t == 0 && !local_p) bulk_wait0();
+    if (!FP8 && t == 0 && !local_p) bulk_wait0();
   }
 
   // ================================================================ teardown
@@ -1043,7 +1268,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
 template <bool FP8, bool kSub>
 static cudaError_t prepare_pair_variant() {
   cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<FP8, kSub>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kPairDynBytes);
+                                       pair_dyn_bytes(FP8));
   if (e != cudaSuccess) return e;
   cudaFuncAttributes attr;
   e = cudaFuncGetAttributes(&attr, decode_pair_kernel<FP8, kSub>);
@@ -1057,7 +1282,7 @@ static cudaError_t launch_pair_variant(const DecodeArgs& a, int pairs, cudaStrea
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(kPairThreads);
-  cfg.dynamicSmemBytes = kPairDynBytes;
+  cfg.dynamicSmemBytes = pair_dyn_bytes(FP8);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -238,6 +238,16 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
                : "memory");
 }
 // Arrive once on `bar` when every tcgen05 op this thread issued so far has completed.
+// E4M3 operands from shared memory (kind::f8f6f4; format code 0 of the instruction
+// descriptor's A and B fields is E4M3 there), K = 32 per instruction.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "setp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+               :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                :: "r"(bar) : "memory");
@@ -268,6 +278,25 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
   d |= 1ull << 46;
   d |= static_cast<uint64_t>(swizzle & 7u) << 61;
   return d;
+}
+
+// x0, x1 (|x| < 448) as E4M3 pairs hi and lo with hi + lo ~ x: on the fp16 roundings h of
+// x, hi is h truncated to 4 significant bits (its low 7 mantissa bits cleared), exact in
+// E4M3 wherever |h| >= 2^-6, and lo = h - hi (exact in fp16) rounded to E4M3 (nearest
+// even, saturating). A value with at most 8 significant bits (a bf16 q, say) is split
+// exactly while lo stays a normal E4M3 number. Returns hi in bits 0-15 and lo in bits
+// 16-31, element 0 in the lower byte of each.
+__device__ __forceinline__ uint32_t split_e4m3x2(float x0, float x1) {
+  uint32_t out;
+  asm("{\n\t.reg .b32 h, t, r;\n\t.reg .b16 hb, lb;\n\t"
+      "cvt.rn.f16x2.f32 h, %2, %1;\n\t"
+      "and.b32 t, h, 0xFF80FF80;\n\t"
+      "sub.rn.f16x2 r, h, t;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 hb, t;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 lb, r;\n\t"
+      "mov.b32 %0, {hb, lb};\n\t}"
+      : "=r"(out) : "f"(x0), "f"(x1));
+  return out;
 }
 
 // Hardware exp2 (MUFU), approximate, subnormal results flushed to zero.

@@ -13,6 +13,10 @@
 //   P: thread t writes key row t (N bytes, 64-byte swizzle for N = 64): MN-major B, 8-key
 //      groups 512 B apart
 //   2 MMAs of K = 32 keys.
+// mode 2 ("values, P unswizzled"): as mode 1 with N in {16, 32, 64} and P written without
+//   swizzle: key row t's N bytes as N / 16 core matrices of 16 B, [8-key group][core][8 keys]
+//   [16 B]: MN-major B without swizzle, where the leading offset steps along K (8-key groups,
+//   LBO = 8 N bytes) and the stride offset along MN (cores, SBO = 128 B).
 // All waits are bounded; out-of-range modes return an error before launching.
 #include <cstdint>
 #include <cstring>
@@ -79,6 +83,18 @@ __global__ void __launch_bounds__(128, 1) f8_probe_kernel(const __grid_constant_
         *reinterpret_cast<uint4*>(g + 16384 + sw64(atom, t, u & 3)) = v;
       }
     }
+  } else if (mode == 2) {
+    if (t == 0) {
+      mbar_arrive_expect_tx(bt, 8192);
+      tma_load_4d(sA, &tma_a, bt, 0, 0, 0, 0);
+    }
+    // P key row t (t < 64): n bytes, one 16-byte unit per core matrix
+    if (t < 64) {
+      for (int c = 0; c < n / 16; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(b_glob + t * n + c * 16);
+        *reinterpret_cast<uint4*>(g + 16384 + (t >> 3) * (8 * n) + c * 128 + (t & 7) * 16) = v;
+      }
+    }
   } else {
     if (t == 0) {
       mbar_arrive_expect_tx(bt, 8192);
@@ -103,6 +119,13 @@ __global__ void __launch_bounds__(128, 1) f8_probe_kernel(const __grid_constant_
         const uint32_t off = (uint32_t)(kk >> 1) * 512u + (uint32_t)(kk & 1) * 32u;
         const uint64_t ad = make_sdesc(sA + off, 16, 1024, kSwizzle64);
         const uint64_t bd = make_sdesc(sB + off, 16, 1024, kSwizzle64);
+        mma_f8(tmem, ad, bd, idesc, kk > 0);
+      }
+    } else if (mode == 2) {
+      const uint32_t idesc = make_idesc(128, (uint32_t)n, 0, 1, 1);
+      for (int kk = 0; kk < 2; ++kk) {
+        const uint64_t ad = make_sdesc(sA + kk * 4096, 512, 1024, kSwizzle64);
+        const uint64_t bd = make_sdesc(sB + kk * 32 * n, 8 * n, 128, kSwizzleNone);
         mma_f8(tmem, ad, bd, idesc, kk > 0);
       }
     } else {
@@ -159,12 +182,13 @@ static int make_map(CUtensorMap* m, const void* ptr, uint64_t rows) {
 
 // mode 0: a [128 x 128] E4M3, b [n x 128] E4M3, n in {16, 32, 64}.
 // mode 1: a = V [64 x 128] E4M3, b = P [64 x 64] E4M3 (n = 64).
+// mode 2: a = V [64 x 128] E4M3, b = P [64 x n] E4M3, n in {16, 32, 64}.
 // d [128 x n] float32. err: device uint32 (1 = TMA wait gave up, 2 = MMA wait gave up).
 extern "C" __attribute__((visibility("default"))) int umma_f8_probe(int mode, int n, const void* a,
                                                                     const void* b, float* d,
                                                                     uint32_t* err, cudaStream_t s) {
-  if (mode < 0 || mode > 1 || !a || !b || !d || !err) return -1;
-  if (mode == 0 ? (n != 16 && n != 32 && n != 64) : n != 64) return -1;
+  if (mode < 0 || mode > 2 || !a || !b || !d || !err) return -1;
+  if (mode == 1 ? n != 64 : (n != 16 && n != 32 && n != 64)) return -1;
   if (!encoder()) return -2;
   CUtensorMap ta;
   if (make_map(&ta, a, mode == 0 ? 128 : 64)) return -3;

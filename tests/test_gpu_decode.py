@@ -248,10 +248,11 @@ def test_out_of_range_block_table_entry_is_reported_not_faulted(H, P, kv, entry)
 
 
 def test_fp8_query_beyond_the_float16_range_is_reported():
-    """With an FP8 cache the MMAs run in fp16, so q is converted bf16 -> fp16; a query value
-    above the fp16 range is flagged in the device error word (MLA_DEVERR_Q_RANGE) rather
-    than silently saturated, and a clean call afterwards reports nothing."""
-    case = synth.make_case(B=2, s_q=1, H=16, page_size=64, seq_lens=[100, 200], seed=47, kv_dtype=F8)
+    """With an FP8 cache and 33-64 rows the MMAs run in fp16, so q is converted bf16 -> fp16;
+    a query value above the fp16 range is flagged in the device error word
+    (MLA_DEVERR_Q_RANGE) rather than silently saturated, and a clean call afterwards
+    reports nothing."""
+    case = synth.make_case(B=2, s_q=1, H=64, page_size=64, seq_lens=[100, 200], seed=47, kv_dtype=F8)
     g = GpuCase(case)
     q0 = g.q.clone()
     g.q[1, 0, 5, 17] = 1.0e5                       # a bf16 value, above 65504
@@ -285,6 +286,34 @@ def test_fp8_pairs_take_any_bf16_query_magnitude():
     ro, rl = oracle_decode(case, g.cache_numpy())
     # the output contract on every row; the LSE of rows scaled by 1e30 or 3e38 is itself of
     # that size, where one float32 step is ~1e23 to ~1e30: those get a relative bound
+    lg = lse.cpu().numpy().astype(np.float64)
+    big = np.abs(rl) > 1.0e6
+    assert big.sum() == 2
+    assert (np.abs(lg - rl)[big] <= 1.0e-6 * np.abs(rl[big])).all()
+    compare(case, out, lse, ro, rl, rows=np.argwhere(~big))
+    og = out.float().cpu().numpy().astype(np.float64)
+    assert (np.abs(og - ro)[big] <= 2.0e-2).all()
+
+
+@pytest.mark.parametrize("H", [16, 32])
+def test_fp8_16_and_32_rows_take_any_bf16_query_magnitude(H):
+    """With an FP8 cache and up to 32 rows the keys stay E4M3 in the MMAs too: each unit's q
+    rows are scaled per row by a power of two and split into two E4M3 terms, so rows of very
+    different magnitude (1e30, 1e-30, 3e38 with a tiny neighbour, all zero) decode with no
+    error bit and within the FP8 tolerance of the oracle."""
+    case = synth.make_case(B=2, s_q=1, H=H, page_size=64, seq_lens=[700, 300], seed=53 + H, kv_dtype=F8)
+    q = torch.from_numpy(case.q_bits.view(np.int16).copy()).view(torch.bfloat16).float()
+    q[0, 0, 3, :] *= 1.0e30
+    q[0, 0, 7, :] *= 1.0e-30
+    q[1, 0, 5, :] = 0.0
+    q[1, 0, 9, :] = 0.0
+    q[1, 0, 9, 100] = 3.0e38
+    q[1, 0, 9, 101] = -1.0e-38
+    case.q_bits[...] = q.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    g = GpuCase(case)
+    out, lse = g.decode()
+    assert api.decode_check(g.workspace) == (0, 0)
+    ro, rl = oracle_decode(case, g.cache_numpy())
     lg = lse.cpu().numpy().astype(np.float64)
     big = np.abs(rl) > 1.0e6
     assert big.sum() == 2

@@ -4,7 +4,9 @@ decode, checked on known matrices.
 Scores: K-major A (TMA, 64-byte swizzle, the cache's key boxes) and K-major B written by
 threads in the same layout; K advanced 32 bytes inside the swizzle atom.
 Values: MN-major A straight from the cache's row layout (64-byte swizzle, two 64-column
-chunks) and MN-major B (one 64-byte swizzled key row per thread).
+chunks) and MN-major B (one 64-byte swizzled key row per thread), or MN-major B without
+swizzle (each key row's N bytes as N / 16 core matrices of 16 bytes, for 16 to 64 query
+rows).
 The products of two E4M3 values are exact in float32, so on integer-valued operands the
 sums are exact too and the comparison is strict; random codes use a relative bound.
 """
@@ -76,6 +78,21 @@ def test_values_layout_e4m3(probe, small_ints):
     v = e4m3_codes((64, 128), g, small_ints)
     p = e4m3_codes((64, 64), g, small_ints)
     d = run(probe, 1, 64, v.cuda(), p.cuda())
+    ref = as_f64(v).T @ as_f64(p)
+    if small_ints:
+        assert torch.equal(d, ref), (d - ref).abs().max()
+    else:
+        bound = (as_f64(v).abs().T @ as_f64(p).abs()) * 2.0 ** -20
+        assert ((d - ref).abs() <= bound).all(), ((d - ref).abs() / bound.clamp_min(1e-30)).max()
+
+
+@pytest.mark.parametrize("n", [16, 32, 64])
+@pytest.mark.parametrize("small_ints", [True, False])
+def test_values_layout_e4m3_unswizzled_p(probe, n, small_ints):
+    g = torch.Generator().manual_seed(500 + n + small_ints)
+    v = e4m3_codes((64, 128), g, small_ints)
+    p = e4m3_codes((64, n), g, small_ints)
+    d = run(probe, 2, n, v.cuda(), p.cuda())
     ref = as_f64(v).T @ as_f64(p)
     if small_ints:
         assert torch.equal(d, ref), (d - ref).abs().max()
