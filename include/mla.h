@@ -37,7 +37,8 @@
  * - Host-detectable errors return a negative mla_status and launch nothing.
  *   Errors only the device can see (a block-table entry outside [0, num_pages), a
  *   sequence length outside [s_q, min(max_seq_len, max_blocks_per_seq*page_size)],
- *   an FP8-path query value outside the float16 range, a stalled pipeline) set bits
+ *   with the FP8 cache and 33-64 query rows a query value outside the float16 range,
+ *   a stalled pipeline) set bits
  *   of a device error word; mla_decode_check() reads it. Such entries are not
  *   dereferenced out of bounds.
  * - Asynchronous CUDA faults surface at the caller's next synchronisation.
@@ -74,7 +75,7 @@ typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
 /* Device error word bits (see mla_decode_check). */
 #define MLA_DEVERR_BLOCK_TABLE   0x1u   /* block_table entry outside [0, num_pages) */
 #define MLA_DEVERR_SEQ_LEN       0x2u   /* seq_lens[b] outside the allowed range */
-#define MLA_DEVERR_Q_RANGE       0x4u   /* FP8 cache: |q| above the float16 range */
+#define MLA_DEVERR_Q_RANGE       0x4u   /* FP8 cache, 33-64 rows: |q| above the float16 range */
 #define MLA_DEVERR_TIMEOUT       0x8u   /* a bounded pipeline wait expired */
 #define MLA_DEVERR_SLOT          0x10u  /* cache write: slot >= num_pages*page_size */
 

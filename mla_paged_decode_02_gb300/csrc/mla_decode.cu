@@ -28,21 +28,28 @@
 //   warp 1      QK^T issuer (one thread): Q of each unit (TMA), then per tile the S^T
 //               buffer and every key slot in program order.
 //   warp 3      PV issuer (one thread): per tile P^T, then the four value chunk pairs.
-//   FP8 cache (384 threads):
+//   FP8 cache (384 threads): the MMAs read the E4M3 cache bytes as TMA landed them
+//   (kind::f8f6f4), q and P entering as two E4M3 terms each (hi and lo).
+//   16 or 32 rows:
+//   warp 2      key-stage producer (one thread; the warp zeroes tail rows): each tile's
+//               128 whole 576-byte rows into one of two stages, once the PV MMAs of the
+//               tile that used it have completed; the stage serves both QK^T (keys) and
+//               PV (values, the rows' first 512 bytes).
+//   warps 8-11  each unit's Q, bf16 -> q' = q 2^e as E4M3 hi and lo in place, with the
+//               row factors 2^-e for the softmax.
+//   64 rows:
 //   warps 8-11  one thread per key row: each unit's Q to fp16 in place; every raw E4M3
 //               key position (TMA-staged) to fp16 in a tensor-memory key slot, read by
-//               the QK^T MMAs as their A operand.
-//   warp 2      raw value producer (one thread): value chunk pairs into a raw staging
-//               ring.
+//               the QK^T MMAs as their A operand (kind::f16).
+//   warp 2      raw value producer: 4-chunk E4M3 value stages, read by the PV MMAs.
 //   warps 0, 1  PV and QK^T issuers.
 //   both:
 //   warps 4-7   softmax (one thread per key of the tile = one TMEM lane): scale, causal
 //               mask, online softmax with a lazily-rescaled running max (the reference
-//               max moves only when a score exceeds it by more than 2^8, so O^T is
-//               rescaled rarely; the final normalisation uses the same reference, so the
-//               result is exact), P^T to shared memory; FP8: then the tile's four value
-//               pairs from the raw ring into the fp16 value ring;
-//               epilogue (O^T / l -> output or split partial plus LSE).
+//               max moves only when a score exceeds it by more than 2^8 (FP8: 2^4), so
+//               O^T is rescaled rarely; the final normalisation uses the same reference,
+//               so the result is exact), P^T to shared memory; epilogue (O^T / l ->
+//               output or split partial plus LSE).
 //
 // Every wait is bounded (mla_ptx.cuh): a stall sets the device error word and the CTA
 // waits for its in-flight copies and MMAs, frees its tensor memory and exits. Value rows
@@ -65,7 +72,7 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kSoftmaxBar = 1;          // named barrier of the 4 softmax warps
-constexpr uint32_t kKeyDqBar = 2;            // FP8 key dequantising warps 8-11
+constexpr uint32_t kKeyDqBar = 2;            // FP8: warps 8-11 (Q, and keys with 64 rows)
 constexpr int kKeyDqThreads = 128;
 constexpr int kSmemLimit = 232448;           // 227 KB per CTA
 constexpr int kStaticBudget = 3072;          // static shared memory (barriers, scratch)
@@ -89,13 +96,13 @@ struct Cfg {
   static constexpr int kSlotsPerTile = 9 / KC;
   // Ring layouts, as strides of the MMA operand descriptors. bf16 (TMA boxes): a key slot
   // is [16 row groups][KC chunks][8 rows x 128 B], a value slot [16 groups][2 chunks][...].
-  // FP8 (written by the dequantising threads): [chunk][16 groups][8 rows x 128 B].
+  // FP8 with 64 rows: the keys dequantised into tensor memory (below).
   static constexpr uint32_t kKGroupStride = FP8 ? 1024 : KC * 1024;    // key operand SBO
   static constexpr uint32_t kKChunkStride = FP8 ? kChunkBytes : 1024;
   static constexpr uint32_t kVChunkStride = FP8 ? kChunkBytes : 1024;  // value operand LBO
   static constexpr uint32_t kVGroupStride = FP8 ? 1024 : 2048;         // value operand SBO
-  // FP8: the dequantised key slots live in tensor memory after S^T (2 RC columns) and
-  // O^T (4 RC columns), KC chunks x 32 columns each (two fp16 per 32-bit column)
+  // FP8 with 64 rows: the dequantised key slots live in tensor memory after S^T (2 RC
+  // columns) and O^T (4 RC columns), KC chunks x 32 columns each (two fp16 per column)
   static constexpr int kKTmemBase = 6 * RC;
   static constexpr int kKTmemSlotCols = KC * 32;
   static constexpr int NK = FP8 ? (RC == 32 ? 3 : 4) : (RC < 64 ? 2 : 3);
@@ -171,16 +178,10 @@ __device__ __forceinline__ float unordered(int k) {
   return __int_as_float(k ^ ((k >> 31) & 0x7FFFFFFF));
 }
 
-// Two probabilities rounded to the MMA operand type (fp16 for the FP8 cache, else bf16).
-template <bool FP8>
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-  if (FP8) {
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-  } else {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-  }
+// Two probabilities rounded to bf16 (the bf16 cache's P).
+__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
 // Walks the key tiles of this CTA's units in the order every role consumes them, with
@@ -777,8 +778,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
             pw[r / 4] = __byte_perm(o0, o1, 0x5410);
             pw[RC / 4 + r / 4] = __byte_perm(o0, o1, 0x7632);
           } else {
-            pw[r / 2] = pack2<FP8>(pr[0], pr[1]);
-            pw[r / 2 + 1] = pack2<FP8>(pr[2], pr[3]);
+            pw[r / 2] = pack2_bf16(pr[0], pr[1]);
+            pw[r / 2 + 1] = pack2_bf16(pr[2], pr[3]);
           }
         }
         // the buffer's previous user, PV(n - NP), must have completed
