@@ -126,6 +126,17 @@ SMALL = [
     (3, 1, 128, 128, [64, 65, 190], F8, True),       # block edges, ragged 32-key steps
     (4, 1, 128, 128, [32, 33, 95, 96], F8, True),    # 32-key step edges
     (2, 1, 100, 64, [500, 129], F8, True),           # rows not a multiple of 8: Q by chunks
+    # FP8 with 16 or 32 rows: E4M3 MMAs on whole-row key stages
+    (1, 1, 16, 64, [1], F8, True),                   # a single key
+    (3, 1, 16, 64, [127, 128, 129], F8, True),       # tile edges
+    (4, 1, 16, 128, [32, 33, 95, 96], F8, True),     # 32-key step edges
+    (4, 1, 16, 64, [5000, 17, 640, 2049], F8, True), # several splits, ragged tail
+    (3, 1, 16, 8, [1, 9, 300], F8, True),            # 8-row pages
+    (2, 1, 32, 64, [200, 129], F8, True),            # 32 rows
+    (2, 1, 20, 64, [77, 333], F8, True),             # a ragged row group
+    (2, 2, 16, 64, [300, 129], F8, False),           # 32 rows from s_q = 2, non-causal
+    (2, 4, 4, 64, [700, 4], F8, True),               # 16 rows from s_q = 4, causal
+    (3, 1, 32, 16, [1, 95, 300], F8, True),          # 16-row pages, 32 rows
     (2, 2, 64, 64, [1000, 65], F8, True),            # 128 rows from s_q = 2
     (3, 1, 128, 16, [1, 255, 513], F8, True),        # pages smaller than a block
     (2, 1, 128, 24, [77, 1000], F8, True),
