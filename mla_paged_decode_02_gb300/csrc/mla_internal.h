@@ -43,7 +43,7 @@ inline int plan_workers(const Plan& p, int num_sms) { return p.pair ? num_sms / 
 //            [split_list int4 x max_split][units int4 x max_units]
 //            [part_lse f32 x max_slots*RC][part_o f32 x max_slots*RC*512]
 // header word 0: device error bits; 1: number of units; 2: number of split streams;
-// 3: tiles per CTA (q). The bounds follow from the partition (mla_schedule.cu): every
+// 3: positions per CTA (q); 4: positions charged at the start of every stream (X). The bounds follow from the partition (mla_schedule.cu): every
 // CTA boundary cuts at most one (sequence, row group) stream, so there are at most
 // B*G + grid - 1 units, grid - 1 split streams and 2*(grid - 1) partial slots.
 struct WsLayout {
@@ -80,6 +80,7 @@ struct SchedArgs {
   int4* units;           // (b, g, tile_begin | tile_end << 16, partial slot or -1)
   int32_t B, s_q, G, max_len, grid;
   int32_t tile;          // keys per tile (128, or 256 for CTA pairs)
+  int32_t setup;         // tiles' worth of work charged at the start of every stream
   // fused cache write of the step's new tokens (w_n > 0): done before the schedule
   const uint4* w_latent;
   const uint4* w_rope;

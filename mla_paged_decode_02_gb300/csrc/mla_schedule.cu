@@ -9,11 +9,15 @@
 //
 // Work is counted in (key tile, row group) pairs. Sequence b has n_b = ceil(L_b / T)
 // key tiles (T = 128, or 256 for CTA pairs) and G groups of query rows; each (g, b) is a
-// stream of n_b tiles, and the streams are laid end to end, group-major:
-//   pos(g, b) = g * N + sum_{b' < b} n_b',    N = sum_b n_b,    W = G * N,
+// stream of X + n_b positions — X for the set-up of a unit (loading and converting its
+// q, refilling the pipeline, its epilogue; about two tiles of streaming) and one per tile —
+// and the streams are laid end to end, group-major:
+//   pos(g, b) = g * N + sum_{b' < b} (X + n_b'),    N = sum_b (X + n_b),    W = G * N,
 // The persistent decode grid has one CTA per SM; CTA c takes the positions
-// [c q, (c + 1) q) with q = ceil(W / grid), so no CTA has more than one tile more work
-// than another whatever the length mix. When G divides the grid, each row group instead
+// [c q, (c + 1) q) with q = ceil(W / grid), i.e. the tiles among them, so no CTA has
+// more than one tile more work than another (counting a unit's set-up) whatever the length
+// mix. X is dropped when a CTA's share would be too small for it (q <= 2 X): then every
+// CTA range holds at least one tile. When G divides the grid, each row group instead
 // gets exactly grid / G CTAs and the same partition of its N tiles (q = ceil(N G / grid)):
 // CTA c + k grid / G then reads the same key tiles as CTA c, in the same order and at about
 // the same time, so of the G reads of every key tile only the first comes from DRAM. A stream that a CTA boundary cuts becomes one
@@ -115,25 +119,33 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
   }
   __syncthreads();                     // batch_info (global, this block's writes) and n_tiles_s
   const int64_t n_tiles = n_tiles_s;
-  const int64_t W = (int64_t)G * n_tiles;
   const bool aligned = G > 1 && a.grid % G == 0;   // one CTA block per row group
   const int cpg = aligned ? a.grid / G : a.grid;    // CTAs per row group
-  const int64_t q = aligned ? (n_tiles + cpg - 1) / cpg : (W + a.grid - 1) / a.grid;   // >= 1
+  int X = a.setup > 0 ? a.setup : 0;
+  int64_t Nv = n_tiles + (int64_t)B * X;            // positions of one row group
+  int64_t q = aligned ? (Nv + cpg - 1) / cpg : ((int64_t)G * Nv + a.grid - 1) / a.grid;   // >= 1
+  if (X > 0 && q <= 2 * (int64_t)X) {
+    X = 0;
+    Nv = n_tiles;
+    q = aligned ? (Nv + cpg - 1) / cpg : ((int64_t)G * Nv + a.grid - 1) / a.grid;
+  }
 
   // 2. the (row group g, sequence b) streams in position order, flattened: item i = g B + b,
-  //    stream start pos = (aligned ? 0 : g N) + first tile of b. Every stream is cut at the
-  //    CTA boundaries it crosses (multiples of q): ns pieces, one unit each; a cut stream
-  //    (ns >= 2) gets ns consecutive partial slots and an entry in the split list.
+  //    stream start pos = (aligned ? 0 : g N) + b X + first tile of b, its tiles from
+  //    pos + X on. Every stream is cut at the CTA boundaries its tiles cross (multiples of
+  //    q): ns pieces, one unit each; a cut stream (ns >= 2) gets ns consecutive partial
+  //    slots and an entry in the split list.
   const int64_t items = (int64_t)G * B;
   const int64_t ichunk = (items + kSchedThreads - 1) / kSchedThreads;
   const int64_t i0 = (int64_t)tid * ichunk, i1 = min(items, i0 + ichunk);
   auto pieces = [&](int64_t i, int64_t* pre_out, int* n_out) -> int64_t {
     const int g = (int)(i / B), b = (int)(i - (int64_t)g * B);
     const int4 bi = a.batch_info[b];
-    const int64_t pre = (aligned ? 0 : (int64_t)g * n_tiles) + bi.y;
+    const int64_t pre = (aligned ? 0 : (int64_t)g * Nv) + (int64_t)b * X + bi.y;   // the stream's start
+    const int64_t ts = pre + X;                                                        // its first tile
     *pre_out = pre;
     *n_out = bi.x;
-    return (pre + bi.x - 1) / q - pre / q + 1;
+    return (ts + bi.x - 1) / q - ts / q + 1;
   };
   int64_t my_units = 0, my_split = 0, my_slots = 0;
   for (int64_t i = i0; i < i1; ++i) {
@@ -164,16 +176,18 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
     const int g = (int)(i / B), b = (int)(i - (int64_t)g * B);
     const int cbase = aligned ? g * cpg : 0;
     if (b == 0 && g > 0) gend_s[g - 1] = (int32_t)unit_off;   // the units of groups < g end here
-    const int64_t c_lo = pre / q;
+    const int64_t ts = pre + X;
+    const int64_t c_lo = ts / q;
     const int slot0 = ns >= 2 ? (int)slot_off : -1;
     if (ns >= 2) a.split_list[split_off++] = make_int4(b, g, ns, slot0);
     for (int k = 0; k < ns; ++k) {
       const int64_t c = c_lo + k;
-      const int64_t s0 = pre > c * q ? pre : c * q;
-      const int64_t s1 = pre + n < (c + 1) * q ? pre + n : (c + 1) * q;
-      const int tb = (int)(s0 - pre), te = (int)(s1 - pre);
+      const int64_t s0 = ts > c * q ? ts : c * q;
+      const int64_t s1 = ts + n < (c + 1) * q ? ts + n : (c + 1) * q;
+      const int tb = (int)(s0 - ts), te = (int)(s1 - ts);
       a.units[unit_off] = make_int4(b, g, tb | (te << 16), ns >= 2 ? slot0 + k : -1);
-      if (s0 == c * q) a.cta_first[cbase + c] = (int32_t)unit_off;
+      // the CTA's first unit: its range starts at this piece, or inside this stream's set-up
+      if (s0 == c * q || (k == 0 && pre <= c * q)) a.cta_first[cbase + c] = (int32_t)unit_off;
       ++unit_off;
     }
     if (ns >= 2) slot_off += ns;
@@ -189,6 +203,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(SchedArgs a) {
     a.hdr[1] = (uint32_t)n_units;
     a.hdr[2] = (uint32_t)n_split;
     a.hdr[3] = (uint32_t)(q < 0xFFFFFFFFll ? q : 0xFFFFFFFFll);
+    a.hdr[4] = (uint32_t)X;
   }
 }
 

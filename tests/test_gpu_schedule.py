@@ -1,9 +1,10 @@
 """The split scheduler's partition, read back from the workspace after a decode.
 
-The scheduler lays the (row group, sequence) streams of key tiles end to end and gives
-CTA c the positions [c q, (c + 1) q), q = ceil(W / grid); when the G row groups divide the
-grid, each group gets grid / G CTAs and the same partition of its N tiles instead
-(q = ceil(N / (grid / G))). With more than 64 rows the workers are CTA pairs
+The scheduler lays the (row group, sequence) streams end to end, each X positions for a
+unit's set-up followed by one position per key tile, and gives CTA c the tiles among the
+positions [c q, (c + 1) q), q = ceil(W / grid); when the G row groups divide the grid, each
+group gets grid / G CTAs and the same partition of its N positions instead
+(q = ceil(N / (grid / G))). X (header word 4) is 0 when q would be at most 2 X. With more than 64 rows the workers are CTA pairs
 (grid = #SM / 2), a row group is 128 rows and a tile 256 keys. Checked here on the device's own output: every tile of every
 stream is covered exactly once, every CTA's units are a contiguous range holding exactly
 its share of tiles, and only streams cut by a CTA boundary get partial slots (consecutive
@@ -49,21 +50,26 @@ def _offsets(B, R, grid):
     return rc, G, cta, split, units
 
 
+BF, F8 = synth.KV_BF16, synth.KV_FP8_E4M3
 CASES = [
-    (2, 1, 16, 64, [100, 257]),
-    (4, 1, 16, 64, [5000, 17, 640, 2049]),
-    (3, 4, 128, 64, [1000, 67, 3000]),
-    (2, 1, 128, 128, [300, 1000]),
-    (2, 2, 128, 64, [4000, 70]),
-    (3, 1, 96, 64, [500, 129, 20000]),
-    (1, 1, 16, 64, [131072]),
-    (300, 1, 16, 64, (1, 700)),
+    (2, 1, 16, 64, [100, 257], BF),
+    (4, 1, 16, 64, [5000, 17, 640, 2049], BF),
+    (3, 4, 128, 64, [1000, 67, 3000], BF),
+    (2, 1, 128, 128, [300, 1000], BF),
+    (2, 2, 128, 64, [4000, 70], BF),
+    (3, 1, 96, 64, [500, 129, 20000], BF),
+    (1, 1, 16, 64, [131072], BF),
+    (300, 1, 16, 64, (1, 700), BF),
+    (4, 1, 16, 64, [5000, 17, 640, 2049], F8),    # a set-up charge of 4 per stream
+    (300, 1, 16, 64, (1, 700), F8),
+    (2, 1, 16, 64, [100, 257], F8),               # shares too small for it: dropped
+    (3, 1, 128, 64, [1500, 130, 9000], F8),
 ]
 
 
-@pytest.mark.parametrize("B,s_q,H,P,lens", CASES)
-def test_partition_is_exact_and_balanced(B, s_q, H, P, lens):
-    case = synth.make_case(B=B, s_q=s_q, H=H, page_size=P, seq_lens=lens, seed=71 + B)
+@pytest.mark.parametrize("B,s_q,H,P,lens,kv", CASES)
+def test_partition_is_exact_and_balanced(B, s_q, H, P, lens, kv):
+    case = synth.make_case(B=B, s_q=s_q, H=H, page_size=P, seq_lens=lens, seed=71 + B, kv_dtype=kv)
     g = GpuCase(case)
     g.decode()
     torch.cuda.synchronize()
@@ -71,26 +77,37 @@ def test_partition_is_exact_and_balanced(B, s_q, H, P, lens):
     _, tile, grid = _plan(R, torch.cuda.get_device_properties(0).multi_processor_count)
     rc, G, cta_off, split_off, units_off = _offsets(B, R, grid)
     ws = g.workspace.cpu().numpy().view(np.uint8)
-    hdr = ws[:16].view(np.uint32)
-    n_units, n_split, q = int(hdr[1]), int(hdr[2]), int(hdr[3])
+    hdr = ws[:32].view(np.uint32)
+    n_units, n_split, q, X = int(hdr[1]), int(hdr[2]), int(hdr[3]), int(hdr[4])
     assert hdr[0] == 0
     cta_first = ws[cta_off:cta_off + 4 * (grid + 1)].view(np.int32)
     units = ws[units_off:units_off + 16 * n_units].view(np.int32).reshape(n_units, 4)
     splits = ws[split_off:split_off + 16 * n_split].view(np.int32).reshape(n_split, 4)
 
     n_b = (case.seq_lens.astype(np.int64) + tile - 1) // tile
-    N = int(n_b.sum())
-    W = G * N
     aligned = G > 1 and grid % G == 0
     cpg = grid // G if aligned else grid
-    assert q == (-(-N // cpg) if aligned else -(-W // grid))
+    qs = lambda x: -(-(int(n_b.sum()) + B * x) // cpg) if aligned else -(-G * (int(n_b.sum()) + B * x) // grid)
+    # charged per stream: 2 for CTA pairs, 4 for the FP8 cache and 0 for bf16 up to 64 rows,
+    # dropped when a CTA's share would be at most twice that
+    want = 2 if R > 64 else (4 if case.kv_dtype == synth.KV_FP8_E4M3 else 0)
+    assert X == (want if qs(want) > 2 * want else 0)
+    N = int(n_b.sum()) + B * X                       # positions of one row group
+    W = G * N
+    assert q == qs(X)
+    # every stream's tiles as an interval of positions
+    starts = np.concatenate([[0], np.cumsum(n_b + X)[:-1]])
+    tiles_of = {(b, gg): ((0 if aligned else gg * N) + int(starts[b]) + X, int(n_b[b]))
+                for b in range(B) for gg in range(G)}
     assert cta_first[grid] == n_units and np.all(np.diff(cta_first) >= 0)
     tb = units[:, 2] & 0xFFFF
     te = units[:, 2] >> 16
     assert np.all(te > tb)
     for c in range(grid):
-        cc, total = (c % cpg, N) if aligned else (c, W)
-        share = max(0, min((cc + 1) * q, total) - cc * q)
+        cc = c % cpg if aligned else c
+        lo, hi = cc * q, (cc + 1) * q
+        share = sum(max(0, min(hi, t0 + n) - max(lo, t0)) for (b, gg), (t0, n) in tiles_of.items()
+                    if not aligned or gg == c // cpg)
         sl = slice(cta_first[c], cta_first[c + 1])
         assert int((te[sl] - tb[sl]).sum()) == share, c
         if aligned:
