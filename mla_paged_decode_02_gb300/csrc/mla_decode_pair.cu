@@ -43,16 +43,18 @@
 // same warpgroup of the peer whether any of its scores exceeds the reference by more than
 // the rescale threshold (and, only then, its row maxima) through distributed shared
 // memory; both then move the reference identically. P^T rows 64w.. go to CTA w's P^T
-// buffer (its own, or the peer's by one bulk copy). At the end of a unit the row sums are
+// buffer (its own, or the peer's: bf16 by one bulk copy, FP8 by st.async). At the end of a unit the row sums are
 // exchanged the same way; with the FP8 cache the row factors 2^-e too, at its start.
 //
-// Pipeline per CTA (384 threads). Warp 0: producer — one ring of 32 KB slots in the order
-// the MMAs consume them (the key slots of tile n, then the value slots of tile n-1; a
-// unit's last value slots right after its last key slots), plus each unit's Q. A TMA load's
-// cost grows with the number of contiguous row pieces in its box (measured on this GPU:
-// about 22 GB/s per SM for 128-byte pieces from L2, 44 for 256, 87 for 512), so key boxes
-// take 256-byte pieces of each row (two 64-column bf16 chunks, or four E4M3 ones) and value
-// boxes four chunks. Every key and value load completes on the even CTA's barrier, which
+// Pipeline per CTA (384 threads). Warp 0: producer, plus each unit's Q. bf16: one ring of
+// 32 KB slots in the order the MMAs consume them (the key slots of tile n, then the value
+// slots of tile n-1; a unit's last value slots right after its last key slots). FP8: a key
+// tile of this CTA's 128 keys as whole 576-byte rows, loaded once the previous tile's QK^T
+// is done, and a ring of two 16 KB value blocks one tile behind, fed by one polling thread.
+// A TMA load's cost grows with the number of contiguous row pieces in its box (measured on
+// this GPU: about 22 GB/s per SM for 128-byte pieces from L2, 44 for 256, 87 for 512), so
+// bf16 key boxes take 256-byte pieces of each row (two 64-column chunks), E4M3 key boxes
+// whole rows, and value boxes four chunks. Every key and value load completes on the even CTA's barrier, which
 // the even CTA alone arms with the bytes of both CTAs (it knows which key halves its peer
 // loads), so that no load needs a cross-CTA arrival (each costs a fraction of a
 // microsecond). Warp 1 of the even CTA: the single MMA issuer, in program order QK^T(n),
