@@ -258,7 +258,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ uint8_t dsmem_raw[];
   __shared__ __align__(8) uint64_t bar_kfull[NK], bar_kempty[NK], bar_vfull[NV], bar_vempty[NV];
   __shared__ __align__(8) uint64_t bar_qfull, bar_qready, bar_qempty;
-  __shared__ __align__(8) uint64_t bar_kstage[NKS], bar_ksfree[NKS], bar_vstage[NVS], bar_vsempty[NVS];
+  __shared__ __align__(8) uint64_t bar_kstage[NKS], bar_ksfree[2 * NKS], bar_vstage[NVS], bar_vsempty[NVS];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_s_empty[2], bar_p_full[NP], bar_pv[NP];
   __shared__ __align__(8) uint64_t bar_o_empty, bar_drain[2], bar_vaux, bar_never;
   __shared__ uint32_t tmem_base_s;
@@ -295,7 +295,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   const uint32_t b_qempty = smem_u32(&bar_qempty);
   const uint32_t b_qsc = smem_u32(&bar_qsc), b_qfree = smem_u32(&bar_qfree);
   const uint32_t b_kstage = smem_u32(bar_kstage), b_vstage = smem_u32(bar_vstage);
-  const uint32_t b_ksfree = smem_u32(bar_ksfree);   // whole-row key stages: the tile's PV is done
+  // whole-row key stages: half h (keys 64 h ..) of stage s is free again at 2 s + h, once
+  // the tile's PV MMAs over those keys have completed
+  const uint32_t b_ksfree = smem_u32(bar_ksfree);
   const uint32_t b_vsempty = smem_u32(bar_vsempty);
   const uint32_t b_s_full = smem_u32(bar_s_full), b_s_empty = smem_u32(bar_s_empty);
   const uint32_t b_p_full = smem_u32(bar_p_full), b_pv = smem_u32(bar_pv);
@@ -319,7 +321,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
     mbar_init(b_qready, 4);
     for (int i = 0; i < NKS; ++i) {
       mbar_init(b_kstage + 8 * i, 1);
-      mbar_init(b_ksfree + 8 * i, 1);
+      mbar_init(b_ksfree + 8 * (2 * i), 1);
+      mbar_init(b_ksfree + 8 * (2 * i + 1), 1);
     }
     for (int i = 0; i < NVS; ++i) {
       mbar_init(b_vstage + 8 * i, 1);
@@ -568,7 +571,8 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
           const int valid = U.L - (U.tb + k) * kTileTokens;
           if constexpr (FP8 && C::kRawRows) {
             // the values are the first 8 chunks of the tile's whole-row key stage
-            // ([2 halves][8 groups][9 chunks][8 rows][64 B]), released when these complete
+            // ([2 halves][8 groups][9 chunks][8 rows][64 B]); each half is released once the
+            // MMAs of its two K steps complete (its keys' QK^T completed before P was ready)
             const int ksteps = valid >= kTileTokens ? 4 : (valid + 31) / 32;
             const uint32_t st = n % NKS;
             ok = wait(b_kstage + 8 * st, (n / NKS) & 1);
@@ -578,12 +582,15 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
             // N = 2 RC: P^T's cores hold hi (O^T columns 0 .. RC - 1) then lo (RC .. 2 RC - 1)
             const uint64_t bs = dP8s + (uint64_t)(pb * (C::kPBytes >> 4));
             // consecutive MMAs go to the four O^T tiles in turn (independent accumulators)
-            for (int kk = 0; kk < ksteps; ++kk)
+            for (int kk = 0; kk < ksteps; ++kk) {
 #pragma unroll
               for (int j = 0; j < kPairsPerTile; ++j)
                 umma_f8(tmem + C::kOBase + j * C::kNC, as + (uint64_t)((2 * j * 512 + kk * 4 * 9 * 512) >> 4),
                         bs + (uint64_t)((kk * 64 * RC) >> 4), idesc_pv8, !(k == 0 && kk == 0));
-            umma_commit(b_ksfree + 8 * st);
+              if (kk == 1) umma_commit(b_ksfree + 8 * (2 * st));
+            }
+            if (ksteps < 2) umma_commit(b_ksfree + 8 * (2 * st));
+            umma_commit(b_ksfree + 8 * (2 * st + 1));
           } else if constexpr (FP8) {
             const int ksteps = valid >= kTileTokens ? 4 : (valid + 31) / 32;
             const uint64_t bh = dP8 + (uint64_t)(pb * (C::kPBytes >> 4));
@@ -1117,8 +1124,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
   } else if (FP8 && C::kRawRows && warp == 2) {
     // ============================================================ FP8 whole-row key stages
     // Every tile's 128 key rows as two TMA boxes (one per 64-row page half) of all 9 chunks,
-    // into a stage once the PV MMAs of the tile that used it before have completed. The key
-    // group converts the stage into tensor memory, and the PV MMAs read its values. On a tile
+    // each half into a stage once the PV MMAs of the tile that used it before have completed
+    // over that half's keys. The QK^T MMAs read the stage's keys and the PV MMAs its values
+    // (the first 8 chunks of each row). On a tile
     // that ends inside a 32-key MMA step the warp loads the stage on its own barrier and
     // zeroes the rows from the sequence end to the end of that step (the cache may hold NaN
     // there, and 0 * NaN is NaN inside the MMA; those keys are masked) before it signals.
@@ -1131,14 +1139,16 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
       const int valid = it.U.L - it.tile * kTileTokens;
       const bool tail = valid < kTileTokens && (valid & 31) != 0;
       const uint32_t sl = p % NKS;
-      ok = wait_warp(b_ksfree + 8 * sl, ((p / NKS) & 1) ^ 1);
-      if (!ok) break;
       const uint32_t bar = tail ? b_vaux : b_kstage + 8 * sl, dst = sKS + sl * C::kKStageBytes;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar, it.boxes() * box_bytes);
-        for (int h = 0; h < 2; ++h)
+      for (int h = 0; h < 2 && ok; ++h) {
+        ok = wait_warp(b_ksfree + 8 * (2 * sl + h), ((p / NKS) & 1) ^ 1);
+        if (!ok) break;
+        if (lane == 0) {
+          if (h == 0) mbar_arrive_expect_tx(bar, it.boxes() * box_bytes);
           load_half<kSub>(it, a, h, &a.tm_k, dst + h * (C::kKStageBytes / 2), bar, 0, box_bytes);
+        }
       }
+      if (!ok) break;
       if (tail) {
         ok = wait_warp(b_vaux, aux & 1);
         ++aux;
