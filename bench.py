@@ -241,7 +241,9 @@ class ClockSampler:
 
 def roofline(case, kern_ms, flops, kv_bytes, q_bytes):
     """The decode kernel's roofline: the slower of the flops at the bf16 tensor peak and the
-    KV + Q bytes at the HBM copy bandwidth (both measured on this GPU model)."""
+    KV + Q bytes at the HBM copy bandwidth (both measured on this GPU model). With the FP8
+    cache the MMAs are E4M3 (twice the bf16 rate) but take q and P as two E4M3 terms each,
+    so the algorithmic flops at the bf16 peak equal the issued flops at the E4M3 peak."""
     peaks, peak_kind = load_peaks()
     t = kern_ms * 1e-3
     hbm_t = (kv_bytes + q_bytes) / (peaks["hbm_gbs"] * 1e9)
