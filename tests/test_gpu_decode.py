@@ -137,6 +137,11 @@ SMALL = [
     (2, 2, 16, 64, [300, 129], F8, False),           # 32 rows from s_q = 2, non-causal
     (2, 4, 4, 64, [700, 4], F8, True),               # 16 rows from s_q = 4, causal
     (3, 1, 32, 16, [1, 95, 300], F8, True),          # 16-row pages, 32 rows
+    (4, 1, 16, 64, [95, 96, 97, 191], F8, True),     # 32-key step edges inside a tile
+    (4, 1, 32, 128, [192, 193, 287, 288], F8, True), # the same, 32 rows
+    (3, 1, 16, 96, [250, 1000, 97], F8, True),       # P = 96: 32-row boxes
+    (2, 1, 16, 24, [300, 95], F8, True),             # P = 24: 8-row boxes
+    (2, 3, 8, 64, [96, 1000], F8, True),             # 24 rows from s_q = 3, causal
     (2, 2, 64, 64, [1000, 65], F8, True),            # 128 rows from s_q = 2
     (3, 1, 128, 16, [1, 255, 513], F8, True),        # pages smaller than a block
     (2, 1, 128, 24, [77, 1000], F8, True),
