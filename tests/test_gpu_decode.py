@@ -369,6 +369,23 @@ def test_bad_arguments_launch_nothing():
     assert e.value.status == -3
 
 
+# ----------------------------------------------------------- the longest sequence
+@pytest.mark.parametrize("H,P,kv", [(16, 64, BF), (128, 128, F8)])
+def test_the_longest_sequence_matches_the_oracle(H, P, kv):
+    """A sequence of 2^20 keys (the largest max_seq_len the library takes) beside a short
+    one: every row against the float64 oracle. The long stream is cut over every worker and
+    merged by the combine kernel."""
+    case = synth.make_case(B=2, s_q=1, H=H, page_size=P, seq_lens=[1 << 20, 300], seed=97 + H,
+                           kv_dtype=kv)
+    g = GpuCase(case)
+    out, lse = g.decode()
+    torch.cuda.synchronize()
+    st, bits = api.decode_check(g.workspace)
+    assert st == 0 and bits == 0
+    ro, rl = oracle_decode(case, g.cache_numpy())
+    compare(case, out, lse, ro, rl)
+
+
 # ---------------------------------------------------------------- full-size configs
 FULL = [(2, None, None), (3, None, None), (4, BF, None), (4, F8, None), (5, None, 1), (5, None, 4)]
 
