@@ -487,7 +487,7 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
             const uint64_t as = dKS + (uint64_t)(st * (C::kKStageBytes >> 4));
             // N = 2 RC: the 512-byte groups of 8 rows alternate hi and lo, so that S^T column
             // 16 g + i is row 8 g + i of K . hi and column 16 g + 8 + i the same row of K . lo
-#pragma unroll 1
+#pragma unroll
             for (int c = 0; c < 9; ++c) {
               const uint64_t bd = dQ8 + (uint64_t)(c * (RC * 128 >> 4));
 #pragma unroll
@@ -582,7 +582,9 @@ decode_kernel(const __grid_constant__ DecodeArgs a) {
             // N = 2 RC: P^T's cores hold hi (O^T columns 0 .. RC - 1) then lo (RC .. 2 RC - 1)
             const uint64_t bs = dP8s + (uint64_t)(pb * (C::kPBytes >> 4));
             // consecutive MMAs go to the four O^T tiles in turn (independent accumulators)
-            for (int kk = 0; kk < ksteps; ++kk) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              if (kk >= ksteps) break;
 #pragma unroll
               for (int j = 0; j < kPairsPerTile; ++j)
                 umma_f8(tmem + C::kOBase + j * C::kNC, as + (uint64_t)((2 * j * 512 + kk * 4 * 9 * 512) >> 4),

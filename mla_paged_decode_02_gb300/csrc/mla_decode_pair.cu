@@ -706,8 +706,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
               // P^T of block kb: key half kb / 2, keys 64 (kb % 2) .. of it; lo 8 KB after hi
               const uint64_t bd = dP0 + (uint64_t)(((kb >> 1) * 16384 + (kb & 1) * 4096) >> 4);
               // M-tile j: this CTA's value columns 128 j .. (its chunks 2j, 2j + 1)
+#pragma unroll
               for (int j = 0; j < 2; ++j)
-                for (int kk = 0; kk < ksteps; ++kk) {
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                  if (kk >= ksteps) break;
                   const uint64_t aj = ad + (uint64_t)((1024 * j + 8192 * kk) >> 4);
                   const uint64_t bk = bd + (uint64_t)((2048 * kk) >> 4);
                   umma_pair_f8(tmem + kOCol + 128 * j, aj, bk, idesc_pv, !(pv.first && kb == 0 && kk == 0));
@@ -730,10 +733,14 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
             tc_fence_after();
             const uint64_t ad = dV0 + (uint64_t)((slot * kSlotBytes) >> 4);
             const uint64_t bd = dP0 + (uint64_t)((64 * kb * 128) >> 4);
+#pragma unroll
             for (int j = 0; j < 2; ++j)
-              for (int kk = 0; kk < ksteps; ++kk)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                if (kk >= ksteps) break;
                 umma_pair_f16(tmem + kOCol + 128 * j, ad + (uint64_t)((2048 * j + 8192 * kk) >> 4), bd + kk * (2048 >> 4),
                               idesc_pv, !(pv.first && kb == 0 && kk == 0));
+              }
             umma_pair_commit(b_empty + 8 * slot);
             ++r;
           }
@@ -754,6 +761,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
               ok = ok && wait(b_ktfull, nkt & 1);
               if (!ok) break;
               tc_fence_after();
+#pragma unroll
               for (int c = 0; c < 9; ++c) {
                 const uint64_t bd = dQ0 + (uint64_t)(c * (q_chunk >> 4));
 #pragma unroll
@@ -773,7 +781,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
               if (!ok) break;
               tc_fence_after();
               const uint64_t ad = dK0 + (uint64_t)(slot * (kSlotBytes >> 4));
-              for (int cc = 0; cc < nc; ++cc) {
+#pragma unroll
+              for (int cc = 0; cc < KC; ++cc) {
+                if (cc >= nc) break;
                 const int c = KC * ks + cc;
                 const uint64_t bd = dQ0 + (uint64_t)(c * (q_chunk >> 4));
 #pragma unroll
