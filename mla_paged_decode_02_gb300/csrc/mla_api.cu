@@ -237,9 +237,10 @@ static mla_status decode_impl(const mla_decode_params* p, const void* q, const v
   sa.grid = grid;
   sa.tile = plan.tile;
   // a unit's set-up (its q, the pipeline's refill, its epilogue) is charged to the CTA that
-  // starts the stream, in tiles of streaming: measured best at 2 for CTA pairs and 4 for the
-  // FP8 cache with up to 64 rows; with bf16 and up to 64 rows a unit change costs little (0)
-  sa.setup = plan.pair ? 2 : fp8 ? 4 : 0;
+  // starts the stream, in tiles of streaming: measured best at 2 for bf16 CTA pairs, 3 for
+  // FP8 pairs and 4 for the FP8 cache with up to 64 rows; with bf16 and up to 64 rows a unit
+  // change costs little (0)
+  sa.setup = plan.pair ? (fp8 ? 3 : 2) : fp8 ? 4 : 0;
   sa.max_units = w.max_units;
   sa.max_split = w.max_split;
   sa.max_slots = w.max_slots;

@@ -88,9 +88,11 @@ def test_partition_is_exact_and_balanced(B, s_q, H, P, lens, kv):
     aligned = G > 1 and grid % G == 0
     cpg = grid // G if aligned else grid
     qs = lambda x: -(-(int(n_b.sum()) + B * x) // cpg) if aligned else -(-G * (int(n_b.sum()) + B * x) // grid)
-    # charged per stream: 2 for CTA pairs, 4 for the FP8 cache and 0 for bf16 up to 64 rows,
+    # charged per stream: 2 for bf16 CTA pairs, 3 for FP8 pairs, 4 for the FP8 cache and 0 for
+    # bf16 up to 64 rows,
     # dropped when a CTA's share would be at most twice that
-    want = 2 if R > 64 else (4 if case.kv_dtype == synth.KV_FP8_E4M3 else 0)
+    fp8 = case.kv_dtype == synth.KV_FP8_E4M3
+    want = (3 if fp8 else 2) if R > 64 else (4 if fp8 else 0)
     assert X == (want if qs(want) > 2 * want else 0)
     N = int(n_b.sum()) + B * X                       # positions of one row group
     W = G * N
