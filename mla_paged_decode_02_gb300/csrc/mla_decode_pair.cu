@@ -666,6 +666,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) decode_pair_kernel(const __gr
     } else if (warp == 1 && leader) {
       // ================================================================ MMA issuer (even CTA)
       if (lane == 0) {
+        // The MMA loops are fully unrolled (a partial block leaves early): this one thread
+        // issues every MMA of the pair, and its own instructions per MMA set their pace. The
+        // loops around them, which wait on barriers, stay rolled (their code would crowd the
+        // instruction cache the CTA's roles share).
         // operands bf16 (kind::f16), or E4M3 (kind::f8f6f4: format code 0 is E4M3 there)
         const uint32_t idesc_qk = make_idesc(256, 128, FP8 ? 0u : 1u, 0, 0);
         const uint32_t idesc_pv = make_idesc(256, 128, FP8 ? 0u : 1u, 1, 1);
